@@ -1,0 +1,69 @@
+// Plan object and launch parameters shared by the library's translation
+// units (host + device).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dma.h"
+
+namespace dma {
+
+constexpr int kTileM = 128;  // query rows per tile (positions x heads of a group)
+constexpr int kTileN = 128;  // key positions per tile
+constexpr uint32_t kPartialBit = 0x80000000u;
+constexpr uint32_t kIndexMask = 0x7FFFFFFFu;
+
+// Device-visible shape and workspace pointers of one rank's plan.
+struct PlanDev {
+  int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
+  int chunk, local_len, group, tile_pos, n_qtiles, n_ktiles;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  uint64_t timeout_ns;
+  uint32_t* status;
+  int32_t* qpos;      // [Lq]
+  int32_t* doc_lo;    // [B][Lq]
+  int32_t* chunk_order;
+  uint8_t* tile_class;  // [B][nQt][nKt]
+  int32_t* row_cnt;   // [B*nQt]
+  int32_t* row_ptr;   // [B*nQt + 1]
+  int32_t* row_idx;   // [B*nQt*nKt]
+  int32_t* col_cnt;   // [B*nKt]
+  int32_t* col_ptr;   // [B*nKt + 1]
+  int32_t* col_idx;   // [B*nQt*nKt]
+  int32_t* fwd_order; // [B*nQt]
+  int32_t* bwd_order; // [B*nKt]
+  float* delta;       // [B][Hq][Lq]
+};
+
+struct WorkspaceLayout {
+  size_t status, qpos, doc_lo, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
+      col_ptr, col_idx, fwd_order, bwd_order, delta, total;
+};
+
+}  // namespace dma
+
+struct dma_plan_s {
+  dma::PlanDev d;
+  int device;
+  int num_sms;
+  const int32_t* cu;  // only read while the plan kernels run
+  int n_docs;
+};
+
+namespace dma {
+// Launchers implemented in the .cu files (host side).
+cudaError_t launch_plan_kernels(const dma_plan_s& p, cudaStream_t s);
+cudaError_t launch_cp_copy(const dma_plan_s& p, const void* src, void* dst, size_t row_bytes,
+                           bool gather, cudaStream_t s);
+cudaError_t launch_fwd(const dma_plan_s& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, dma_bf16* o, float* lse, cudaStream_t s);
+cudaError_t launch_bwd(const dma_plan_s& p, const dma_bf16* o, const dma_bf16* dout,
+                       const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tlse,
+                       const CUtensorMap& tdelta, dma_bf16* dq, float* dk, float* dv,
+                       cudaStream_t s);
+cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
+}  // namespace dma

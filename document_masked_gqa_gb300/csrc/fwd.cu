@@ -1,0 +1,377 @@
+// Forward kernel: causal + document-masked GQA attention for one CP rank.
+//
+// One CTA per (query tile, K/V head).  A query tile is 128 rows: P = 128/g
+// consecutive local positions x the g query heads sharing K/V head `kvh`
+// (GQA, "The Llama 3 Herd of Models - part 3/16", 3.3.2, and "Paper notes:
+// The Llama 3 Herd of Models", 8 key-value heads), so one K/V tile feeds g
+// heads at once.  The CTA walks the tile's list of non-skipped key tiles
+// (built by the block-mask builder) and keeps the online-softmax running max
+// and sum per row, rescaling the partial output, then divides by the sum
+// ("Training Infrastructure and Systems", "FlashAttention: never write the
+// score matrix", sections "Online softmax" and "Tiling").
+//
+// GB300 mapping (sm_103a):
+//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring
+//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers,
+//               O += P V into a TMEM accumulator; owns the TMEM allocation
+//   warps 2-3   load the tile's positions / document starts, then idle
+//   warps 4-7   softmax: thread r owns row r (TMEM lane r): masks partial
+//               tiles, exponentiates in base 2, writes P (bf16) to shared
+//               memory in the 128-byte-swizzled K-major layout, rescales O in
+//               TMEM when its reference max moves, and writes O and LSE.
+// The reference max only moves when a row's max grows by more than 2^8, so
+// most tiles need no rescale of O; the final O / l is exact either way.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dma {
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (bf16)
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kPBytes = 128 * 128 * 2;
+  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+};
+
+// Wait for a phase ignoring the abort flag, bounded by limit_ns (used only to
+// drain this CTA's own copies before it exits after an abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const PlanDev p,
+               __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  using Cfg = FwdCfg<D>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  {  // a failed plan or an earlier expired wait: do nothing (CTA-uniform)
+    __shared__ uint32_t s_status;
+    if (threadIdx.x == 0) s_status = *reinterpret_cast<volatile uint32_t*>(p.status);
+    __syncthreads();
+    if (s_status != 0u) return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
+  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  const int bq = p.fwd_order[ord];
+  const int b = bq / p.n_qtiles, qt = bq % p.n_qtiles;
+  const int l0 = qt * P;
+  const int rp0 = p.row_ptr[bq];
+  const int n = p.row_ptr[bq + 1] - rp0;
+  const int32_t* list = p.row_idx + rp0;
+
+  uint8_t* sQ = smem + Cfg::kQ;
+  uint8_t* sK = smem + Cfg::kK;
+  uint8_t* sV = smem + Cfg::kV;
+  uint8_t* sP = smem + Cfg::kP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + S;
+  uint64_t* v_full = k_empty + S;
+  uint64_t* v_empty = v_full + S;
+  uint64_t* s_full = v_empty + S;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* o_done = p_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
+  int* s_qpos = reinterpret_cast<int*>(smem + Cfg::kMisc + 16);
+  int* s_lo = s_qpos + 128;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2 || warp == 3) {
+    for (int r = threadIdx.x - 64; r < P; r += 64) {
+      s_qpos[r] = p.qpos[l0 + r];
+      s_lo[r] = p.doc_lo[static_cast<long long>(b) * Lq + l0 + r];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      int last_phase_k[S], last_phase_v[S];
+#pragma unroll
+      for (int i = 0; i < S; ++i) last_phase_k[i] = last_phase_v[i] = -1;
+      mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < Cfg::kChunks; ++c)
+        tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % S;
+        const uint32_t ph = (j / S) & 1;
+        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
+        const int krow = b * p.seq_len + kt * kTileN;
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[st], Cfg::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_2d(sK + st * Cfg::kTileBytes + c * Cfg::kRegion, &tk, &k_full[st],
+                      kvh * D + c * 64, krow);
+        last_phase_k[st] = static_cast<int>(ph);
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[st], Cfg::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_2d(sV + st * Cfg::kTileBytes + c * Cfg::kRegion, &tv, &v_full[st],
+                      kvh * D + c * 64, krow);
+        last_phase_v[st] = static_cast<int>(ph);
+      }
+      if (!ok) {  // drain our own copies before the CTA exits
+        drain_wait(q_full, 0, 100000000ull);
+        for (int i = 0; i < S; ++i) {
+          if (last_phase_k[i] >= 0) drain_wait(&k_full[i], last_phase_k[i], 100000000ull);
+          if (last_phase_v[i] >= 0) drain_wait(&v_full[i], last_phase_v[i], 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = mbar_wait(q_full, 0, ctl);
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i % S;
+        const uint32_t ph = (i / S) & 1;
+        if (!mbar_wait(p_full, i & 1, ctl)) return false;
+        if (!mbar_wait(&v_full[st], ph, ctl)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint64_t a =
+              sdesc_sw128(p_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemO, a, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(&v_empty[st]);
+        last_commit = o_done;
+        last_parity = i & 1;
+        return true;
+      };
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j % S;
+        const uint32_t ph = (j / S) & 1;
+        const int sb = j & 1;
+        if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
+        if (!mbar_wait(&s_free[sb], ((j >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTileBytes);
+        const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(d_s, sdesc_sw128(q_addr + off, 16, 1024),
+                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[sb]);
+        mma_commit(&k_empty[st]);
+        last_commit = &s_full[sb];
+        last_parity = (j >> 1) & 1;
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && n > 0) ok = issue_pv(n - 1);
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int lg = 31 - __clz(g);
+    const int pos = r >> lg, h = r & (g - 1);
+    const int qabs = s_qpos[pos], lo_r = s_lo[pos];
+    const float sl2 = p.scale_log2;
+    const uint32_t p_addr = smem_u32(sP);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, ctl))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+      const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+      tmem_ld32(sc, s);
+      tmem_ld32(sc + 32, s + 32);
+      tmem_ld32(sc + 64, s + 64);
+      tmem_ld32(sc + 96, s + 96);
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+      const uint32_t e = static_cast<uint32_t>(list[j]);
+      if (e & kPartialBit) {
+        const int k0 = static_cast<int>(e & kIndexMask) * kTileN;
+        const int lo_c = lo_r - k0, hi_c = qabs - k0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < lo_c || c > hi_c) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float mxl2 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
+      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(m_run - m_ref);
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        s[c] = ex2(fmaf(s[c], sl2, -m_ref));
+        s[c + 1] = ex2(fmaf(s[c + 1], sl2, -m_ref));
+        sum0 += s[c];
+        sum1 += s[c + 1];
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      if (j >= 1) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, ctl))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // P row r -> shared memory, 128-byte swizzle, K-major, two 64-key regions
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint32_t addr = p_addr + (ch >> 3) * Cfg::kRegion + r * 128 +
+                              ((((ch & 7) ^ (r & 7))) << 4);
+        st_shared_v4(addr, pack_bf16(s[8 * ch], s[8 * ch + 1]),
+                     pack_bf16(s[8 * ch + 2], s[8 * ch + 3]),
+                     pack_bf16(s[8 * ch + 4], s[8 * ch + 5]),
+                     pack_bf16(s[8 * ch + 6], s[8 * ch + 7]));
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float t[32];
+          const uint32_t oc = tmem + lane_base + Cfg::kTmemO + c0;
+          tmem_ld32(oc, t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[i] *= alpha;
+          tmem_st32(oc, t);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      m_run = m_new;
+    }
+    if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, ctl))) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const int hq = kvh * g + h;
+      const long long row = static_cast<long long>(b) * Lq + l0 + pos;
+      uint4* dst = reinterpret_cast<uint4*>(o + (row * p.n_heads + hq) * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float t[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemO + c0, t);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 u;
+          u.x = pack_bf16(t[8 * q4 + 0] * inv, t[8 * q4 + 1] * inv);
+          u.y = pack_bf16(t[8 * q4 + 2] * inv, t[8 * q4 + 3] * inv);
+          u.z = pack_bf16(t[8 * q4 + 4] * inv, t[8 * q4 + 5] * inv);
+          u.w = pack_bf16(t[8 * q4 + 6] * inv, t[8 * q4 + 7] * inv);
+          dst[c0 / 8 + q4] = u;
+        }
+      }
+      lse[(static_cast<long long>(b) * p.n_heads + hq) * Lq + l0 + pos] =
+          (m_run + lg2(l_run)) * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, dma_bf16* o, float* lse, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const int grid = p.batch * p.n_qtiles * p.n_kv_heads;
+  if (grid == 0) return cudaSuccess;
+  const int smem = FwdCfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  fwd_kernel<D><<<grid, 256, smem, s>>>(tq, tk, tv, p, reinterpret_cast<__nv_bfloat16*>(o), lse);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const dma_plan_s& pl, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, dma_bf16* o, float* lse, cudaStream_t s) {
+  if (pl.d.head_dim == 128) return launch_fwd_d<128>(pl, tq, tk, tv, o, lse, s);
+  return launch_fwd_d<64>(pl, tq, tk, tv, o, lse, s);
+}
+
+}  // namespace dma

@@ -1,0 +1,274 @@
+// Context-parallel shard planner and block-mask builder.
+//
+// Planner: the query-position map of a rank holding chunks i and 2*CP-1-i
+// ("The Llama 3 Herd of Models - part 3/16", 3.3.2, "Context parallelism for
+// long sequences"), the document start of each local query from the whole
+// sequence's document boundaries (review of "Scaling Llama 3 Training with
+// Efficient Parallelism Strategies", CP integration: every rank sees the
+// full sequence's document information), and validation of cu_doc_lens.
+//
+// Block-mask builder: for each (query tile, key tile) the class skip / full /
+// partial under the causal + document mask.  A query tile covers P = 128/g
+// consecutive local positions (never straddling the rank's two chunks, so
+// positions are consecutive), whose allowed key ranges are [lo(p), p] with
+// both ends non-decreasing in p.  The tile pair is
+//   skip    iff no row's range meets [k0, k1],
+//   full    iff every row's range contains [k0, k1],
+//   partial otherwise,
+// then row lists (per query tile, ascending key tiles), column lists (per key
+// tile, ascending query tiles) and longest-first launch orders.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dma {
+
+namespace {
+
+__global__ void plan_positions_kernel(PlanDev p, const int32_t* __restrict__ cu, int n_docs) {
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthreads = gridDim.x * blockDim.x;
+  const int C = p.chunk, Lq = p.local_len, S = p.seq_len;
+  const long long total = static_cast<long long>(p.batch) * S;
+
+  // --- validation of the document table
+  for (int i = tid; i < n_docs; i += nthreads) {
+    if (cu[i + 1] <= cu[i]) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_BAD_DOCS));
+  }
+  if (tid == 0) {
+    if (cu[0] != 0 || static_cast<long long>(cu[n_docs]) != total)
+      atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_BAD_DOCS));
+  }
+  for (int b = tid + 1; b < p.batch; b += nthreads) {
+    // every sample boundary b*S must be a document boundary
+    const long long want = static_cast<long long>(b) * S;
+    int lo = 0, hi = n_docs;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= want) lo = mid; else hi = mid - 1;
+    }
+    if (cu[lo] != want) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_BAD_DOCS));
+  }
+
+  // --- chunk order (rank-major) and position map
+  for (int j = tid; j < 2 * p.cp_size; j += nthreads)
+    p.chunk_order[j] = (j & 1) ? (2 * p.cp_size - 1 - (j >> 1)) : (j >> 1);
+  const int ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
+  for (int l = tid; l < Lq; l += nthreads) p.qpos[l] = (l < C) ? (ca * C + l) : (cb * C + (l - C));
+
+  // --- document start of every local query of every sample
+  const long long n = static_cast<long long>(p.batch) * Lq;
+  for (long long i = tid; i < n; i += nthreads) {
+    const int b = static_cast<int>(i / Lq);
+    const int l = static_cast<int>(i % Lq);
+    const int pos = (l < C) ? (ca * C + l) : (cb * C + (l - C));
+    const long long g = static_cast<long long>(b) * S + pos;
+    int lo = 0, hi = n_docs - 1;  // last d with cu[d] <= g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    long long start = static_cast<long long>(cu[lo]) - static_cast<long long>(b) * S;
+    // keep indices in range even for a malformed table (the status is set)
+    if (start < 0) start = 0;
+    if (start > pos) start = pos;
+    p.doc_lo[i] = static_cast<int32_t>(start);
+  }
+}
+
+// grid (n_qtiles, batch), block 128
+__global__ void mask_classify_kernel(PlanDev p) {
+  __shared__ int s_q[kTileM], s_lo[kTileM];
+  __shared__ int s_cnt;
+  const int t = blockIdx.x, b = blockIdx.y;
+  const int P = p.tile_pos;
+  const int l0 = t * P;
+  if (threadIdx.x == 0) s_cnt = 0;
+  for (int r = threadIdx.x; r < P; r += blockDim.x) {
+    s_q[r] = p.qpos[l0 + r];
+    s_lo[r] = p.doc_lo[static_cast<long long>(b) * p.local_len + l0 + r];
+  }
+  __syncthreads();
+  const int q_min = s_q[0], lo_max = s_lo[P - 1];
+  int cnt = 0;
+  uint8_t* cls_row = p.tile_class + (static_cast<long long>(b) * p.n_qtiles + t) * p.n_ktiles;
+  for (int kt = threadIdx.x; kt < p.n_ktiles; kt += blockDim.x) {
+    const int k0 = kt * kTileN, k1 = k0 + kTileN - 1;
+    bool any = false;
+    for (int r = 0; r < P && !any; ++r) any = (s_lo[r] <= k1) && (s_q[r] >= k0);
+    uint8_t c = DMA_TILE_SKIP;
+    if (any) c = (lo_max <= k0 && k1 <= q_min) ? DMA_TILE_FULL : DMA_TILE_PARTIAL;
+    cls_row[kt] = c;
+    if (c != DMA_TILE_SKIP) {
+      ++cnt;
+      atomicAdd(&p.col_cnt[b * p.n_ktiles + kt], 1);
+    }
+  }
+  atomicAdd(&s_cnt, cnt);
+  __syncthreads();
+  if (threadIdx.x == 0) p.row_cnt[b * p.n_qtiles + t] = s_cnt;
+}
+
+// Block-wide exclusive scan helper (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_tmp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = (lane < (blockDim.x >> 5)) ? s_tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_tmp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int warp_prefix = (wid > 0) ? s_tmp[wid - 1] : 0;
+  const int incl = x + warp_prefix;
+  *total = s_tmp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return incl - v;
+}
+
+// one block of 1024: exclusive scans of the row and column counts
+__global__ void scan_kernel(PlanDev p) {
+  __shared__ int s_tmp[32];
+  for (int which = 0; which < 2; ++which) {
+    const int n = which == 0 ? p.batch * p.n_qtiles : p.batch * p.n_ktiles;
+    const int32_t* cnt = which == 0 ? p.row_cnt : p.col_cnt;
+    int32_t* ptr = which == 0 ? p.row_ptr : p.col_ptr;
+    int carry = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const int v = (i < n) ? cnt[i] : 0;
+      int tot;
+      const int ex = block_exclusive_scan(v, s_tmp, &tot);
+      if (i < n) ptr[i] = carry + ex;
+      carry += tot;
+    }
+    if (threadIdx.x == 0) ptr[n] = carry;
+    __syncthreads();
+  }
+}
+
+// grid (n_qtiles, batch) for rows or (n_ktiles, batch) for columns; block 1024
+__global__ void fill_lists_kernel(PlanDev p, int columns) {
+  __shared__ int s_tmp[32];
+  const int line = blockIdx.x, b = blockIdx.y;
+  const int n = columns ? p.n_qtiles : p.n_ktiles;
+  const long long stride = columns ? p.n_ktiles : 1;
+  const uint8_t* base =
+      columns ? p.tile_class + static_cast<long long>(b) * p.n_qtiles * p.n_ktiles + line
+              : p.tile_class + (static_cast<long long>(b) * p.n_qtiles + line) * p.n_ktiles;
+  const int list = columns ? b * p.n_ktiles + line : b * p.n_qtiles + line;
+  int32_t* out = columns ? p.col_idx + p.col_ptr[list] : p.row_idx + p.row_ptr[list];
+  int carry = 0;
+  for (int s0 = 0; s0 < n; s0 += blockDim.x) {
+    const int i = s0 + threadIdx.x;
+    const uint8_t c = (i < n) ? base[i * stride] : static_cast<uint8_t>(DMA_TILE_SKIP);
+    const int flag = c != DMA_TILE_SKIP;
+    int tot;
+    const int ex = block_exclusive_scan(flag, s_tmp, &tot);
+    if (flag)
+      out[carry + ex] = static_cast<int32_t>(static_cast<uint32_t>(i) |
+                                             (c == DMA_TILE_PARTIAL ? kPartialBit : 0u));
+    carry += tot;
+  }
+}
+
+// Longest-first order: position of unit u = #units with larger count +
+// #units with equal count and smaller index.
+__global__ void order_kernel(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ order) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= n) return;
+  const int c = cnt[u];
+  int pos = 0;
+  for (int j = 0; j < n; ++j) {
+    const int cj = cnt[j];
+    pos += (cj > c) || (cj == c && j < u);
+  }
+  order[pos] = u;
+}
+
+// Row copy between full-sequence and local layouts.  One block per row.
+__global__ void cp_copy_kernel(PlanDev p, const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                               size_t row_bytes, int gather) {
+  const long long row = blockIdx.x;  // b*Lq + l
+  const int b = static_cast<int>(row / p.local_len);
+  const int l = static_cast<int>(row % p.local_len);
+  const long long full_row = static_cast<long long>(b) * p.seq_len + p.qpos[l];
+  const uint8_t* s = src + (gather ? full_row : row) * row_bytes;
+  uint8_t* d = dst + (gather ? row : full_row) * row_bytes;
+  if ((row_bytes & 15) == 0 && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(s);
+    uint4* d4 = reinterpret_cast<uint4*>(d);
+    for (size_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) d4[i] = s4[i];
+  } else {
+    for (size_t i = threadIdx.x; i < row_bytes; i += blockDim.x) d[i] = s[i];
+  }
+}
+
+__global__ void wait_probe_kernel(uint64_t timeout_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  WaitCtl ctl{&abort_flag, status, timeout_ns};
+  // Phase 0 of this barrier never completes: nothing arrives on it.  The
+  // bounded wait gives up after timeout_ns and records DMA_ERR_TIMEOUT.
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0u, ctl);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t) * 4, s);
+  if (e != cudaSuccess) return e;
+  if (p.batch == 0) return cudaSuccess;
+  e = cudaMemsetAsync(p.col_cnt, 0, sizeof(int32_t) * p.batch * p.n_ktiles, s);
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(p.batch) * p.local_len;
+  int blocks = static_cast<int>((n + 255) / 256);
+  if (blocks > 4 * pl.num_sms) blocks = 4 * pl.num_sms;
+  if (blocks < 1) blocks = 1;
+  plan_positions_kernel<<<blocks, 256, 0, s>>>(p, pl.cu, pl.n_docs);
+  mask_classify_kernel<<<dim3(p.n_qtiles, p.batch), 128, 0, s>>>(p);
+  scan_kernel<<<1, 1024, 0, s>>>(p);
+  fill_lists_kernel<<<dim3(p.n_qtiles, p.batch), 1024, 0, s>>>(p, 0);
+  fill_lists_kernel<<<dim3(p.n_ktiles, p.batch), 1024, 0, s>>>(p, 1);
+  const int nq = p.batch * p.n_qtiles, nk = p.batch * p.n_ktiles;
+  order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
+  order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cp_copy(const dma_plan_s& pl, const void* src, void* dst, size_t row_bytes,
+                           bool gather, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const long long rows = static_cast<long long>(p.batch) * p.local_len;
+  if (rows == 0) return cudaSuccess;
+  cp_copy_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
+      p, static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), row_bytes, gather ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(timeout_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dma

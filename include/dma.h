@@ -1,0 +1,220 @@
+/*
+ * dma.h - causal + document-masked grouped-query attention for one
+ * context-parallel rank, on NVIDIA GB300 (sm_103a).
+ *
+ * The problem (as the Llama 3 infrastructure pages state it):
+ *   - "The Llama 3 Herd of Models - part 3/16", section 3.3.2, "Context
+ *     parallelism for long sequences": the sequence is cut into 2*CP equal
+ *     chunks, rank i holds chunks i and 2*CP-1-i; K and V are all-gathered
+ *     and attention is computed for the local queries against the full K/V,
+ *     under the full causal mask; K/V are small thanks to GQA.
+ *   - "Paper notes: The Llama 3 Herd of Models", "Two architectural
+ *     choices": GQA with 8 key-value heads; document masking keeps attention
+ *     inside a document.
+ *   - review of "Scaling Llama 3 Training with Efficient Parallelism
+ *     Strategies", section "Context Parallelism (CP)": every CP rank receives
+ *     the whole sequence's document information to build its mask.
+ *   - "Training Infrastructure and Systems", "FlashAttention: never write the
+ *     score matrix" ("Online softmax", "Tiling"): the blocked forward keeps a
+ *     running max and sum, writes O and per-row statistics, and the backward
+ *     recomputes the scores.
+ *
+ * Query at global position p may attend key k iff doc_start(p) <= k <= p.
+ * Query head h uses K/V head h / (n_heads / n_kv_heads) (contiguous groups).
+ *
+ * Tensor layouts (all row-major, contiguous, device memory):
+ *   q, o, dout, dq : [batch][2*C][n_heads][head_dim]   bf16, this rank's rows
+ *                    in local order: chunk cp_rank first, then chunk
+ *                    2*cp_size-1-cp_rank (C = seq_len / (2*cp_size)).
+ *   k, v           : [batch][seq_len][n_kv_heads][head_dim] bf16, the full
+ *                    gathered sequence in natural position order.
+ *   lse            : [batch][n_heads][2*C] fp32, natural log of the sum of
+ *                    exp of the scaled, masked logits of each query row.
+ *   dk, dv         : [batch][seq_len][n_kv_heads][head_dim] fp32: this rank's
+ *                    partial gradients (only its own query rows contribute);
+ *                    summing them over all ranks gives the full gradients.
+ *                    Every element is written (zeros where no local query
+ *                    attends).
+ *   cu_doc_lens    : int32 [n_docs + 1] cumulative document offsets over the
+ *                    flattened batch*seq_len token stream: cu[0] = 0,
+ *                    strictly increasing, cu[n_docs] = batch*seq_len, and
+ *                    every sample boundary b*seq_len present.
+ *
+ * Ownership: every device buffer (tensors, cu_doc_lens, the plan workspace)
+ * belongs to the caller.  The library never allocates device memory.  The
+ * plan handle itself is a small host object created by dma_plan and freed by
+ * dma_plan_destroy; it points into the caller's workspace, which must stay
+ * valid (and untouched) until the plan is destroyed.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).  Nothing synchronizes except dma_plan_check and
+ * dma_debug_wait_probe.
+ *
+ * Errors: arguments the host can check are rejected before any launch with
+ * DMA_ERR_INVALID_ARG / DMA_ERR_UNSUPPORTED / DMA_ERR_WORKSPACE.  Problems only
+ * the device can see (malformed cu_doc_lens, an expired bounded wait) are
+ * recorded in a status word in the workspace and returned by dma_plan_check;
+ * kernels launched on a plan whose status is set do no work.  No call aborts
+ * or traps.
+ */
+#ifndef DMA_H_
+#define DMA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DMA_OK = 0,
+  DMA_ERR_INVALID_ARG = 1, /* null pointer, negative size, rank out of range */
+  DMA_ERR_BAD_DOCS = 2,    /* cu_doc_lens violates its contract (device) */
+  DMA_ERR_UNSUPPORTED = 3, /* shape outside the supported set, or not sm_103 */
+  DMA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
+  DMA_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired */
+  DMA_ERR_WORKSPACE = 6    /* workspace too small or misaligned */
+} dma_status;
+
+/* bf16 values are passed as raw 16-bit patterns. */
+typedef uint16_t dma_bf16;
+
+/* Tile classes (one byte per pair of query tile and key tile). */
+enum { DMA_TILE_SKIP = 0, DMA_TILE_FULL = 1, DMA_TILE_PARTIAL = 2 };
+
+typedef struct dma_plan_s* dma_plan_t;
+
+/*
+ * Bytes of device workspace dma_plan needs for this shape (256-byte aligned
+ * base required).  Returns 0 for an unsupported or invalid shape.
+ * max_docs is accepted for interface stability and does not change the size.
+ */
+size_t dma_plan_workspace_bytes(int batch, int seq_len, int cp_size,
+                                int n_heads, int n_kv_heads, int head_dim,
+                                int max_docs);
+
+/*
+ * Build the rank's plan: the context-parallel query-position map (part 3/16,
+ * 3.3.2: chunks i and 2*CP-1-i), the document start of every local query,
+ * the rank-major chunk order, and the classification of every pair of query
+ * tile and key tile as skip / full / partial with its row and column lists.
+ *
+ * Supported shapes: cp_size >= 1; 0 <= cp_rank < cp_size; batch >= 0
+ * (batch 0 builds an empty plan whose calls do nothing); seq_len divisible
+ * by 2*cp_size with chunk C = seq_len/(2*cp_size) a multiple of 64;
+ * g = n_heads/n_kv_heads in {1,2,4,8,16} with C a multiple of 128/g;
+ * head_dim in {64, 128}.  A query tile is 128 rows = 128/g positions x g
+ * heads of one K/V group; a key tile is 128 positions.
+ *
+ * softmax_scale <= 0 selects 1/sqrt(head_dim).
+ * cu_doc_lens (device) is read only by kernels this call enqueues; it may be
+ * freed once they complete.  The returned handle is valid on success only.
+ * Device: the current CUDA device must be compute capability 10.3.
+ */
+dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch,
+                    int seq_len, int cp_size, int cp_rank, int n_heads,
+                    int n_kv_heads, int head_dim, float softmax_scale,
+                    void* workspace, size_t workspace_bytes, void* stream,
+                    dma_plan_t* out);
+
+/*
+ * Forward: o = softmax(scale * q k^T + mask) v and the row log-sum-exp.
+ * One persistent-style launch; pairs of tiles classified skip issue no work.
+ */
+dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                        const dma_bf16* v, dma_bf16* o, float* lse,
+                        void* stream);
+
+/*
+ * Backward: dq (bf16), and this rank's partial dk, dv (fp32), given the
+ * forward's o and lse and the upstream gradient dout.  Three launches:
+ * Delta = rowsum(dout * o) into the plan workspace, a key-stationary dK/dV
+ * kernel reduced over the group's query heads, and a query-stationary dQ
+ * kernel.  dk and dv are fully overwritten.
+ */
+dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                        const dma_bf16* v, const dma_bf16* o, const float* lse,
+                        const dma_bf16* dout, dma_bf16* dq, float* dk,
+                        float* dv, void* stream);
+
+/* Synchronize `stream` and return the plan's device status word
+ * (DMA_OK, DMA_ERR_BAD_DOCS or DMA_ERR_TIMEOUT) or DMA_ERR_CUDA. */
+dma_status dma_plan_check(dma_plan_t plan, void* stream);
+
+/* Free the host handle (the caller's workspace is untouched). NULL is ok. */
+dma_status dma_plan_destroy(dma_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+const char* dma_status_str(dma_status s);
+
+/*
+ * Cut this rank's rows out of a full-sequence tensor, and put them back:
+ *   full  : [batch][seq_len][H][elem_bytes-sized elements x row_elems]
+ *   local : [batch][2*C][...] in the plan's local order.
+ * row_bytes = bytes of one position (H * head_dim * element size).
+ * Bit-exact copies; used to emulate the sharding on one device.
+ */
+dma_status dma_cp_gather(dma_plan_t plan, const void* full, void* local,
+                         size_t row_bytes, void* stream);
+dma_status dma_cp_scatter(dma_plan_t plan, const void* local, void* full,
+                          size_t row_bytes, void* stream);
+
+/*
+ * Read-only view of the plan's device arrays (for tests and tools).
+ * All pointers are device pointers into the caller's workspace.
+ *   qpos      int32 [2C]             global position of each local row
+ *   doc_lo    int32 [batch][2C]      first position of that row's document
+ *   chunk_order int32 [2*cp_size]    rank-major chunk order
+ *   tile_class uint8 [batch][n_qtiles][n_ktiles]
+ *   row_ptr   int32 [batch*n_qtiles + 1], row_idx int32 [nnz]:
+ *             ascending non-skip key tiles of each query tile; bit 31 set
+ *             when the pair is partial.
+ *   col_ptr   int32 [batch*n_ktiles + 1], col_idx int32 [nnz]: the same by
+ *             key tile (query-tile indices, bit 31 = partial).
+ *   fwd_order int32 [batch*n_qtiles]: query tiles (b*n_qtiles + t) by
+ *             non-increasing list length, ties by index.
+ *   bwd_order int32 [batch*n_ktiles]: key tiles likewise.
+ */
+typedef struct {
+  int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
+  int chunk, local_len, group, q_tile_positions, n_qtiles, n_ktiles;
+  float softmax_scale;
+  const int32_t* qpos;
+  const int32_t* doc_lo;
+  const int32_t* chunk_order;
+  const uint8_t* tile_class;
+  const int32_t* row_ptr;
+  const int32_t* row_idx;
+  const int32_t* col_ptr;
+  const int32_t* col_idx;
+  const int32_t* fwd_order;
+  const int32_t* bwd_order;
+  const uint32_t* status;
+} dma_plan_view;
+
+dma_status dma_plan_get_view(dma_plan_t plan, dma_plan_view* out);
+
+/*
+ * Bounded device waits: every spin on a barrier gives up after this many
+ * nanoseconds, records DMA_ERR_TIMEOUT in the status word, drains its own
+ * copies, frees its tensor memory and returns.  Default 2e9 (2 s); the
+ * environment variable DMA_WAIT_TIMEOUT_NS overrides the default at dma_plan.
+ */
+dma_status dma_plan_set_wait_timeout(dma_plan_t plan, uint64_t timeout_ns);
+
+/*
+ * Test hook for the failure path: launch one block that waits, bounded by
+ * timeout_ns, on a shared-memory barrier nothing will ever arrive on.  It
+ * writes DMA_ERR_TIMEOUT into *status_dev (device uint32) when the wait
+ * expires.  Synchronizes `stream`, and returns the recorded status (or
+ * DMA_ERR_CUDA).  Nothing faults or hangs: the kernel returns after the limit.
+ */
+dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMA_H_ */
