@@ -121,16 +121,6 @@ dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p) {
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Row statistics [B*Hq][Lq] fp32; box = P positions x g heads.
-dma_status map_rowstat(CUtensorMap* m, const void* base, const dma::PlanDev& p) {
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.local_len),
-                              static_cast<cuuint64_t>(p.batch) * p.n_heads};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.local_len) * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.tile_pos), static_cast<cuuint32_t>(p.group)};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 dma_status check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
@@ -251,16 +241,14 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return DMA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv, tdo, tlse, tdelta;
+  CUtensorMap tq, tk, tv, tdo;
   dma_status st;
   const int rows = p.batch * p.local_len;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  if ((st = map_rowstat(&tlse, lse, p)) != DMA_OK) return st;
-  if ((st = map_rowstat(&tdelta, p.delta, p)) != DMA_OK) return st;
-  return dma::launch_bwd(*plan, o, dout, lse, tq, tk, tv, tdo, tlse, tdelta, dq, dk, dv,
+  return dma::launch_bwd(*plan, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;

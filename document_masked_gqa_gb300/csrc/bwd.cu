@@ -1,11 +1,786 @@
-// Backward kernels (placeholder until the dK/dV and dQ kernels land).
+// Backward kernels: causal + document-masked GQA attention for one CP rank.
+//
+// The backward recomputes the scores from Q, K and the forward's row
+// log-sum-exp instead of storing them ("Training Infrastructure and
+// Systems", "FlashAttention: never write the score matrix", "Tiling": the
+// backward recomputes the scores).  With P = exp(scale*S - LSE):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - Delta),  Delta = rowsum(dO*O),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+// dK and dV are this rank's partial sums (its own query rows only), kept in
+// fp32 ("The Llama 3 Herd of Models - part 3/16", 3.3.2 "Numerical
+// stability": gradients accumulated and reduce-scattered in FP32).
+//
+// Three launches:
+//   delta_kernel  Delta[b, h, l] = sum_d dO * O (HBM-bound, one pass).
+//   dkdv_kernel   one CTA per (key tile, K/V head): K and V stay in shared
+//                 memory; the CTA walks the column list of query tiles (all g
+//                 heads of the group packed in each 128-row tile, so the GQA
+//                 reduction over the group happens inside the accumulation).
+//                 TMEM: dV, dK accumulators + S^T and dP^T of the current
+//                 query tile.  Thread r of warps 4-7 owns key r.
+//   dq_kernel     one CTA per (query tile, K/V head): Q and dO stay in shared
+//                 memory; the CTA walks the row list of key tiles.  TMEM: S,
+//                 dP and the dQ accumulator.  Thread r owns query row r.
+// Both attention kernels: warp 0 = TMA producer, warp 1 = tcgen05 issuer,
+// warps 4-7 = element-wise work, bounded waits everywhere.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dma {
-cudaError_t launch_bwd(const dma_plan_s&, const dma_bf16*, const dma_bf16*, const float*,
-                       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, dma_bf16*,
-                       float*, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block on sm_103
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
 }
+
+// Bits t in [lo, hi) of a 32-column chunk (clamped to the chunk).
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t upto_hi = (hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  const uint32_t below_lo = (1u << lo) - 1u;
+  return upto_hi & ~below_lo;
+}
+
+// Warp-uniform bounded wait (every lane waits; all agree on the outcome).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
+}
+
+__device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint32_t* pk) {
+  // one 128-element bf16 row (64 packed words) into a K-major 128-byte
+  // swizzled [128 rows][128 cols] tile made of two 64-column regions
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch) {
+    const uint32_t addr = base + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+  }
+}
+
+// ---------------------------------------------------------------- Delta
+
+// Delta[(b*Hq + h)*Lq + l] = sum_d dO[b,l,h,d] * O[b,l,h,d]; D/8 threads per row.
+template <int D>
+__global__ void delta_kernel(const __nv_bfloat16* __restrict__ o,
+                             const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                             int rows, int n_heads, int local_len) {
+  constexpr int TPR = D / 8;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR;
+  const int sub = threadIdx.x % TPR;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[sub];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[sub];
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
+    const long long bl = row / n_heads;  // b*Lq + l
+    const int h = static_cast<int>(row % n_heads);
+    const long long b = bl / local_len, l = bl % local_len;
+    delta[(b * n_heads + h) * local_len + l] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- dK / dV
+
+template <int D>
+struct DkdvCfg {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kRegion = 16384;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;         // 2 stages
+  static constexpr int kDO = kQ + 2 * kTile;    // 2 stages
+  static constexpr int kPS = kDO + 2 * kTile;   // P^T, then dS^T (128 x 128 bf16)
+  static constexpr int kCOL = kPS + 128 * 128 * 2;  // 2 stages x (lse*log2e, Delta), column order
+  static constexpr int kBar = kCOL + 2 * 1024;
+  static constexpr int kNumBars = 17;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kNeed = kMisc + 16;
+  static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
+  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384;
+  static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                const PlanDev p, const float* __restrict__ lse, float* __restrict__ dk,
+                float* __restrict__ dv) {
+  using Cfg = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (__syncthreads_or(threadIdx.x == 0 &&
+                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u))
+    return;
+  if (pad + Cfg::kNeed > static_cast<uint32_t>(Cfg::kAlloc)) {  // cannot lay out the tiles
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_UNSUPPORTED));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
+  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  const int bk = p.bwd_order[ord];
+  const int b = bk / p.n_ktiles, kt = bk % p.n_ktiles;
+  const int cp0 = p.col_ptr[bk];
+  const int n = p.col_ptr[bk + 1] - cp0;
+  const int32_t* list = p.col_idx + cp0;
+
+  uint8_t* sK = smem + Cfg::kK;
+  uint8_t* sV = smem + Cfg::kV;
+  uint8_t* sQ = smem + Cfg::kQ;
+  uint8_t* sDO = smem + Cfg::kDO;
+  uint8_t* sPS = smem + Cfg::kPS;
+  float* sCOL = reinterpret_cast<float*>(smem + Cfg::kCOL);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;    // [2]
+  uint64_t* q_empty = bars + 3;   // [2]
+  uint64_t* do_full = bars + 5;   // [2]
+  uint64_t* do_empty = bars + 7;  // [2]
+  uint64_t* sdp_full = bars + 9;
+  uint64_t* s_free = bars + 10;
+  uint64_t* p_full = bars + 11;
+  uint64_t* pv_done = bars + 12;
+  uint64_t* ds_full = bars + 13;
+  uint64_t* ds_done = bars + 14;
+  uint64_t* dp_free = bars + 15;
+  uint64_t* col_ready = bars + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&do_full[i], 1);
+      mbar_init(&do_empty[i], 1);
+    }
+    mbar_init(sdp_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(dp_free, 128);
+    mbar_init(col_ready, 128);
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(ds_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+  const int krow0 = b * p.seq_len + kt * kTileN;
+
+  if (warp == 0) {
+    if (lane == 0 && n > 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
+#pragma unroll
+      for (int c = 0; c < Cfg::kChunks; ++c) {
+        tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, kvh * D + c * 64, krow0);
+        tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, kvh * D + c * 64, krow0);
+      }
+      int lastq0 = -1, lastq1 = -1, lastdo0 = -1, lastdo1 = -1;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int qt = static_cast<int>(static_cast<uint32_t>(list[i]) & kIndexMask);
+        const int qrow = b * Lq + qt * P;
+        if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64, kvh * g,
+                      qrow);
+        if (st) lastq1 = static_cast<int>(ph); else lastq0 = static_cast<int>(ph);
+        if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
+                      kvh * g, qrow);
+        if (st) lastdo1 = static_cast<int>(ph); else lastdo0 = static_cast<int>(ph);
+      }
+      if (!ok) {
+        drain_wait(kv_full, 0, 100000000ull);
+        if (lastq0 >= 0) drain_wait(&q_full[0], lastq0, 100000000ull);
+        if (lastq1 >= 0) drain_wait(&q_full[1], lastq1, 100000000ull);
+        if (lastdo0 >= 0) drain_wait(&do_full[0], lastdo0, 100000000ull);
+        if (lastdo1 >= 0) drain_wait(&do_full[1], lastdo1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n > 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ps_addr = smem_u32(sPS);
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = mbar_wait(kv_full, 0, ctl);
+      auto issue_dk = [&](int i) -> bool {  // dK += dS^T Q_i
+        const int st = i & 1;
+        if (!mbar_wait(ds_full, i & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemDK, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(ds_done);
+        mma_commit(&q_empty[st]);
+        last_commit = ds_done;
+        last_parity = i & 1;
+        return true;
+      };
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        // S^T = K Q_i^T and dP^T = V dO_i^T
+        if (!mbar_wait(&q_full[st], ph, ctl)) { ok = false; break; }
+        if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
+                      sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        if (!mbar_wait(&do_full[st], ph, ctl)) { ok = false; break; }
+        if (i > 0 && !mbar_wait(dp_free, (i - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
+                      sdesc_sw128(do_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full);
+        last_commit = sdp_full;
+        last_parity = i & 1;
+        if (i > 0 && !issue_dk(i - 1)) { ok = false; break; }
+        // dV += P^T dO_i
+        if (!mbar_wait(p_full, i & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemDV, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(pv_done);
+        mma_commit(&do_empty[st]);
+        last_commit = pv_done;
+        last_parity = i & 1;
+      }
+      if (ok) ok = issue_dk(n - 1);
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------------------- key rows
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int lg = 31 - __clz(g);
+    const int key = kt * kTileN + r;  // position within the sample
+    const float sl2 = p.scale_log2;
+    const uint32_t ps_addr = smem_u32(sPS);
+    const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
+    const int32_t* lo_b = p.doc_lo + static_cast<long long>(b) * Lq;
+    // column r of every query tile is query row (position r >> lg, head r & (g-1))
+    const long long stat_base =
+        (static_cast<long long>(b) * p.n_heads + kvh * g + (r & (g - 1))) * Lq + (r >> lg);
+    float nxt_lse = 0.f, nxt_del = 0.f;
+    if (n > 0) {
+      const int l1 = static_cast<int>(static_cast<uint32_t>(list[0]) & kIndexMask) * P;
+      nxt_lse = lse[stat_base + l1];
+      nxt_del = p.delta[stat_base + l1];
+    }
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int st = i & 1;
+      const uint32_t e = static_cast<uint32_t>(list[i]);
+      const int qt = static_cast<int>(e & kIndexMask);
+      // allowed query positions of this key form one range of the tile's
+      // positions: p_first..p_last (columns p_first*g .. (p_last+1)*g - 1)
+      int c_lo = 0, c_hi = 128;
+      if (e & kPartialBit) {
+        const int l0 = qt * P;
+        const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
+        const int p_first = max(0, key - q0);
+        int lo = 0, hi = P;  // count of positions with doc_lo <= key
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (lo_b[l0 + mid] <= key) lo = mid + 1; else hi = mid;
+        }
+        c_lo = p_first << lg;
+        c_hi = lo << lg;
+      }
+      // column-ordered copies of this tile's row statistics: column j is
+      // query row (position j >> lg, head j & (g-1)); thread r fills column r
+      {
+        const float cur_lse = nxt_lse, cur_del = nxt_del;
+        if (i + 1 < n) {  // prefetch the next tile's statistics for column r
+          const int l1 = static_cast<int>(static_cast<uint32_t>(list[i + 1]) & kIndexMask) * P;
+          nxt_lse = lse[stat_base + l1];
+          nxt_del = p.delta[stat_base + l1];
+        }
+        sCOL[st * 256 + r] = cur_lse * kLog2e;
+        sCOL[st * 256 + 128 + r] = cur_del;
+        mbar_arrive(col_ready);  // 128 arrivals per tile: a bounded barrier
+        if (!warp_wait(col_ready, i & 1, ctl)) { ok = false; break; }
+      }
+      const float4* lse_c = reinterpret_cast<const float4*>(sCOL + st * 256);
+      const float4* del_c = reinterpret_cast<const float4*>(sCOL + st * 256 + 128);
+      // pass 1: P^T row from S^T (needs only S^T)
+      if (!warp_wait(sdp_full, i & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float s[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemS + c0, s);
+        const uint32_t allow = range_bits(c_lo - c0, c_hi - c0);
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = lse_c[(c0 + t) >> 2];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float pv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            pv[u] = ((allow >> (t + u)) & 1u) ? ex2(fmaf(s[t + u], sl2, -lv[u])) : 0.f;
+          pk[(c0 + t) >> 1] = pack_bf16(pv[0], pv[1]);
+          pk[((c0 + t) >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      if (i > 0 && !warp_wait(ds_done, (i - 1) & 1, ctl)) { ok = false; break; }
+      store_row_sw128(ps_addr, r, pk);
+      fence_proxy_async_smem();
+      mbar_arrive(p_full);
+      // pass 2: dS^T = P^T * (dP^T - Delta), P^T read back from this thread's
+      // own row once dV has consumed it, dS^T written in its place
+      if (!warp_wait(pv_done, i & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float dp[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemDP + c0, dp);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // four 16-byte chunks of 8 columns
+          const int ch = (c0 >> 3) + q;
+          const uint32_t addr =
+              ps_addr + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          uint32_t w[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(addr));
+          uint32_t o4[4];
+          const float4 d0 = del_c[(c0 + 8 * q) >> 2];
+          const float4 d1 = del_c[((c0 + 8 * q) >> 2) + 1];
+          const float dl[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = __uint_as_float(w[e] << 16);
+            const float p1 = __uint_as_float(w[e] & 0xFFFF0000u);
+            o4[e] = pack_bf16(p0 * (dp[8 * q + 2 * e] - dl[2 * e]),
+                              p1 * (dp[8 * q + 2 * e + 1] - dl[2 * e + 1]));
+          }
+          st_shared_v4(addr, o4[0], o4[1], o4[2], o4[3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dp_free);
+      fence_proxy_async_smem();
+      mbar_arrive(ds_full);
+    }
+    const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
+    float4* dv_dst = reinterpret_cast<float4*>(dv + out_row * D);
+    float4* dk_dst = reinterpret_cast<float4*>(dk + out_row * D);
+    if (n == 0) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int c = 0; c < D / 4; ++c) {
+        dv_dst[c] = z;
+        dk_dst[c] = z;
+      }
+    } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
+      tc_fence_after();
+      const float sc = p.scale;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float t[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemDV + c0, t);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dv_dst[c0 / 4 + q4] = make_float4(t[4 * q4], t[4 * q4 + 1], t[4 * q4 + 2], t[4 * q4 + 3]);
+        tmem_ld32(tmem + lane_base + Cfg::kTmemDK + c0, t);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dk_dst[c0 / 4 + q4] = make_float4(t[4 * q4] * sc, t[4 * q4 + 1] * sc,
+                                            t[4 * q4 + 2] * sc, t[4 * q4 + 3] * sc);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------- dQ
+
+template <int D>
+struct DqCfg {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kRegion = 16384;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTile;
+  static constexpr int kK = kDO + kTile;       // 2 stages
+  static constexpr int kV = kK + 2 * kTile;    // 2 stages
+  static constexpr int kDS = kV + 2 * kTile;   // dS (128 x 128 bf16)
+  static constexpr int kBar = kDS + 128 * 128 * 2;
+  static constexpr int kNumBars = 13;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kNeed = kMisc + 16;
+  static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
+  static_assert(kNeed <= kMaxSmem, "dQ shared-memory layout exceeds 227 KB");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+              const PlanDev p, const float* __restrict__ lse, __nv_bfloat16* __restrict__ dq) {
+  using Cfg = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (__syncthreads_or(threadIdx.x == 0 &&
+                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u))
+    return;
+  if (pad + Cfg::kNeed > static_cast<uint32_t>(Cfg::kAlloc)) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_UNSUPPORTED));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
+  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  const int bq = p.fwd_order[ord];
+  const int b = bq / p.n_qtiles, qt = bq % p.n_qtiles;
+  const int l0 = qt * P;
+  const int rp0 = p.row_ptr[bq];
+  const int n = p.row_ptr[bq + 1] - rp0;
+  const int32_t* list = p.row_idx + rp0;
+
+  uint8_t* sQ = smem + Cfg::kQ;
+  uint8_t* sDO = smem + Cfg::kDO;
+  uint8_t* sK = smem + Cfg::kK;
+  uint8_t* sV = smem + Cfg::kV;
+  uint8_t* sDS = smem + Cfg::kDS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* q_full = bars;       // Q and dO
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* sdp_full = bars + 9;
+  uint64_t* st_free = bars + 10;
+  uint64_t* ds_full = bars + 11;
+  uint64_t* ds_done = bars + 12;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(sdp_full, 1);
+    mbar_init(st_free, 128);
+    mbar_init(ds_full, 128);
+    mbar_init(ds_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0 && n > 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_expect_tx(q_full, 2 * Cfg::kTile);
+#pragma unroll
+      for (int c = 0; c < Cfg::kChunks; ++c) {
+        tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
+        tma_load_3d(sDO + c * Cfg::kRegion, &tdo, q_full, c * 64, kvh * g, b * Lq + l0);
+      }
+      int lastk0 = -1, lastk1 = -1, lastv0 = -1, lastv1 = -1;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
+        const int krow = b * p.seq_len + kt * kTileN;
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[st], Cfg::kTile);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_2d(sK + st * Cfg::kTile + c * Cfg::kRegion, &tk, &k_full[st], kvh * D + c * 64,
+                      krow);
+        if (st) lastk1 = static_cast<int>(ph); else lastk0 = static_cast<int>(ph);
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[st], Cfg::kTile);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_2d(sV + st * Cfg::kTile + c * Cfg::kRegion, &tv, &v_full[st], kvh * D + c * 64,
+                      krow);
+        if (st) lastv1 = static_cast<int>(ph); else lastv0 = static_cast<int>(ph);
+      }
+      if (!ok) {
+        drain_wait(q_full, 0, 100000000ull);
+        if (lastk0 >= 0) drain_wait(&k_full[0], lastk0, 100000000ull);
+        if (lastk1 >= 0) drain_wait(&k_full[1], lastk1, 100000000ull);
+        if (lastv0 >= 0) drain_wait(&v_full[0], lastv0, 100000000ull);
+        if (lastv1 >= 0) drain_wait(&v_full[1], lastv1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n > 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), ds_addr = smem_u32(sDS);
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = mbar_wait(q_full, 0, ctl);
+      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j
+        const int st = j & 1;
+        if (!mbar_wait(ds_full, j & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(ds_done);
+        mma_commit(&k_empty[st]);
+        last_commit = ds_done;
+        last_parity = j & 1;
+        return true;
+      };
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
+        if (j > 0 && !mbar_wait(st_free, (j - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(q_addr + off, 16, 1024),
+                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        if (!mbar_wait(&v_full[st], ph, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(do_addr + off, 16, 1024),
+                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full);
+        mma_commit(&v_empty[st]);
+        last_commit = sdp_full;
+        last_parity = j & 1;
+        if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+      }
+      if (ok) ok = issue_dq(n - 1);
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------------------- query rows
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int lg = 31 - __clz(g);
+    const int pos = r >> lg, h = r & (g - 1);
+    const int l = l0 + pos;
+    const int C = p.chunk;
+    const int qabs = (l < C) ? (p.cp_rank * C + l) : ((2 * p.cp_size - 1 - p.cp_rank) * C + l - C);
+    const int lo_r = p.doc_lo[static_cast<long long>(b) * Lq + l];
+    const int hq = kvh * g + h;
+    const long long stat = (static_cast<long long>(b) * p.n_heads + hq) * Lq + l;
+    const float lse2 = lse[stat] * kLog2e;
+    const float del = p.delta[stat];
+    const float sl2 = p.scale_log2;
+    const uint32_t ds_addr = smem_u32(sDS);
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t e = static_cast<uint32_t>(list[j]);
+      int c_lo = 0, c_hi = 128;
+      if (e & kPartialBit) {
+        const int k0 = static_cast<int>(e & kIndexMask) * kTileN;
+        c_lo = lo_r - k0;
+        c_hi = qabs - k0 + 1;
+      }
+      if (!warp_wait(sdp_full, j & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float s[32], dp[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemS + c0, s);
+        tmem_ld32(tmem + lane_base + Cfg::kTmemDP + c0, dp);
+        const uint32_t allow = range_bits(c_lo - c0, c_hi - c0);
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float pj = ((allow >> (t + u)) & 1u) ? ex2(fmaf(s[t + u], sl2, -lse2)) : 0.f;
+            dsv[u] = pj * (dp[t + u] - del);
+          }
+          pk[(c0 + t) >> 1] = pack_bf16(dsv[0], dsv[1]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(st_free);
+      if (j > 0 && !warp_wait(ds_done, (j - 1) & 1, ctl)) { ok = false; break; }
+      store_row_sw128(ds_addr, r, pk);
+      fence_proxy_async_smem();
+      mbar_arrive(ds_full);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(
+        dq + ((static_cast<long long>(b) * Lq + l) * p.n_heads + hq) * D);
+    if (n == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
+      tc_fence_after();
+      const float sc = p.scale;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float t[32];
+        tmem_ld32(tmem + lane_base + Cfg::kTmemDQ + c0, t);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 u;
+          u.x = pack_bf16(t[8 * q4 + 0] * sc, t[8 * q4 + 1] * sc);
+          u.y = pack_bf16(t[8 * q4 + 2] * sc, t[8 * q4 + 3] * sc);
+          u.z = pack_bf16(t[8 * q4 + 4] * sc, t[8 * q4 + 5] * sc);
+          u.w = pack_bf16(t[8 * q4 + 6] * sc, t[8 * q4 + 7] * sc);
+          dst[c0 / 8 + q4] = u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+                         const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, dma_bf16* dq, float* dk,
+                         float* dv,
+                         cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const int rows = p.batch * p.local_len * p.n_heads;
+  if (rows == 0) return cudaSuccess;
+  constexpr int TPR = D / 8;
+  const int blocks = (rows * TPR + 255) / 256;
+  delta_kernel<D><<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(o),
+                                         reinterpret_cast<const __nv_bfloat16*>(dout), p.delta,
+                                         rows, p.n_heads, p.local_len);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DkdvCfg<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  dkdv_kernel<D><<<p.batch * p.n_ktiles * p.n_kv_heads, 256, DkdvCfg<D>::kAlloc, s>>>(
+      tq, tk, tv, tdo, p, lse, dk, dv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DqCfg<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  dq_kernel<D><<<p.batch * p.n_qtiles * p.n_kv_heads, 256, DqCfg<D>::kAlloc, s>>>(
+      tq, tk, tv, tdo, p, lse, reinterpret_cast<__nv_bfloat16*>(dq));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+                       const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, dma_bf16* dq, float* dk,
+                       float* dv,
+                       cudaStream_t s) {
+  if (pl.d.head_dim == 128)
+    return launch_bwd_d<128>(pl, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv, s);
+  return launch_bwd_d<64>(pl, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv, s);
+}
+
 }  // namespace dma

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(256, 1)
     const int qabs = s_qpos[pos], lo_r = s_lo[pos];
     const float sl2 = p.scale_log2;
     const uint32_t p_addr = smem_u32(sP);
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, lr_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
@@ -278,15 +278,24 @@ __global__ void __launch_bounds__(256, 1)
       const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2(m_run - m_ref);
-      float sum0 = 0.f, sum1 = 0.f;
+      // p in fp32 for the log-sum-exp; p rounded to bf16 (the operand the
+      // tensor core sees) both for P V and for the sum O is divided by, so
+      // that O is an exact convex combination of V rows.
+      float sum0 = 0.f, sum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+      uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        s[c] = ex2(fmaf(s[c], sl2, -m_ref));
-        s[c + 1] = ex2(fmaf(s[c + 1], sl2, -m_ref));
-        sum0 += s[c];
-        sum1 += s[c + 1];
+        const float e0 = ex2(fmaf(s[c], sl2, -m_ref));
+        const float e1 = ex2(fmaf(s[c + 1], sl2, -m_ref));
+        sum0 += e0;
+        sum1 += e1;
+        const uint32_t u = pack_bf16(e0, e1);
+        pk[c >> 1] = u;
+        rsum0 += __uint_as_float(u << 16);
+        rsum1 += __uint_as_float(u & 0xFFFF0000u);
       }
       l_run = l_run * alpha + (sum0 + sum1);
+      lr_run = lr_run * alpha + (rsum0 + rsum1);
       if (j >= 1) {
         if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, ctl))) {
           ok = false;
@@ -299,10 +308,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int ch = 0; ch < 16; ++ch) {
         const uint32_t addr = p_addr + (ch >> 3) * Cfg::kRegion + r * 128 +
                               ((((ch & 7) ^ (r & 7))) << 4);
-        st_shared_v4(addr, pack_bf16(s[8 * ch], s[8 * ch + 1]),
-                     pack_bf16(s[8 * ch + 2], s[8 * ch + 3]),
-                     pack_bf16(s[8 * ch + 4], s[8 * ch + 5]),
-                     pack_bf16(s[8 * ch + 6], s[8 * ch + 7]));
+        st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, ctl))) {
       tc_fence_after();
-      const float inv = 1.f / l_run;
+      const float inv = 1.f / lr_run;
       const int hq = kvh * g + h;
       const long long row = static_cast<long long>(b) * Lq + l0 + pos;
       uint4* dst = reinterpret_cast<uint4*>(o + (row * p.n_heads + hq) * D);

@@ -1,0 +1,103 @@
+"""Backward parity on the GPU against the float64 oracle: dQ, dK, dV relative
+Frobenius error <= 2e-2 per tensor per rank (full tensors where the oracle is
+quick), CP re-assembly of the per-rank partial gradients against the CP=1
+oracle, and at the 405B size sampled dQ rows plus identities that hold at any
+size."""
+import numpy as np
+import pytest
+import torch
+
+from document_masked_gqa_gb300 import workloads as wl
+from helpers import TOL_GRAD, TOL_LSE, TOL_O, gpu_rank, max_abs, oracle_rank, rel_fro
+from oracle import attention as oa
+from oracle import cp as ocp
+from test_plan_gpu import EDGE
+
+pytestmark = pytest.mark.gpu
+
+
+def _bwd_case(w, rank, inp=None, cu=None):
+    cu = wl.cu_doc_lens(w) if cu is None else cu
+    inp = wl.tensors(w) if inp is None else inp
+    g, _ = gpu_rank(w, rank, inp, cu, backward=True)
+    ref = oracle_rank(w, rank, inp, cu, backward=True)
+    assert max_abs(g["o"].numpy(), ref["o"]) <= TOL_O
+    assert max_abs(g["lse"].numpy(), ref["lse"]) <= TOL_LSE
+    errs = {}
+    for key in ("dq", "dk", "dv"):
+        x = g[key].numpy()
+        assert np.isfinite(x).all(), (w.name, rank, key)
+        errs[key] = rel_fro(x, ref[key])
+        assert errs[key] <= TOL_GRAD, (w.name, rank, key, errs[key])
+    return g, ref, errs
+
+
+@pytest.mark.parametrize("name", ["tiny", "70b", "sparse", "8b"])
+def test_bwd_parity_full(name):
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    for r in w.ranks:
+        _bwd_case(w, r, inp, cu)
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_bwd_parity_edge(name):
+    w = EDGE[name]
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    for r in w.ranks:
+        _bwd_case(w, r, inp, cu)
+
+
+@pytest.mark.parametrize("name", ["tiny", "70b", "sparse"])
+def test_cp_reassembly_against_cp1_oracle(name):
+    """All ranks of the GPU path, put back together, equal the oracle run on
+    the whole sequence as one rank (CP=1); partial dK/dV sum to the full."""
+    w = wl.WORKLOADS[name]
+    assert tuple(w.ranks) == tuple(range(w.cp_size))
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    outs = {r: gpu_rank(w, r, inp, cu)[0] for r in w.ranks}
+    full = oa.attention(inp["q"], inp["k"], inp["v"], cu, 1, 0, do_local=inp["do"], threads=4)
+    o = ocp.assemble_full({r: outs[r]["o"].numpy() for r in outs}, w.seq_len, w.cp_size)
+    dq = ocp.assemble_full({r: outs[r]["dq"].numpy() for r in outs}, w.seq_len, w.cp_size)
+    lse = ocp.assemble_full({r: outs[r]["lse"].numpy().transpose(0, 2, 1) for r in outs},
+                            w.seq_len, w.cp_size).transpose(0, 2, 1)
+    assert max_abs(o, full["o"]) <= TOL_O
+    assert max_abs(lse, full["lse"]) <= TOL_LSE
+    assert rel_fro(dq, full["dq"]) <= TOL_GRAD
+    dk = sum(outs[r]["dk"].numpy() for r in outs)
+    dv = sum(outs[r]["dv"].numpy() for r in outs)
+    assert rel_fro(dk, full["dk"]) <= TOL_GRAD
+    assert rel_fro(dv, full["dv"]) <= TOL_GRAD
+
+
+@pytest.mark.parametrize("name", ["405b-logu", "405b-1doc"])
+def test_bwd_405b_sampled_rows_and_identities(name):
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    rng = np.random.default_rng(7)
+    for r in w.ranks:
+        g, _ = gpu_rank(w, r, inp, cu, backward=True)
+        rows = np.unique(np.concatenate([[0, w.chunk - 1, w.chunk, w.local_len - 1],
+                                         rng.integers(0, w.local_len, 28)]))
+        ref = oracle_rank(w, r, inp, cu, backward=True, rows=rows, threads=8)
+        assert max_abs(g["o"].numpy()[:, rows], ref["o"][:, rows]) <= TOL_O
+        assert max_abs(g["lse"].numpy()[:, :, rows], ref["lse"][:, :, rows]) <= TOL_LSE
+        assert rel_fro(g["dq"].numpy()[:, rows], ref["dq"][:, rows]) <= TOL_GRAD
+        dk, dv, dq = g["dk"].numpy(), g["dv"].numpy(), g["dq"].numpy()
+        assert np.isfinite(dk).all() and np.isfinite(dv).all() and np.isfinite(dq).all()
+        # every row's P sums to one: sum over keys of dV = sum over rows and
+        # the group's heads of dO
+        do_l = ocp.gather_local(inp["do"].double().numpy(), w.seq_len, w.cp_size, r)
+        lhs = dv.astype(np.float64).sum(axis=1)                       # [B, Hkv, D]
+        rhs = do_l.reshape(w.batch, w.local_len, w.n_kv_heads, w.group, w.head_dim
+                           ).sum(axis=(1, 3))
+        assert rel_fro(lhs, rhs) <= TOL_GRAD
+        # sum_q <q, dQ> = sum_k <k, dK> (both equal scale * sum dS * (q.k))
+        q_l = ocp.gather_local(inp["q"].double().numpy(), w.seq_len, w.cp_size, r)
+        a = float((q_l * dq.astype(np.float64)).sum())
+        b = float((inp["k"].double().numpy() * dk.astype(np.float64)).sum())
+        assert abs(a - b) <= TOL_GRAD * max(abs(a), abs(b), 1e-6), (a, b)
