@@ -1,0 +1,533 @@
+#!/usr/bin/env python3
+"""Throughput of causal + document-masked GQA attention, forward + backward,
+for emulated context-parallel ranks on GB300.
+
+One step = the whole hot path for every emulated rank of the workload:
+plan (CP position map + block-mask builder), forward (O, LSE), backward
+(Delta, dK/dV, dQ), inputs already resident in HBM.  The metric counts only
+unmasked (query, key) pairs: FLOPs = sum over ranks and samples of
+Hq * pairs * (4*D forward + 10*D backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b]
+    python bench.py --impl reference ...   # the float64 oracle on host cores
+
+Under torchrun (N > 1) every rank runs its own copy of the workload with its
+own seed (independent problems, weak scaling, no data-path collective); the
+step time is the max over ranks.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from document_masked_gqa_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "doc-masked GQA attn fwd+bwd TFLOP/s (unmasked FLOPs), % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, NVIDIA's figure without sparsity
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_RANK_STEP = 11  # plan: 7, forward: 1, backward: 3
+
+
+# ------------------------------------------------------------------ counting
+
+def local_positions(seq_len: int, cp_size: int, rank: int) -> np.ndarray:
+    c = seq_len // (2 * cp_size)
+    a, b = rank, 2 * cp_size - 1 - rank
+    return np.concatenate([np.arange(a * c, (a + 1) * c), np.arange(b * c, (b + 1) * c)])
+
+
+def pairs_per_sample(cu: np.ndarray, batch: int, seq_len: int, cp_size: int,
+                     rank: int) -> np.ndarray:
+    """Allowed (query, key) pairs of one rank per sample and head."""
+    qpos = local_positions(seq_len, cp_size, rank)
+    cu = np.asarray(cu, dtype=np.int64)
+    out = []
+    for b in range(batch):
+        g = b * seq_len + qpos
+        d = np.searchsorted(cu, g, side="right") - 1
+        start = cu[d] - b * seq_len
+        out.append(int((qpos - start + 1).sum()))
+    return np.asarray(out, dtype=np.int64)
+
+
+def flops_of(w: wl.Workload, cu, ranks, heads=None, fwd=4, bwd=10) -> float:
+    h = w.n_heads if heads is None else heads
+    tot = 0
+    for r in ranks:
+        tot += int(pairs_per_sample(cu, w.batch, w.seq_len, w.cp_size, r).sum())
+    return float(h) * tot * (fwd + bwd) * w.head_dim
+
+
+# ---------------------------------------------------------- distributed bits
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
+    """Weak scaling: every process gets the same shape with its own seed."""
+    return dataclasses.replace(w, seed=w.seed + 7919 * rank) if rank else w
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world == 1:
+        return
+    import torch
+    import torch.distributed as dist
+    t = torch.zeros(1, device=device)
+    dist.all_reduce(t)
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = self.rows
+        if self.bus_id:
+            mine = [r for r in rows if self.bus_id.endswith(r[0].lower()[-12:]) or
+                    r[0].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if not rows:
+            return None
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in rows for i in range(1, 5)
+                          if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "document_masked_gqa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel
+    and workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample_step(w: wl.Workload, inputs: dict, cu, rows=None, threads=None):
+    """One bounded sample of the workload on the float64 oracle: sample 0,
+    the query heads of K/V head 0, rank ranks[0]; fwd + bwd.  Returns the
+    counted FLOPs of the sample."""
+    from oracle import attention as oa
+    from oracle import cp as ocp
+    r = w.ranks[0]
+    g = w.group
+    q = ocp.gather_local(inputs["q"][:1, :, :g], w.seq_len, w.cp_size, r)
+    do = ocp.gather_local(inputs["do"][:1, :, :g], w.seq_len, w.cp_size, r)
+    k = inputs["k"][:1, :, :1]
+    v = inputs["v"][:1, :, :1]
+    cu0 = np.asarray([x for x in cu if x <= w.seq_len], dtype=np.int64)
+    threads = threads or min(g, os.cpu_count() or 1)
+    oa.attention(q, k, v, cu0, w.cp_size, r, do_local=do, rows=rows, threads=threads,
+                 kv_grads_from_rows=True)
+    qpos = local_positions(w.seq_len, w.cp_size, r)
+    sel = qpos if rows is None else qpos[np.asarray(rows)]
+    d = np.searchsorted(cu0, sel, side="right") - 1
+    pairs = int((sel - cu0[d] + 1).sum())
+    return float(g) * pairs * 14 * w.head_dim, threads
+
+
+def run_reference(args, w: wl.Workload):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    cu = wl.cu_doc_lens(w)
+    inputs = wl.tensors(w)
+    budget = float(os.environ.get("DMA_REF_BUDGET_S", "150"))
+    steps_total = args.steps + args.warmup
+    # size the sample: all rows of one K/V group of sample 0, cut to fit budget
+    t0 = time.perf_counter()
+    flops, threads = oracle_sample_step(w, inputs, cu)
+    t_full = time.perf_counter() - t0
+    rows = None
+    sample = (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank {w.ranks[0]}, "
+              f"all {w.local_len} local rows, fwd+bwd")
+    if t_full * steps_total > budget:
+        frac = max(budget / (t_full * steps_total), 1.0 / w.local_len)
+        n = max(1, int(w.local_len * frac))
+        rows = np.arange(w.local_len - n, w.local_len)  # the heaviest rows: last chunk tail
+        sample = (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank {w.ranks[0]}, "
+                  f"local rows {rows[0]}-{rows[-1]}, fwd+bwd (dK/dV from those rows)")
+    times = []
+    for i in range(steps_total):
+        t0 = time.perf_counter()
+        flops, threads = oracle_sample_step(w, inputs, cu, rows=rows)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample, "threads": threads},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: wl.Workload) -> dict:
+    docs = {"uniform": f"uniform [{w.doc_lo}, {w.doc_hi}]",
+            "loguniform": f"log-uniform [{w.doc_lo}, {w.doc_hi}] per sample",
+            "single": "one document per sample"}.get(w.doc_dist, w.doc_dist)
+    return {"workload": w.name, "seq_len": w.seq_len, "cp_size": w.cp_size,
+            "ranks": list(w.ranks), "batch": w.batch, "n_heads": w.n_heads,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "docs": docs,
+            "q_prescale": w.q_prescale, "seed": w.seed,
+            "l2": "flushed between steps (256 MiB write, outside the timed events)",
+            "flops": "unmasked pairs x Hq x (4D fwd + 10D bwd)"}
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w: wl.Workload):
+    import torch
+
+    import document_masked_gqa_gb300 as dma
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = rank_workload(w, rank)
+    cu_np = wl.cu_doc_lens(w)
+    cu = torch.from_numpy(cu_np).to(dev)
+    inputs = wl.tensors(w)
+    stream = torch.cuda.current_stream(dev)
+
+    k = inputs["k"].to(dev)
+    v = inputs["v"].to(dev)
+    ranks = []
+    for r in w.ranks:
+        need = dma.dma_plan_workspace_bytes(w.batch, w.seq_len, w.cp_size, w.n_heads,
+                                            w.n_kv_heads, w.head_dim)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
+                            w.head_dim, workspace=ws)
+        q = dma.dma_cp_gather(plan, inputs["q"].to(dev))
+        do = dma.dma_cp_gather(plan, inputs["do"].to(dev))
+        o, lse = dma.dma_attn_fwd(plan, q, k, v)
+        dq, dk, dv = dma.dma_attn_bwd(plan, q, k, v, o, lse, do)
+        ranks.append(dict(r=r, ws=ws, q=q, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+    torch.cuda.synchronize(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    names = ("plan", "fwd", "delta", "dkdv", "dq")
+    ktime = {n: 0.0 for n in names}
+
+    def step(record: bool):
+        evs = []
+        for R in ranks:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+            if record:
+                e[0].record(stream)
+            plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, R["r"], w.n_heads,
+                                w.n_kv_heads, w.head_dim, workspace=R["ws"])
+            R["plan"] = plan
+            if record:
+                e[1].record(stream)
+            dma.dma_attn_fwd(plan, R["q"], k, v, R["o"], R["lse"])
+            if record:
+                e[2].record(stream)
+            dma.dma_attn_bwd_delta(plan, R["o"], R["do"])
+            if record:
+                e[3].record(stream)
+            dma.dma_attn_bwd_dkdv(plan, R["q"], k, v, R["lse"], R["do"], R["dk"], R["dv"])
+            if record:
+                e[4].record(stream)
+            dma.dma_attn_bwd_dq(plan, R["q"], k, v, R["lse"], R["do"], R["dq"])
+            if record:
+                e[5].record(stream)
+            evs.append(e)
+        return evs
+
+    for _ in range(args.warmup):
+        step(False)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for R in ranks:
+        st = dma.dma_plan_check(R["plan"])
+        if st != 0:
+            raise RuntimeError(f"plan status {st}: {dma.status_str(st)}")
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id if hasattr(
+            torch.cuda.get_device_properties(dev), "pci_bus_id") else None
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus)
+    sampler.start()
+    time.sleep(0.3)
+
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    step_pairs = []
+    all_evs = []
+    for _ in range(args.steps):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        evs = step(True)
+        s1.record(stream)
+        step_pairs.append((s0, s1))
+        all_evs.append(evs)
+        flush.zero_()  # L2 flush between steps, outside the step's events
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop()
+
+    ms_steps = [a.elapsed_time(b) for a, b in step_pairs]
+    ms_local = sum(ms_steps) / len(ms_steps)
+    for evs in all_evs:
+        for e in evs:
+            for i, n in enumerate(names):
+                ktime[n] += e[i].elapsed_time(e[i + 1])
+    n_launch = args.steps * len(ranks)
+    kms = {n: ktime[n] / n_launch for n in names}
+    for R in ranks:
+        st = dma.dma_plan_check(R["plan"])
+        if st != 0:
+            raise RuntimeError(f"plan status {st}: {dma.status_str(st)}")
+
+    ms = reduce_max(ms_local, world, dev)
+    flops_step = flops_of(w, cu_np, w.ranks)
+    value = world * flops_step / (ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (largest share of the step)
+    per_rank_pairs = [int(pairs_per_sample(cu_np, w.batch, w.seq_len, w.cp_size, r).sum())
+                      for r in w.ranks]
+    algo = {"fwd": 4, "dkdv": 8, "dq": 6}  # contractions over D per pair and head, x D
+    dom = max(("fwd", "dkdv", "dq"), key=lambda n: kms[n])
+    algo_flops = w.n_heads * (sum(per_rank_pairs) / len(w.ranks)) * algo[dom] * w.head_dim
+    achieved = algo_flops / (kms[dom] * 1e-3) / 1e12
+    peaks = measured_peaks()
+    peak = peaks.get("bf16_tflops")
+    peak_src = "measured burst (MEASURED_PEAKS.json bf16_tflops)"
+    if not peak:
+        peak, peak_src = FALLBACK_BF16_TFLOPS, "fallback"
+    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+            "traffic": profiled_traffic(dom, w.name),
+            "algorithmic_flops_per_launch": algo_flops,
+            "kernel_ms": {n: round(kms[n], 5) for n in names}}
+
+    # end to end through the public API: pinned host inputs -> device -> step ->
+    # results back to pinned host memory, every step
+    e2e = run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        fl, threads = oracle_sample_step(w, inputs, cu_np)
+        dt = time.perf_counter() - t0
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+               "kind": "oracle", "threads": threads,
+               "sample": (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank "
+                          f"{w.ranks[0]}, all {w.local_len} local rows, fwd+bwd, "
+                          f"{dt:.1f} s, float64 numpy")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+            "pct_of_measured_peak": 100.0 * value / world / peak,
+            "pct_of_datasheet_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_RANK_STEP * len(w.ranks) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
+    import torch
+    steps = max(3, min(args.steps, 20))
+    h_k = inputs["k"].pin_memory()
+    h_v = inputs["v"].pin_memory()
+    h_cu = torch.from_numpy(cu_np).pin_memory()
+    per = []
+    for r in w.ranks:
+        pos = torch.from_numpy(local_positions(w.seq_len, w.cp_size, r))
+        h_q = inputs["q"][:, pos].contiguous().pin_memory()
+        h_do = inputs["do"][:, pos].contiguous().pin_memory()
+        outs = {"o": torch.empty_like(h_q).pin_memory(),
+                "lse": torch.empty(w.batch, w.n_heads, w.local_len).pin_memory(),
+                "dq": torch.empty_like(h_q).pin_memory(),
+                "dk": torch.empty(h_k.shape, dtype=torch.float32).pin_memory(),
+                "dv": torch.empty(h_k.shape, dtype=torch.float32).pin_memory()}
+        per.append((r, h_q, h_do, outs))
+    h2d = h_k.nbytes + h_v.nbytes + h_cu.nbytes + sum(p[1].nbytes + p[2].nbytes for p in per)
+    d2h = sum(sum(t.nbytes for t in p[3].values()) for p in per)
+
+    def one():
+        cu = h_cu.to(dev, non_blocking=True)
+        k = h_k.to(dev, non_blocking=True)
+        v = h_v.to(dev, non_blocking=True)
+        for r, h_q, h_do, outs in per:
+            q = h_q.to(dev, non_blocking=True)
+            do = h_do.to(dev, non_blocking=True)
+            plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
+                                w.head_dim)
+            o, lse = dma.dma_attn_fwd(plan, q, k, v)
+            dq, dk, dv = dma.dma_attn_bwd(plan, q, k, v, o, lse, do)
+            outs["o"].copy_(o, non_blocking=True)
+            outs["lse"].copy_(lse, non_blocking=True)
+            outs["dq"].copy_(dq, non_blocking=True)
+            outs["dk"].copy_(dk, non_blocking=True)
+            outs["dv"].copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(a.elapsed_time(b) / steps, world, dev)
+    return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default="8b", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -28,7 +28,7 @@ EXPORTED = [
     "dma_plan_workspace_bytes", "dma_plan", "dma_attn_fwd", "dma_attn_bwd",
     "dma_plan_check", "dma_plan_destroy", "dma_status_str", "dma_cp_gather",
     "dma_cp_scatter", "dma_plan_get_view", "dma_plan_set_wait_timeout",
-    "dma_debug_wait_probe",
+    "dma_debug_wait_probe", "dma_attn_bwd_delta", "dma_attn_bwd_dkdv", "dma_attn_bwd_dq",
 ]
 
 
@@ -70,6 +70,9 @@ def _load():
         "dma_plan_get_view": (i32, [vp, ctypes.POINTER(PlanView)]),
         "dma_plan_set_wait_timeout": (i32, [vp, u64]),
         "dma_debug_wait_probe": (i32, [u64, vp, vp]),
+        "dma_attn_bwd_delta": (i32, [vp] * 4),
+        "dma_attn_bwd_dkdv": (i32, [vp] * 9),
+        "dma_attn_bwd_dq": (i32, [vp] * 8),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -215,6 +218,22 @@ def dma_attn_bwd(plan: Plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, s
                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
            "dma_attn_bwd")
     return dq, dk, dv
+
+
+def dma_attn_bwd_delta(plan: Plan, o, dout, stream=None):
+    _check(lib().dma_attn_bwd_delta(plan.handle, _ptr(o), _ptr(dout), _stream(stream)),
+           "dma_attn_bwd_delta")
+
+
+def dma_attn_bwd_dkdv(plan: Plan, q, k, v, lse, dout, dk, dv, stream=None):
+    _check(lib().dma_attn_bwd_dkdv(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
+                                   _ptr(dout), _ptr(dk), _ptr(dv), _stream(stream)),
+           "dma_attn_bwd_dkdv")
+
+
+def dma_attn_bwd_dq(plan: Plan, q, k, v, lse, dout, dq, stream=None):
+    _check(lib().dma_attn_bwd_dq(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
+                                 _ptr(dout), _ptr(dq), _stream(stream)), "dma_attn_bwd_dq")
 
 
 def dma_plan_check(plan: Plan, stream=None) -> int:

@@ -231,15 +231,25 @@ dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
              : DMA_ERR_CUDA;
 }
 
-dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
-                        const dma_bf16* o, const float* lse, const dma_bf16* dout, dma_bf16* dq,
-                        float* dk, float* dv, void* stream) {
+dma_status dma_attn_bwd_delta(dma_plan_t plan, const dma_bf16* o, const dma_bf16* dout,
+                              void* stream) {
+  if (!plan) return DMA_ERR_INVALID_ARG;
+  if (plan->d.batch == 0) return DMA_OK;
+  if (!o || !dout || !aligned16(o) || !aligned16(dout)) return DMA_ERR_INVALID_ARG;
+  return dma::launch_delta(*plan, o, dout, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DMA_OK
+             : DMA_ERR_CUDA;
+}
+
+dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                             const dma_bf16* v, const float* lse, const dma_bf16* dout, float* dk,
+                             float* dv, void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
   const dma::PlanDev& p = plan->d;
   if (p.batch == 0) return DMA_OK;
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return DMA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+  if (!q || !k || !v || !lse || !dout || !dk || !dv) return DMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dk) || !aligned16(dv))
     return DMA_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv, tdo;
   dma_status st;
@@ -248,10 +258,46 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
   if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  return dma::launch_bwd(*plan, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv,
-                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, dk, dv,
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;
+}
+
+dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                           const dma_bf16* v, const float* lse, const dma_bf16* dout,
+                           dma_bf16* dq, void* stream) {
+  if (!plan) return DMA_ERR_INVALID_ARG;
+  const dma::PlanDev& p = plan->d;
+  if (p.batch == 0) return DMA_OK;
+  if (!q || !k || !v || !lse || !dout || !dq) return DMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq))
+    return DMA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv, tdo;
+  dma_status st;
+  const int rows = p.batch * p.local_len;
+  if ((st = map_rows_heads(&tq, q, p, p.n_heads, rows)) != DMA_OK) return st;
+  if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
+  if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
+  if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
+  return dma::launch_dq(*plan, lse, tq, tk, tv, tdo, dq, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? DMA_OK
+             : DMA_ERR_CUDA;
+}
+
+dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
+                        const dma_bf16* o, const float* lse, const dma_bf16* dout, dma_bf16* dq,
+                        float* dk, float* dv, void* stream) {
+  if (!plan) return DMA_ERR_INVALID_ARG;
+  if (plan->d.batch == 0) return DMA_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return DMA_ERR_INVALID_ARG;
+  dma_status st = dma_attn_bwd_delta(plan, o, dout, stream);
+  if (st != DMA_OK) return st;
+  st = dma_attn_bwd_dkdv(plan, q, k, v, lse, dout, dk, dv, stream);
+  if (st != DMA_OK) return st;
+  return dma_attn_bwd_dq(plan, q, k, v, lse, dout, dq, stream);
 }
 
 dma_status dma_plan_check(dma_plan_t plan, void* stream) {

@@ -741,11 +741,8 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
-                         const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, dma_bf16* dq, float* dk,
-                         float* dv,
-                         cudaStream_t s) {
+cudaError_t launch_delta_d(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+                           cudaStream_t s) {
   const PlanDev& p = pl.d;
   const int rows = p.batch * p.local_len * p.n_heads;
   if (rows == 0) return cudaSuccess;
@@ -754,33 +751,58 @@ cudaError_t launch_bwd_d(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16
   delta_kernel<D><<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(o),
                                          reinterpret_cast<const __nv_bfloat16*>(dout), p.delta,
                                          rows, p.n_heads, p.local_len);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
+                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                          float* dk, float* dv, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const int grid = p.batch * p.n_ktiles * p.n_kv_heads;
+  if (grid == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DkdvCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DkdvCfg<D>::kAlloc);
+  dkdv_kernel<D><<<grid, 256, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse, dk, dv);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
+                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                        dma_bf16* dq, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const int grid = p.batch * p.n_qtiles * p.n_kv_heads;
+  if (grid == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DqCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<p.batch * p.n_ktiles * p.n_kv_heads, 256, DkdvCfg<D>::kAlloc, s>>>(
-      tq, tk, tv, tdo, p, lse, dk, dv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DqCfg<D>::kAlloc);
-  if (e != cudaSuccess) return e;
-  dq_kernel<D><<<p.batch * p.n_qtiles * p.n_kv_heads, 256, DqCfg<D>::kAlloc, s>>>(
-      tq, tk, tv, tdo, p, lse, reinterpret_cast<__nv_bfloat16*>(dq));
+  dq_kernel<D><<<grid, 256, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse,
+                                                   reinterpret_cast<__nv_bfloat16*>(dq));
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
-                       const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, dma_bf16* dq, float* dk,
-                       float* dv,
-                       cudaStream_t s) {
-  if (pl.d.head_dim == 128)
-    return launch_bwd_d<128>(pl, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv, s);
-  return launch_bwd_d<64>(pl, o, dout, lse, tq, tk, tv, tdo, dq, dk, dv, s);
+cudaError_t launch_delta(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+                         cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_delta_d<128>(pl, o, dout, s)
+                              : launch_delta_d<64>(pl, o, dout, s);
+}
+
+cudaError_t launch_dkdv(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
+                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                        float* dk, float* dv, cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, dk, dv, s)
+                              : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, dk, dv, s);
+}
+
+cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
+                      const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                      dma_bf16* dq, cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_dq_d<128>(pl, lse, tq, tk, tv, tdo, dq, s)
+                              : launch_dq_d<64>(pl, lse, tq, tk, tv, tdo, dq, s);
 }
 
 }  // namespace dma

@@ -60,9 +60,13 @@ cudaError_t launch_cp_copy(const dma_plan_s& p, const void* src, void* dst, size
                            bool gather, cudaStream_t s);
 cudaError_t launch_fwd(const dma_plan_s& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, dma_bf16* o, float* lse, cudaStream_t s);
-cudaError_t launch_bwd(const dma_plan_s& p, const dma_bf16* o, const dma_bf16* dout,
-                       const float* lse, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, dma_bf16* dq, float* dk,
-                       float* dv, cudaStream_t s);
+cudaError_t launch_delta(const dma_plan_s& p, const dma_bf16* o, const dma_bf16* dout,
+                         cudaStream_t s);
+cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
+                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                        float* dk, float* dv, cudaStream_t s);
+cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
+                      const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                      dma_bf16* dq, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 }  // namespace dma

@@ -138,6 +138,24 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
                         const dma_bf16* dout, dma_bf16* dq, float* dk,
                         float* dv, void* stream);
 
+/*
+ * The three launches dma_attn_bwd makes, callable one by one (same stream
+ * order required: delta before the other two, which are independent of each
+ * other and may run on different streams once delta has completed).
+ *   dma_attn_bwd_delta: Delta = rowsum(dout * o) into the plan workspace.
+ *   dma_attn_bwd_dkdv : dk, dv (fp32, fully overwritten) from q, k, v, lse,
+ *                       dout and the plan's Delta.
+ *   dma_attn_bwd_dq   : dq (bf16) from the same inputs.
+ */
+dma_status dma_attn_bwd_delta(dma_plan_t plan, const dma_bf16* o, const dma_bf16* dout,
+                              void* stream);
+dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                             const dma_bf16* v, const float* lse, const dma_bf16* dout,
+                             float* dk, float* dv, void* stream);
+dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                           const dma_bf16* v, const float* lse, const dma_bf16* dout,
+                           dma_bf16* dq, void* stream);
+
 /* Synchronize `stream` and return the plan's device status word
  * (DMA_OK, DMA_ERR_BAD_DOCS or DMA_ERR_TIMEOUT) or DMA_ERR_CUDA. */
 dma_status dma_plan_check(dma_plan_t plan, void* stream);

@@ -80,7 +80,8 @@ def _rows_block(qb, kc, vc, mask, scale, dob):
 
 def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
               scale: float | None = None, do_local=None, rows=None,
-              block: int = 256, threads: int = 1) -> dict:
+              block: int = 256, threads: int = 1,
+              kv_grads_from_rows: bool = False) -> dict:
     """Forward (and, with ``do_local``, backward) for one CP rank.
 
     q_local, do_local : [B, Lq, Hq, D], this rank's query rows in local order
@@ -88,7 +89,9 @@ def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
     k, v              : [B, S, Hkv, D], full sequence, natural order.
     rows              : optional local row indices; then only o / lse / dq
                         of those rows are computed (others are NaN) and no
-                        dk / dv is returned (they need every row).
+                        dk / dv is returned (they need every row), unless
+                        kv_grads_from_rows: then dk / dv are the contribution
+                        of the selected rows alone.
     Returns float64 arrays: o [B,Lq,Hq,D], lse [B,Hq,Lq]; with do_local also
     dq [B,Lq,Hq,D], dk and dv [B,S,Hkv,D].
     """
@@ -106,7 +109,7 @@ def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
     assert len(qpos_all) == Lq
     ids = _cp.doc_ids(cu_doc_lens, B, S)
     sel = np.arange(Lq) if rows is None else np.sort(np.asarray(rows))
-    full = rows is None
+    full = rows is None or kv_grads_from_rows
 
     o = np.full((B, Lq, Hq, D), np.nan)
     lse = np.full((B, Hq, Lq), np.nan)
@@ -151,6 +154,8 @@ def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
             parts = list(ex.map(run_heads, groups))
 
     out = {"o": o, "lse": lse}
+    if rows is not None and full and do is not None:
+        out["kv_grads_rows"] = sel
     if do is not None:
         out["dq"] = dq
         if full:
