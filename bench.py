@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, NVIDIA's figure without sparsity
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_RANK_STEP = 11  # plan: 7, forward: 1, backward: 3
+KERNELS_PER_RANK_STEP = 12  # plan: 7, forward: 2 (V to fp16, attention), backward: 3
 
 
 # ------------------------------------------------------------------ counting
@@ -468,7 +468,7 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
         pos = torch.from_numpy(local_positions(w.seq_len, w.cp_size, r))
         h_q = inputs["q"][:, pos].contiguous().pin_memory()
         h_do = inputs["do"][:, pos].contiguous().pin_memory()
-        outs = {"o": torch.empty_like(h_q).pin_memory(),
+        outs = {"o": torch.empty(h_q.shape, dtype=torch.float32).pin_memory(),
                 "lse": torch.empty(w.batch, w.n_heads, w.local_len).pin_memory(),
                 "dq": torch.empty_like(h_q).pin_memory(),
                 "dk": torch.empty(h_k.shape, dtype=torch.float32).pin_memory(),

@@ -185,10 +185,10 @@ def dma_attn_fwd(plan: Plan, q, k, v, o=None, lse=None, stream=None):
     _expect(k, torch.bfloat16, (B, S, Hkv, D), "k")
     _expect(v, torch.bfloat16, (B, S, Hkv, D), "v")
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty(B, Lq, Hq, D, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
-    _expect(o, torch.bfloat16, (B, Lq, Hq, D), "o")
+    _expect(o, torch.float32, (B, Lq, Hq, D), "o")
     _expect(lse, torch.float32, (B, Hq, Lq), "lse")
     _check(lib().dma_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                               _stream(stream)), "dma_attn_fwd")
@@ -202,7 +202,7 @@ def dma_attn_bwd(plan: Plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, s
     _expect(q, torch.bfloat16, (B, Lq, Hq, D), "q")
     _expect(k, torch.bfloat16, (B, S, Hkv, D), "k")
     _expect(v, torch.bfloat16, (B, S, Hkv, D), "v")
-    _expect(o, torch.bfloat16, (B, Lq, Hq, D), "o")
+    _expect(o, torch.float32, (B, Lq, Hq, D), "o")
     _expect(lse, torch.float32, (B, Hq, Lq), "lse")
     _expect(dout, torch.bfloat16, (B, Lq, Hq, D), "dout")
     if dq is None:

@@ -53,8 +53,6 @@ dma_status check_shape(int batch, int seq_len, int cp_size, int cp_rank, int n_h
 
 WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int n_kv_heads,
                            int head_dim) {
-  (void)n_kv_heads;
-  (void)head_dim;
   const int g = n_heads / n_kv_heads;
   const size_t Lq = static_cast<size_t>(seq_len / cp_size);
   const size_t nqt = Lq / (dma::kTileM / g), nkt = static_cast<size_t>(seq_len) / dma::kTileN;
@@ -80,6 +78,7 @@ WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int
   w.fwd_order = take(4 * B * nqt);
   w.bwd_order = take(4 * B * nkt);
   w.delta = take(4 * B * static_cast<size_t>(n_heads) * Lq);
+  w.v16 = take(2 * B * static_cast<size_t>(seq_len) * n_kv_heads * head_dim);
   w.total = off;
   return w;
 }
@@ -112,13 +111,13 @@ dma_status map_rows_heads(CUtensorMap* m, const void* base, const dma::PlanDev& 
 }
 
 // K / V: [B*S][Hkv*D] bf16; box = 64 columns x 128 positions.
-dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p) {
+dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p,
+                  CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim,
                               static_cast<cuuint64_t>(p.batch) * p.seq_len};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim * 2};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(dma::kTileN)};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 dma_status check_device() {
@@ -196,6 +195,7 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch, int seq_l
   p.fwd_order = reinterpret_cast<int32_t*>(ws + w.fwd_order);
   p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
   p.delta = reinterpret_cast<float*>(ws + w.delta);
+  p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
   pl->cu = cu_doc_lens;
   pl->n_docs = n_docs;
   if (cudaGetDevice(&pl->device) != cudaSuccess ||
@@ -213,25 +213,24 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch, int seq_l
 }
 
 dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
-                        dma_bf16* o, float* lse, void* stream) {
+                        float* o, float* lse, void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
   const dma::PlanDev& p = plan->d;
   if (p.batch == 0) return DMA_OK;
   if (!q || !k || !v || !o || !lse) return DMA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return DMA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv16;
   dma_status st;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, p.batch * p.local_len)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
-  if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  return dma::launch_fwd(*plan, tq, tk, tv, o, lse, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? DMA_OK
-             : DMA_ERR_CUDA;
+  if ((st = map_kv(&tv16, p.v16, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != DMA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dma::launch_v_to_f16(*plan, v, s) != cudaSuccess) return DMA_ERR_CUDA;
+  return dma::launch_fwd(*plan, tq, tk, tv16, o, lse, s) == cudaSuccess ? DMA_OK : DMA_ERR_CUDA;
 }
 
-dma_status dma_attn_bwd_delta(dma_plan_t plan, const dma_bf16* o, const dma_bf16* dout,
+dma_status dma_attn_bwd_delta(dma_plan_t plan, const float* o, const dma_bf16* dout,
                               void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
   if (plan->d.batch == 0) return DMA_OK;
@@ -288,7 +287,7 @@ dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k
 }
 
 dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
-                        const dma_bf16* o, const float* lse, const dma_bf16* dout, dma_bf16* dq,
+                        const float* o, const float* lse, const dma_bf16* dout, dma_bf16* dq,
                         float* dk, float* dv, void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
   if (plan->d.batch == 0) return DMA_OK;

@@ -68,23 +68,25 @@ __device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint
 
 // ---------------------------------------------------------------- Delta
 
-// Delta[(b*Hq + h)*Lq + l] = sum_d dO[b,l,h,d] * O[b,l,h,d]; D/8 threads per row.
+// Delta[(b*Hq + h)*Lq + l] = sum_d dO[b,l,h,d] * O[b,l,h,d] (O fp32, dO bf16);
+// D/8 threads per row, 8 elements each.
 template <int D>
-__global__ void delta_kernel(const __nv_bfloat16* __restrict__ o,
-                             const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
-                             int rows, int n_heads, int local_len) {
+__global__ void delta_kernel(const float* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                             float* __restrict__ delta, int rows, int n_heads, int local_len) {
   constexpr int TPR = D / 8;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR;
   const int sub = threadIdx.x % TPR;
   float acc = 0.f;
   if (row < rows) {
-    const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[sub];
+    const float4 a0 = reinterpret_cast<const float4*>(o + row * D)[2 * sub];
+    const float4 a1 = reinterpret_cast<const float4*>(o + row * D)[2 * sub + 1];
     const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[sub];
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
-      acc = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), acc);
+      acc = fmaf(av[2 * i], __uint_as_float(bw[i] << 16), acc);
+      acc = fmaf(av[2 * i + 1], __uint_as_float(bw[i] & 0xFFFF0000u), acc);
     }
   }
 #pragma unroll
@@ -139,7 +141,10 @@ __global__ void __launch_bounds__(256, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
-  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  // K/V-head-major: CTAs resident together share a head, so the query and
+  // dO tiles they all stream stay in L2; longest lists first within a head.
+  const int nk_all = p.batch * p.n_ktiles;
+  const int kvh = blockIdx.x / nk_all, ord = blockIdx.x % nk_all;
   const int bk = p.bwd_order[ord];
   const int b = bk / p.n_ktiles, kt = bk % p.n_ktiles;
   const int cp0 = p.col_ptr[bk];
@@ -741,15 +746,14 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int D>
-cudaError_t launch_delta_d(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+cudaError_t launch_delta_d(const dma_plan_s& pl, const float* o, const dma_bf16* dout,
                            cudaStream_t s) {
   const PlanDev& p = pl.d;
   const int rows = p.batch * p.local_len * p.n_heads;
   if (rows == 0) return cudaSuccess;
   constexpr int TPR = D / 8;
   const int blocks = (rows * TPR + 255) / 256;
-  delta_kernel<D><<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(o),
-                                         reinterpret_cast<const __nv_bfloat16*>(dout), p.delta,
+  delta_kernel<D><<<blocks, 256, 0, s>>>(o, reinterpret_cast<const __nv_bfloat16*>(dout), p.delta,
                                          rows, p.n_heads, p.local_len);
   return cudaGetLastError();
 }
@@ -785,7 +789,7 @@ cudaError_t launch_dq_d(const dma_plan_s& pl, const float* lse, const CUtensorMa
 
 }  // namespace
 
-cudaError_t launch_delta(const dma_plan_s& pl, const dma_bf16* o, const dma_bf16* dout,
+cudaError_t launch_delta(const dma_plan_s& pl, const float* o, const dma_bf16* dout,
                          cudaStream_t s) {
   return pl.d.head_dim == 128 ? launch_delta_d<128>(pl, o, dout, s)
                               : launch_delta_d<64>(pl, o, dout, s);

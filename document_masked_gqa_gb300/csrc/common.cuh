@@ -36,11 +36,12 @@ struct PlanDev {
   int32_t* fwd_order; // [B*nQt]
   int32_t* bwd_order; // [B*nKt]
   float* delta;       // [B][Hq][Lq]
+  uint16_t* v16;      // [B][S][Hkv][D] fp16 copy of V for the forward's P V
 };
 
 struct WorkspaceLayout {
   size_t status, qpos, doc_lo, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
-      col_ptr, col_idx, fwd_order, bwd_order, delta, total;
+      col_ptr, col_idx, fwd_order, bwd_order, delta, v16, total;
 };
 
 }  // namespace dma
@@ -58,9 +59,10 @@ namespace dma {
 cudaError_t launch_plan_kernels(const dma_plan_s& p, cudaStream_t s);
 cudaError_t launch_cp_copy(const dma_plan_s& p, const void* src, void* dst, size_t row_bytes,
                            bool gather, cudaStream_t s);
+cudaError_t launch_v_to_f16(const dma_plan_s& p, const dma_bf16* v, cudaStream_t s);
 cudaError_t launch_fwd(const dma_plan_s& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, dma_bf16* o, float* lse, cudaStream_t s);
-cudaError_t launch_delta(const dma_plan_s& p, const dma_bf16* o, const dma_bf16* dout,
+                       const CUtensorMap& tv16, float* o, float* lse, cudaStream_t s);
+cudaError_t launch_delta(const dma_plan_s& p, const float* o, const dma_bf16* dout,
                          cudaStream_t s);
 cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,

@@ -23,9 +23,10 @@
  * Query head h uses K/V head h / (n_heads / n_kv_heads) (contiguous groups).
  *
  * Tensor layouts (all row-major, contiguous, device memory):
- *   q, o, dout, dq : [batch][2*C][n_heads][head_dim]   bf16, this rank's rows
+ *   q, dout, dq    : [batch][2*C][n_heads][head_dim]   bf16, this rank's rows
  *                    in local order: chunk cp_rank first, then chunk
  *                    2*cp_size-1-cp_rank (C = seq_len / (2*cp_size)).
+ *   o              : same layout, fp32 (see dma_attn_fwd).
  *   k, v           : [batch][seq_len][n_kv_heads][head_dim] bf16, the full
  *                    gathered sequence in natural position order.
  *   lse            : [batch][n_heads][2*C] fp32, natural log of the sum of
@@ -120,10 +121,15 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch,
 
 /*
  * Forward: o = softmax(scale * q k^T + mask) v and the row log-sum-exp.
- * One persistent-style launch; pairs of tiles classified skip issue no work.
+ * Two launches: an fp16 copy of v into the plan workspace (values beyond
+ * +-65504 saturate), then the attention kernel, in which pairs of tiles
+ * classified skip issue no work.  The probabilities enter the P V product in
+ * fp16 and o is written in fp32: a bf16 o could not hold a 1e-2 absolute
+ * error bound once |o| >= 4 (half a bf16 ulp there is 0.0156), which rows that
+ * see only a few keys of a short document reach.
  */
 dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
-                        const dma_bf16* v, dma_bf16* o, float* lse,
+                        const dma_bf16* v, float* o, float* lse,
                         void* stream);
 
 /*
@@ -134,7 +140,7 @@ dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
  * kernel.  dk and dv are fully overwritten.
  */
 dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
-                        const dma_bf16* v, const dma_bf16* o, const float* lse,
+                        const dma_bf16* v, const float* o, const float* lse,
                         const dma_bf16* dout, dma_bf16* dq, float* dk,
                         float* dv, void* stream);
 
@@ -147,7 +153,7 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
  *                       dout and the plan's Delta.
  *   dma_attn_bwd_dq   : dq (bf16) from the same inputs.
  */
-dma_status dma_attn_bwd_delta(dma_plan_t plan, const dma_bf16* o, const dma_bf16* dout,
+dma_status dma_attn_bwd_delta(dma_plan_t plan, const float* o, const dma_bf16* dout,
                               void* stream);
 dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
                              const dma_bf16* v, const float* lse, const dma_bf16* dout,
