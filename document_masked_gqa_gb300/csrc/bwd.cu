@@ -17,12 +17,16 @@
 //                 heads of the group packed in each 128-row tile, so the GQA
 //                 reduction over the group happens inside the accumulation).
 //                 TMEM: dV, dK accumulators + S^T and dP^T of the current
-//                 query tile.  Thread r of warps 4-7 owns key r.
+//                 query tile.  Warps 4-7 and 8-11: thread r of each owns key
+//                 r, the first warpgroup columns 0-63 of the query tile, the
+//                 second columns 64-127.
 //   dq_kernel     one CTA per (query tile, K/V head): Q and dO stay in shared
 //                 memory; the CTA walks the row list of key tiles.  TMEM: S,
-//                 dP and the dQ accumulator.  Thread r owns query row r.
-// Both attention kernels: warp 0 = TMA producer, warp 1 = tcgen05 issuer,
-// warps 4-7 = element-wise work, bounded waits everywhere.
+//                 dP and the dQ accumulator.  Warps 4-7 and 8-11: thread r of
+//                 each owns query row r, split over the key columns 0-63 and
+//                 64-127 of each key tile.
+// Both attention kernels: warps 0 and 2 = TMA producers, warp 1 = tcgen05
+// issuer, the rest = element-wise work, bounded waits everywhere.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -62,6 +66,16 @@ __device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint
 #pragma unroll
   for (int ch = 0; ch < 16; ++ch) {
     const uint32_t addr = base + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+  }
+}
+
+__device__ __forceinline__ void store_half_row_sw128(uint32_t region, int r, const uint32_t* pk) {
+  // 64 bf16 values (32 packed words) of row r into one 64-column region of a
+  // K-major 128-byte swizzled tile
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint32_t addr = region + r * 128 + ((ch ^ (r & 7)) << 4);
     st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
   }
 }
@@ -113,7 +127,7 @@ struct DkdvCfg {
   static constexpr int kPS = kDO + 2 * kTile;   // P^T, then dS^T (128 x 128 bf16)
   static constexpr int kCOL = kPS + 128 * 128 * 2;  // 2 stages x (lse*log2e, Delta), column order
   static constexpr int kBar = kCOL + 2 * 1024;
-  static constexpr int kNumBars = 17;
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -122,7 +136,7 @@ struct DkdvCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const PlanDev p, const float* __restrict__ lse, float* __restrict__ dk,
@@ -141,10 +155,10 @@ __global__ void __launch_bounds__(256, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
-  // K/V-head-major: CTAs resident together share a head, so the query and
-  // dO tiles they all stream stay in L2; longest lists first within a head.
-  const int nk_all = p.batch * p.n_ktiles;
-  const int kvh = blockIdx.x / nk_all, ord = blockIdx.x % nk_all;
+  // longest column lists first; the K/V heads of one key tile run side by
+  // side (measured faster than a head-major order, which crowds the
+  // resident CTAs onto the same query tiles)
+  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
   const int bk = p.bwd_order[ord];
   const int b = bk / p.n_ktiles, kt = bk % p.n_ktiles;
   const int cp0 = p.col_ptr[bk];
@@ -164,13 +178,12 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* do_full = bars + 5;   // [2]
   uint64_t* do_empty = bars + 7;  // [2]
   uint64_t* sdp_full = bars + 9;
-  uint64_t* s_free = bars + 10;
+  uint64_t* st_free = bars + 10;
   uint64_t* p_full = bars + 11;
   uint64_t* pv_done = bars + 12;
   uint64_t* ds_full = bars + 13;
   uint64_t* ds_done = bars + 14;
-  uint64_t* dp_free = bars + 15;
-  uint64_t* col_ready = bars + 16;
+  uint64_t* col_ready = bars + 15;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -183,12 +196,11 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&do_empty[i], 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(dp_free, 128);
-    mbar_init(col_ready, 128);
-    mbar_init(p_full, 128);
+    mbar_init(st_free, 256);
+    mbar_init(col_ready, 256);
+    mbar_init(p_full, 256);
     mbar_init(pv_done, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(ds_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -206,57 +218,118 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------- producer: K, V, then Q
       tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tdo);
       mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c) {
         tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, kvh * D + c * 64, krow0);
         tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, kvh * D + c * 64, krow0);
       }
-      int lastq0 = -1, lastq1 = -1, lastdo0 = -1, lastdo1 = -1;
+      int last0 = -1, last1 = -1;
       bool ok = true;
       for (int i = 0; i < n; ++i) {
         const int st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         const int qt = static_cast<int>(static_cast<uint32_t>(list[i]) & kIndexMask);
-        const int qrow = b * Lq + qt * P;
         if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64, kvh * g,
-                      qrow);
-        if (st) lastq1 = static_cast<int>(ph); else lastq0 = static_cast<int>(ph);
+                      b * Lq + qt * P);
+        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
+      }
+      if (!ok) {
+        drain_wait(kv_full, 0, 100000000ull);
+        if (last0 >= 0) drain_wait(&q_full[0], last0, 100000000ull);
+        if (last1 >= 0) drain_wait(&q_full[1], last1, 100000000ull);
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0 && n > 0) {
+      // ------------------------------------------------------ producer: dO
+      tma_prefetch_desc(&tdo);
+      int last0 = -1, last1 = -1;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int qt = static_cast<int>(static_cast<uint32_t>(list[i]) & kIndexMask);
         if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
-                      kvh * g, qrow);
-        if (st) lastdo1 = static_cast<int>(ph); else lastdo0 = static_cast<int>(ph);
+                      kvh * g, b * Lq + qt * P);
+        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
       }
       if (!ok) {
-        drain_wait(kv_full, 0, 100000000ull);
-        if (lastq0 >= 0) drain_wait(&q_full[0], lastq0, 100000000ull);
-        if (lastq1 >= 0) drain_wait(&q_full[1], lastq1, 100000000ull);
-        if (lastdo0 >= 0) drain_wait(&do_full[0], lastdo0, 100000000ull);
-        if (lastdo1 >= 0) drain_wait(&do_full[1], lastdo1, 100000000ull);
+        if (last0 >= 0) drain_wait(&do_full[0], last0, 100000000ull);
+        if (last1 >= 0) drain_wait(&do_full[1], last1, 100000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       // --------------------------------------------------------- MMA issuer
+      // per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T into TMEM;
+      // then, once the key-row warps have turned tile i into P^T and dS^T,
+      // dV += P^T dO_i and dK += dS^T Q_i.  S^T / dP^T of tile i+1 are
+      // issued as soon as tile i's have been read, ahead of tile i's dV and
+      // dK, so the tensor pipe works while the key rows compute.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ps_addr = smem_u32(sPS);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = mbar_wait(kv_full, 0, ctl);
-      auto issue_dk = [&](int i) -> bool {  // dK += dS^T Q_i
+      auto issue_sdp = [&](int i) -> bool {
         const int st = i & 1;
-        if (!mbar_wait(ds_full, i & 1, ctl)) return false;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(&q_full[st], ph, ctl)) return false;
+        if (i > 0 && !mbar_wait(st_free, (i - 1) & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
+                      sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        if (!mbar_wait(&do_full[st], ph, ctl)) return false;
+        tc_fence_after();
+        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
+                      sdesc_sw128(do_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full);
+        last_commit = sdp_full;
+        last_parity = i & 1;
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i & 1;
+        if (i + 1 < n && !issue_sdp(i + 1)) { ok = false; break; }
+        // dV += P^T dO_i
+        if (!mbar_wait(p_full, i & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemDV, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(pv_done);
+        mma_commit(&do_empty[st]);
+        last_commit = pv_done;
+        last_parity = i & 1;
+        // dK += dS^T Q_i
+        if (!mbar_wait(ds_full, i & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
 #pragma unroll
@@ -269,72 +342,32 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&q_empty[st]);
         last_commit = ds_done;
         last_parity = i & 1;
-        return true;
-      };
-      for (int i = 0; ok && i < n; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        // S^T = K Q_i^T and dP^T = V dO_i^T
-        if (!mbar_wait(&q_full[st], ph, ctl)) { ok = false; break; }
-        if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
-                      sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        if (!mbar_wait(&do_full[st], ph, ctl)) { ok = false; break; }
-        if (i > 0 && !mbar_wait(dp_free, (i - 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
-                      sdesc_sw128(do_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(sdp_full);
-        last_commit = sdp_full;
-        last_parity = i & 1;
-        if (i > 0 && !issue_dk(i - 1)) { ok = false; break; }
-        // dV += P^T dO_i
-        if (!mbar_wait(p_full, i & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemDV, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done);
-        mma_commit(&do_empty[st]);
-        last_commit = pv_done;
-        last_parity = i & 1;
       }
-      if (ok) ok = issue_dk(n - 1);
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- key rows
-    const int r = threadIdx.x - 128;
+    // two warpgroups: thread (r, half) owns key r and query-tile columns
+    // [64*half, 64*half + 64), i.e. exactly one 64-column swizzle region
+    const int r = (threadIdx.x - 128) & 127;
+    const int half = (threadIdx.x - 128) >> 7;
+    const int cbase = 64 * half;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
     const int key = kt * kTileN + r;  // position within the sample
     const float sl2 = p.scale_log2;
-    const uint32_t ps_addr = smem_u32(sPS);
+    const uint32_t ps_region = smem_u32(sPS) + half * Cfg::kRegion;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
     const int32_t* lo_b = p.doc_lo + static_cast<long long>(b) * Lq;
-    // column r of every query tile is query row (position r >> lg, head r & (g-1))
+    // column r of every query tile is query row (position r >> lg, head r & (g-1));
+    // warpgroup 0 stages LSE of column r, warpgroup 1 stages Delta
     const long long stat_base =
         (static_cast<long long>(b) * p.n_heads + kvh * g + (r & (g - 1))) * Lq + (r >> lg);
-    float nxt_lse = 0.f, nxt_del = 0.f;
-    if (n > 0) {
-      const int l1 = static_cast<int>(static_cast<uint32_t>(list[0]) & kIndexMask) * P;
-      nxt_lse = lse[stat_base + l1];
-      nxt_del = p.delta[stat_base + l1];
-    }
+    const float* stat_src = half ? p.delta : lse;
+    const float stat_mul = half ? 1.f : kLog2e;
+    float nxt = 0.f;
+    if (n > 0)
+      nxt = stat_src[stat_base + static_cast<int>(static_cast<uint32_t>(list[0]) & kIndexMask) * P];
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int st = i & 1;
@@ -355,110 +388,83 @@ __global__ void __launch_bounds__(256, 1)
         c_lo = p_first << lg;
         c_hi = lo << lg;
       }
-      // column-ordered copies of this tile's row statistics: column j is
-      // query row (position j >> lg, head j & (g-1)); thread r fills column r
-      {
-        const float cur_lse = nxt_lse, cur_del = nxt_del;
-        if (i + 1 < n) {  // prefetch the next tile's statistics for column r
-          const int l1 = static_cast<int>(static_cast<uint32_t>(list[i + 1]) & kIndexMask) * P;
-          nxt_lse = lse[stat_base + l1];
-          nxt_del = p.delta[stat_base + l1];
-        }
-        sCOL[st * 256 + r] = cur_lse * kLog2e;
-        sCOL[st * 256 + 128 + r] = cur_del;
-        mbar_arrive(col_ready);  // 128 arrivals per tile: a bounded barrier
+      {  // column-ordered row statistics of this tile, prefetched one ahead
+        const float cur = nxt;
+        if (i + 1 < n)
+          nxt = stat_src[stat_base +
+                         static_cast<int>(static_cast<uint32_t>(list[i + 1]) & kIndexMask) * P];
+        sCOL[st * 256 + half * 128 + r] = cur * stat_mul;
+        mbar_arrive(col_ready);  // 256 arrivals per tile: a bounded barrier
         if (!warp_wait(col_ready, i & 1, ctl)) { ok = false; break; }
       }
       const float4* lse_c = reinterpret_cast<const float4*>(sCOL + st * 256);
       const float4* del_c = reinterpret_cast<const float4*>(sCOL + st * 256 + 128);
-      // pass 1: P^T row from S^T (needs only S^T)
       if (!warp_wait(sdp_full, i & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[64];
+      // one pass: P^T = exp(scale S^T - LSE), dS^T = P^T (dP^T - Delta)
+      uint32_t pk[32], pd[32];
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float s[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemS + c0, s);
-        const uint32_t allow = range_bits(c_lo - c0, c_hi - c0);
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        const int cg = cbase + c0;  // column of the query tile
+        uint32_t su[16], du[16];
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDP + cg, du);
+        tmem_wait_ld();
+        reg_fence16(su);
+        reg_fence16(du);
+        const uint32_t allow = range_bits(c_lo - cg, c_hi - cg);
 #pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = lse_c[(c0 + t) >> 2];
+        for (int t = 0; t < 16; t += 4) {
+          const float4 l4 = lse_c[(cg + t) >> 2];
+          const float4 d4 = del_c[(cg + t) >> 2];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float pv[4];
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dv4[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            pv[u] = ((allow >> (t + u)) & 1u) ? ex2(fmaf(s[t + u], sl2, -lv[u])) : 0.f;
+          for (int u = 0; u < 4; ++u) {
+            pv[u] = ((allow >> (t + u)) & 1u)
+                        ? ex2(fmaf(__uint_as_float(su[t + u]), sl2, -lv[u]))
+                        : 0.f;
+            dv4[u] = pv[u] * (__uint_as_float(du[t + u]) - dl[u]);
+          }
           pk[(c0 + t) >> 1] = pack_bf16(pv[0], pv[1]);
           pk[((c0 + t) >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+          pd[(c0 + t) >> 1] = pack_bf16(dv4[0], dv4[1]);
+          pd[((c0 + t) >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
         }
+        reg_fence8(pk + (c0 >> 1));
+        reg_fence8(pd + (c0 >> 1));
       }
       tc_fence_before();
-      mbar_arrive(s_free);
+      mbar_arrive(st_free);  // S^T and dP^T of this tile have been read
       if (i > 0 && !warp_wait(ds_done, (i - 1) & 1, ctl)) { ok = false; break; }
-      store_row_sw128(ps_addr, r, pk);
+      store_half_row_sw128(ps_region, r, pk);
       fence_proxy_async_smem();
       mbar_arrive(p_full);
-      // pass 2: dS^T = P^T * (dP^T - Delta), P^T read back from this thread's
-      // own row once dV has consumed it, dS^T written in its place
       if (!warp_wait(pv_done, i & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float dp[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemDP + c0, dp);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // four 16-byte chunks of 8 columns
-          const int ch = (c0 >> 3) + q;
-          const uint32_t addr =
-              ps_addr + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          uint32_t w[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                       : "r"(addr));
-          uint32_t o4[4];
-          const float4 d0 = del_c[(c0 + 8 * q) >> 2];
-          const float4 d1 = del_c[((c0 + 8 * q) >> 2) + 1];
-          const float dl[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = __uint_as_float(w[e] << 16);
-            const float p1 = __uint_as_float(w[e] & 0xFFFF0000u);
-            o4[e] = pack_bf16(p0 * (dp[8 * q + 2 * e] - dl[2 * e]),
-                              p1 * (dp[8 * q + 2 * e + 1] - dl[2 * e + 1]));
-          }
-          st_shared_v4(addr, o4[0], o4[1], o4[2], o4[3]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dp_free);
+      store_half_row_sw128(ps_region, r, pd);
       fence_proxy_async_smem();
       mbar_arrive(ds_full);
     }
+    // warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
     const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
-    float4* dv_dst = reinterpret_cast<float4*>(dv + out_row * D);
-    float4* dk_dst = reinterpret_cast<float4*>(dk + out_row * D);
+    float4* dst = reinterpret_cast<float4*>((half ? dk : dv) + out_row * D);
     if (n == 0) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int c = 0; c < D / 4; ++c) {
-        dv_dst[c] = z;
-        dk_dst[c] = z;
-      }
+      for (int c = 0; c < D / 4; ++c) dst[c] = z;
     } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
       tc_fence_after();
-      const float sc = p.scale;
+      const float sc = half ? p.scale : 1.f;
+      const uint32_t acc = tmem + lane_base + (half ? Cfg::kTmemDK : Cfg::kTmemDV);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float t[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemDV + c0, t);
+        tmem_ld32(acc + c0, t);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          dv_dst[c0 / 4 + q4] = make_float4(t[4 * q4], t[4 * q4 + 1], t[4 * q4 + 2], t[4 * q4 + 3]);
-        tmem_ld32(tmem + lane_base + Cfg::kTmemDK + c0, t);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          dk_dst[c0 / 4 + q4] = make_float4(t[4 * q4] * sc, t[4 * q4 + 1] * sc,
-                                            t[4 * q4 + 2] * sc, t[4 * q4 + 3] * sc);
+          dst[c0 / 4 + q4] = make_float4(t[4 * q4] * sc, t[4 * q4 + 1] * sc, t[4 * q4 + 2] * sc,
+                                         t[4 * q4 + 3] * sc);
       }
     }
   }
@@ -493,7 +499,7 @@ struct DqCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
               const PlanDev p, const float* __restrict__ lse, __nv_bfloat16* __restrict__ dq) {
@@ -546,8 +552,8 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(st_free, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(st_free, 256);
+    mbar_init(ds_full, 256);
     mbar_init(ds_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -564,76 +570,74 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------ producer: Q, dO, then K
       tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
       mbar_arrive_expect_tx(q_full, 2 * Cfg::kTile);
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c) {
         tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
         tma_load_3d(sDO + c * Cfg::kRegion, &tdo, q_full, c * 64, kvh * g, b * Lq + l0);
       }
-      int lastk0 = -1, lastk1 = -1, lastv0 = -1, lastv1 = -1;
+      int last0 = -1, last1 = -1;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        const int krow = b * p.seq_len + kt * kTileN;
         if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[st], Cfg::kTile);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_2d(sK + st * Cfg::kTile + c * Cfg::kRegion, &tk, &k_full[st], kvh * D + c * 64,
-                      krow);
-        if (st) lastk1 = static_cast<int>(ph); else lastk0 = static_cast<int>(ph);
+                      b * p.seq_len + kt * kTileN);
+        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
+      }
+      if (!ok) {
+        drain_wait(q_full, 0, 100000000ull);
+        if (last0 >= 0) drain_wait(&k_full[0], last0, 100000000ull);
+        if (last1 >= 0) drain_wait(&k_full[1], last1, 100000000ull);
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0 && n > 0) {
+      // ------------------------------------------------------ producer: V
+      tma_prefetch_desc(&tv);
+      int last0 = -1, last1 = -1;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
         if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[st], Cfg::kTile);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_2d(sV + st * Cfg::kTile + c * Cfg::kRegion, &tv, &v_full[st], kvh * D + c * 64,
-                      krow);
-        if (st) lastv1 = static_cast<int>(ph); else lastv0 = static_cast<int>(ph);
+                      b * p.seq_len + kt * kTileN);
+        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
       }
       if (!ok) {
-        drain_wait(q_full, 0, 100000000ull);
-        if (lastk0 >= 0) drain_wait(&k_full[0], lastk0, 100000000ull);
-        if (lastk1 >= 0) drain_wait(&k_full[1], lastk1, 100000000ull);
-        if (lastv0 >= 0) drain_wait(&v_full[0], lastv0, 100000000ull);
-        if (lastv1 >= 0) drain_wait(&v_full[1], lastv1, 100000000ull);
+        if (last0 >= 0) drain_wait(&v_full[0], last0, 100000000ull);
+        if (last1 >= 0) drain_wait(&v_full[1], last1, 100000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       // --------------------------------------------------------- MMA issuer
+      // per key tile j: S = Q K_j^T and dP = dO V_j^T into TMEM; once the row
+      // warps have turned them into dS: dQ += dS K_j.  S / dP of tile j+1 go
+      // out as soon as tile j's have been read, ahead of tile j's dQ.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), ds_addr = smem_u32(sDS);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_full, 0, ctl);
-      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j
-        const int st = j & 1;
-        if (!mbar_wait(ds_full, j & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(ds_done);
-        mma_commit(&k_empty[st]);
-        last_commit = ds_done;
-        last_parity = j & 1;
-        return true;
-      };
-      for (int j = 0; ok && j < n; ++j) {
+      auto issue_sdp = [&](int j) -> bool {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
-        if (j > 0 && !mbar_wait(st_free, (j - 1) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], ph, ctl)) return false;
+        if (j > 0 && !mbar_wait(st_free, (j - 1) & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
 #pragma unroll
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(256, 1)
           mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(q_addr + off, 16, 1024),
                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (!mbar_wait(&v_full[st], ph, ctl)) { ok = false; break; }
+        if (!mbar_wait(&v_full[st], ph, ctl)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + st * Cfg::kTile);
 #pragma unroll
@@ -655,14 +659,35 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&v_empty[st]);
         last_commit = sdp_full;
         last_parity = j & 1;
-        if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j & 1;
+        if (j + 1 < n && !issue_sdp(j + 1)) { ok = false; break; }
+        if (!mbar_wait(ds_full, j & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
+          mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(ds_done);
+        mma_commit(&k_empty[st]);
+        last_commit = ds_done;
+        last_parity = j & 1;
       }
-      if (ok) ok = issue_dq(n - 1);
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- query rows
-    const int r = threadIdx.x - 128;
+    // two warpgroups: thread (r, half) owns query row r and key columns
+    // [64*half, 64*half + 64) of each key tile (one 64-column swizzle region)
+    const int r = (threadIdx.x - 128) & 127;
+    const int half = (threadIdx.x - 128) >> 7;
+    const int cbase = 64 * half;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
     const int pos = r >> lg, h = r & (g - 1);
@@ -675,7 +700,7 @@ __global__ void __launch_bounds__(256, 1)
     const float lse2 = lse[stat] * kLog2e;
     const float del = p.delta[stat];
     const float sl2 = p.scale_log2;
-    const uint32_t ds_addr = smem_u32(sDS);
+    const uint32_t ds_region = smem_u32(sDS) + half * Cfg::kRegion;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t e = static_cast<uint32_t>(list[j]);
@@ -687,51 +712,62 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (!warp_wait(sdp_full, j & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float s[32], dp[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemS + c0, s);
-        tmem_ld32(tmem + lane_base + Cfg::kTmemDP + c0, dp);
-        const uint32_t allow = range_bits(c_lo - c0, c_hi - c0);
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        const int cg = cbase + c0;
+        uint32_t su[16], du[16];
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDP + cg, du);
+        tmem_wait_ld();
+        reg_fence16(su);
+        reg_fence16(du);
+        const uint32_t allow = range_bits(c_lo - cg, c_hi - cg);
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
+        for (int t = 0; t < 16; t += 2) {
           float dsv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float pj = ((allow >> (t + u)) & 1u) ? ex2(fmaf(s[t + u], sl2, -lse2)) : 0.f;
-            dsv[u] = pj * (dp[t + u] - del);
+            const float pj = ((allow >> (t + u)) & 1u)
+                                 ? ex2(fmaf(__uint_as_float(su[t + u]), sl2, -lse2))
+                                 : 0.f;
+            dsv[u] = pj * (__uint_as_float(du[t + u]) - del);
           }
           pk[(c0 + t) >> 1] = pack_bf16(dsv[0], dsv[1]);
         }
+        reg_fence8(pk + (c0 >> 1));
       }
       tc_fence_before();
       mbar_arrive(st_free);
       if (j > 0 && !warp_wait(ds_done, (j - 1) & 1, ctl)) { ok = false; break; }
-      store_row_sw128(ds_addr, r, pk);
+      store_half_row_sw128(ds_region, r, pk);
       fence_proxy_async_smem();
       mbar_arrive(ds_full);
     }
+    // each warpgroup writes half of the row's head_dim columns
+    constexpr int DH = D / 2;
     uint4* dst = reinterpret_cast<uint4*>(
-        dq + ((static_cast<long long>(b) * Lq + l) * p.n_heads + hq) * D);
+        dq + ((static_cast<long long>(b) * Lq + l) * p.n_heads + hq) * D + half * DH);
     if (n == 0) {
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < DH / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
     } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
       tc_fence_after();
       const float sc = p.scale;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float t[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemDQ + c0, t);
+      for (int c0 = 0; c0 < DH; c0 += 16) {
+        uint32_t u[16];
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDQ + half * DH + c0, u);
+        tmem_wait_ld();
+        reg_fence16(u);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 u;
-          u.x = pack_bf16(t[8 * q4 + 0] * sc, t[8 * q4 + 1] * sc);
-          u.y = pack_bf16(t[8 * q4 + 2] * sc, t[8 * q4 + 3] * sc);
-          u.z = pack_bf16(t[8 * q4 + 4] * sc, t[8 * q4 + 5] * sc);
-          u.w = pack_bf16(t[8 * q4 + 6] * sc, t[8 * q4 + 7] * sc);
-          dst[c0 / 8 + q4] = u;
+        for (int q2 = 0; q2 < 2; ++q2) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(u[8 * q2 + 0]) * sc, __uint_as_float(u[8 * q2 + 1]) * sc);
+          w.y = pack_bf16(__uint_as_float(u[8 * q2 + 2]) * sc, __uint_as_float(u[8 * q2 + 3]) * sc);
+          w.z = pack_bf16(__uint_as_float(u[8 * q2 + 4]) * sc, __uint_as_float(u[8 * q2 + 5]) * sc);
+          w.w = pack_bf16(__uint_as_float(u[8 * q2 + 6]) * sc, __uint_as_float(u[8 * q2 + 7]) * sc);
+          dst[c0 / 8 + q2] = w;
         }
       }
     }
@@ -768,7 +804,7 @@ cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensor
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DkdvCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<grid, 256, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse, dk, dv);
+  dkdv_kernel<D><<<grid, 384, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse, dk, dv);
   return cudaGetLastError();
 }
 
@@ -782,7 +818,7 @@ cudaError_t launch_dq_d(const dma_plan_s& pl, const float* lse, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DqCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dq_kernel<D><<<grid, 256, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse,
+  dq_kernel<D><<<grid, 384, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse,
                                                    reinterpret_cast<__nv_bfloat16*>(dq));
   return cudaGetLastError();
 }

@@ -11,10 +11,12 @@
 // score matrix", sections "Online softmax" and "Tiling").
 //
 // GB300 mapping (sm_103a):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring
+//   warp 0      TMA producer: Q once, then K tiles into a 3-stage ring
+//   warp 2      TMA producer: V tiles into a 2-stage ring (decoupled from K,
+//               so a K load never queues behind the release of a V slot)
 //   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers,
 //               O += P V into a TMEM accumulator; owns the TMEM allocation
-//   warps 2-3   load the tile's positions / document starts, then idle
+//   warps 2-3   load the tile's positions / document starts first
 //   warps 4-7   softmax: thread r owns row r (TMEM lane r): masks partial
 //               tiles, exponentiates in base 2, writes P (fp16) to shared
 //               memory in the 128-byte-swizzled K-major layout, rescales O in
@@ -35,22 +37,24 @@ namespace {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = 2;
+  static constexpr int kStagesK = 3;
+  static constexpr int kStagesV = 2;
   static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (bf16)
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kV = kK + kStagesK * kTileBytes;
+  static constexpr int kP = kV + kStagesV * kTileBytes;
   static constexpr int kPBytes = 128 * 128 * 2;
   static constexpr int kBar = kP + kPBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2;
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+  static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
 };
 
 // Wait for a phase ignoring the abort flag, bounded by limit_ns (used only to
@@ -68,16 +72,14 @@ __global__ void __launch_bounds__(256, 1)
                const __grid_constant__ CUtensorMap tv, const PlanDev p,
                float* __restrict__ o, float* __restrict__ lse) {
   using Cfg = FwdCfg<D>;
-  constexpr int S = Cfg::kStages;
+  constexpr int SK = Cfg::kStagesK, SV = Cfg::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  {  // a failed plan or an earlier expired wait: do nothing (CTA-uniform)
-    __shared__ uint32_t s_status;
-    if (threadIdx.x == 0) s_status = *reinterpret_cast<volatile uint32_t*>(p.status);
-    __syncthreads();
-    if (s_status != 0u) return;
-  }
+  // a failed plan or an earlier expired wait: do nothing (CTA-uniform)
+  if (__syncthreads_or(threadIdx.x == 0 &&
+                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u))
+    return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
@@ -96,10 +98,10 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + S;
-  uint64_t* v_full = k_empty + S;
-  uint64_t* v_empty = v_full + S;
-  uint64_t* s_full = v_empty + S;
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* s_full = v_empty + SV;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
@@ -110,9 +112,11 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < S; ++i) {
+    for (int i = 0; i < SK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < SV; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -143,44 +147,64 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------------- producer: Q, then K
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      int last_phase_k[S], last_phase_v[S];
+      int last_k[SK];
 #pragma unroll
-      for (int i = 0; i < S; ++i) last_phase_k[i] = last_phase_v[i] = -1;
+      for (int i = 0; i < SK; ++i) last_k[i] = -1;
       mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c)
         tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        const int st = j % S;
-        const uint32_t ph = (j / S) & 1;
+        const int st = j % SK;
+        const uint32_t ph = (j / SK) & 1;
         const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        const int krow = b * p.seq_len + kt * kTileN;
         if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[st], Cfg::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_2d(sK + st * Cfg::kTileBytes + c * Cfg::kRegion, &tk, &k_full[st],
-                      kvh * D + c * 64, krow);
-        last_phase_k[st] = static_cast<int>(ph);
+                      kvh * D + c * 64, b * p.seq_len + kt * kTileN);
+#pragma unroll
+        for (int i = 0; i < SK; ++i)
+          if (i == st) last_k[i] = static_cast<int>(ph);
+      }
+      if (!ok) {  // drain our own copies before the CTA exits
+        drain_wait(q_full, 0, 100000000ull);
+#pragma unroll
+        for (int i = 0; i < SK; ++i)
+          if (last_k[i] >= 0) drain_wait(&k_full[i], last_k[i], 100000000ull);
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer: V
+      tma_prefetch_desc(&tv);
+      int last_v[SV];
+#pragma unroll
+      for (int i = 0; i < SV; ++i) last_v[i] = -1;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % SV;
+        const uint32_t ph = (j / SV) & 1;
+        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
         if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[st], Cfg::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_2d(sV + st * Cfg::kTileBytes + c * Cfg::kRegion, &tv, &v_full[st],
-                      kvh * D + c * 64, krow);
-        last_phase_v[st] = static_cast<int>(ph);
+                      kvh * D + c * 64, b * p.seq_len + kt * kTileN);
+#pragma unroll
+        for (int i = 0; i < SV; ++i)
+          if (i == st) last_v[i] = static_cast<int>(ph);
       }
-      if (!ok) {  // drain our own copies before the CTA exits
-        drain_wait(q_full, 0, 100000000ull);
-        for (int i = 0; i < S; ++i) {
-          if (last_phase_k[i] >= 0) drain_wait(&k_full[i], last_phase_k[i], 100000000ull);
-          if (last_phase_v[i] >= 0) drain_wait(&v_full[i], last_phase_v[i], 100000000ull);
-        }
+      if (!ok) {
+#pragma unroll
+        for (int i = 0; i < SV; ++i)
+          if (last_v[i] >= 0) drain_wait(&v_full[i], last_v[i], 100000000ull);
       }
     }
   } else if (warp == 1) {
@@ -193,8 +217,8 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_full, 0, ctl);
       auto issue_pv = [&](int i) -> bool {
-        const int st = i % S;
-        const uint32_t ph = (i / S) & 1;
+        const int st = i % SV;
+        const uint32_t ph = (i / SV) & 1;
         if (!mbar_wait(p_full, i & 1, ctl)) return false;
         if (!mbar_wait(&v_full[st], ph, ctl)) return false;
         tc_fence_after();
@@ -213,8 +237,8 @@ __global__ void __launch_bounds__(256, 1)
         return true;
       };
       for (int j = 0; ok && j < n; ++j) {
-        const int st = j % S;
-        const uint32_t ph = (j / S) & 1;
+        const int st = j % SK;
+        const uint32_t ph = (j / SK) & 1;
         const int sb = j & 1;
         if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
         if (!mbar_wait(&s_free[sb], ((j >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
@@ -255,11 +279,21 @@ __global__ void __launch_bounds__(256, 1)
       }
       tc_fence_after();
       float s[128];
-      const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
-      tmem_ld32(sc, s);
-      tmem_ld32(sc + 32, s + 32);
-      tmem_ld32(sc + 64, s + 64);
-      tmem_ld32(sc + 96, s + 96);
+      {
+        const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+        uint32_t u[128];
+        tmem_ld32_nowait(sc, u);
+        tmem_ld32_nowait(sc + 32, u + 32);
+        tmem_ld32_nowait(sc + 64, u + 64);
+        tmem_ld32_nowait(sc + 96, u + 96);
+        tmem_wait_ld();
+        reg_fence32(u);
+        reg_fence32(u + 32);
+        reg_fence32(u + 64);
+        reg_fence32(u + 96);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+      }
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
       const uint32_t e = static_cast<uint32_t>(list[j]);
