@@ -67,6 +67,7 @@ WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int
   w.status = take(16);
   w.qpos = take(4 * Lq);
   w.doc_lo = take(4 * B * Lq);
+  w.doc_hi = take(4 * B * static_cast<size_t>(seq_len));
   w.chunk_order = take(4 * 2 * static_cast<size_t>(cp_size));
   w.tile_class = take(B * nqt * nkt);
   w.row_cnt = take(4 * B * nqt);
@@ -184,6 +185,7 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch, int seq_l
   p.status = reinterpret_cast<uint32_t*>(ws + w.status);
   p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
   p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
+  p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);
   p.chunk_order = reinterpret_cast<int32_t*>(ws + w.chunk_order);
   p.tile_class = ws + w.tile_class;
   p.row_cnt = reinterpret_cast<int32_t*>(ws + w.row_cnt);

@@ -59,6 +59,9 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
 }
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
+}
 
 __device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint32_t* pk) {
   // one 128-element bf16 row (64 packed words) into a K-major 128-byte
@@ -349,6 +352,10 @@ __global__ void __launch_bounds__(384, 1)
     // ----------------------------------------------------------- key rows
     // two warpgroups: thread (r, half) owns key r and query-tile columns
     // [64*half, 64*half + 64), i.e. exactly one 64-column swizzle region
+    // barriers by shared-window offset (fewer registers than generic pointers)
+    const uint32_t b_col = smem_u32(col_ready), b_sdp = smem_u32(sdp_full),
+                   b_st = smem_u32(st_free), b_dsd = smem_u32(ds_done), b_pf = smem_u32(p_full),
+                   b_pv = smem_u32(pv_done), b_dsf = smem_u32(ds_full);
     const int r = (threadIdx.x - 128) & 127;
     const int half = (threadIdx.x - 128) >> 7;
     const int cbase = 64 * half;
@@ -358,48 +365,44 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     const uint32_t ps_region = smem_u32(sPS) + half * Cfg::kRegion;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
-    const int32_t* lo_b = p.doc_lo + static_cast<long long>(b) * Lq;
+    // queries that may attend this key: positions [key, doc_end)
+    const int doc_end = p.doc_hi[static_cast<long long>(b) * p.seq_len + key];
     // column r of every query tile is query row (position r >> lg, head r & (g-1));
     // warpgroup 0 stages LSE of column r, warpgroup 1 stages Delta
     const long long stat_base =
         (static_cast<long long>(b) * p.n_heads + kvh * g + (r & (g - 1))) * Lq + (r >> lg);
     const float* stat_src = half ? p.delta : lse;
     const float stat_mul = half ? 1.f : kLog2e;
+    // list entries run two tiles ahead, statistics one tile ahead
+    uint32_t e_next = n > 1 ? static_cast<uint32_t>(list[1]) : 0u;
+    uint32_t e = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
     float nxt = 0.f;
-    if (n > 0)
-      nxt = stat_src[stat_base + static_cast<int>(static_cast<uint32_t>(list[0]) & kIndexMask) * P];
+    if (n > 0) nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int st = i & 1;
-      const uint32_t e = static_cast<uint32_t>(list[i]);
       const int qt = static_cast<int>(e & kIndexMask);
-      // allowed query positions of this key form one range of the tile's
-      // positions: p_first..p_last (columns p_first*g .. (p_last+1)*g - 1)
+      // allowed query positions of this key in the tile: [key, doc_end), i.e.
+      // tile positions p_first .. p_end-1 = columns p_first*g .. p_end*g - 1
       int c_lo = 0, c_hi = 128;
       if (e & kPartialBit) {
         const int l0 = qt * P;
         const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
-        const int p_first = max(0, key - q0);
-        int lo = 0, hi = P;  // count of positions with doc_lo <= key
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (lo_b[l0 + mid] <= key) lo = mid + 1; else hi = mid;
-        }
-        c_lo = p_first << lg;
-        c_hi = lo << lg;
+        c_lo = max(0, key - q0) << lg;
+        c_hi = min(P, max(0, doc_end - q0)) << lg;
       }
+      e = e_next;
+      if (i + 2 < n) e_next = static_cast<uint32_t>(list[i + 2]);
       {  // column-ordered row statistics of this tile, prefetched one ahead
         const float cur = nxt;
-        if (i + 1 < n)
-          nxt = stat_src[stat_base +
-                         static_cast<int>(static_cast<uint32_t>(list[i + 1]) & kIndexMask) * P];
+        if (i + 1 < n) nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
         sCOL[st * 256 + half * 128 + r] = cur * stat_mul;
-        mbar_arrive(col_ready);  // 256 arrivals per tile: a bounded barrier
-        if (!warp_wait(col_ready, i & 1, ctl)) { ok = false; break; }
+        mbar_arrive(b_col);  // 256 arrivals per tile: a bounded barrier
+        if (!warp_wait(b_col, i & 1, ctl)) { ok = false; break; }
       }
       const float4* lse_c = reinterpret_cast<const float4*>(sCOL + st * 256);
       const float4* del_c = reinterpret_cast<const float4*>(sCOL + st * 256 + 128);
-      if (!warp_wait(sdp_full, i & 1, ctl)) { ok = false; break; }
+      if (!warp_wait(b_sdp, i & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       // one pass: P^T = exp(scale S^T - LSE), dS^T = P^T (dP^T - Delta)
       uint32_t pk[32], pd[32];
@@ -436,15 +439,15 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence8(pd + (c0 >> 1));
       }
       tc_fence_before();
-      mbar_arrive(st_free);  // S^T and dP^T of this tile have been read
-      if (i > 0 && !warp_wait(ds_done, (i - 1) & 1, ctl)) { ok = false; break; }
+      mbar_arrive(b_st);  // S^T and dP^T of this tile have been read
+      if (i > 0 && !warp_wait(b_dsd, (i - 1) & 1, ctl)) { ok = false; break; }
       store_half_row_sw128(ps_region, r, pk);
       fence_proxy_async_smem();
-      mbar_arrive(p_full);
-      if (!warp_wait(pv_done, i & 1, ctl)) { ok = false; break; }
+      mbar_arrive(b_pf);
+      if (!warp_wait(b_pv, i & 1, ctl)) { ok = false; break; }
       store_half_row_sw128(ps_region, r, pd);
       fence_proxy_async_smem();
-      mbar_arrive(ds_full);
+      mbar_arrive(b_dsf);
     }
     // warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
     const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
@@ -453,18 +456,21 @@ __global__ void __launch_bounds__(384, 1)
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
       for (int c = 0; c < D / 4; ++c) dst[c] = z;
-    } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
+    } else if (ok && warp_wait(b_dsd, (n - 1) & 1, ctl)) {
       tc_fence_after();
       const float sc = half ? p.scale : 1.f;
       const uint32_t acc = tmem + lane_base + (half ? Cfg::kTmemDK : Cfg::kTmemDV);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t t[16];
+        tmem_ld16_nowait(acc + c0, t);
+        tmem_wait_ld();
+        reg_fence16(t);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float t[32];
-        tmem_ld32(acc + c0, t);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          dst[c0 / 4 + q4] = make_float4(t[4 * q4] * sc, t[4 * q4 + 1] * sc, t[4 * q4 + 2] * sc,
-                                         t[4 * q4 + 3] * sc);
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[c0 / 4 + q4] =
+              make_float4(__uint_as_float(t[4 * q4]) * sc, __uint_as_float(t[4 * q4 + 1]) * sc,
+                          __uint_as_float(t[4 * q4 + 2]) * sc, __uint_as_float(t[4 * q4 + 3]) * sc);
       }
     }
   }
@@ -702,8 +708,10 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     const uint32_t ds_region = smem_u32(sDS) + half * Cfg::kRegion;
     bool ok = true;
+    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
     for (int j = 0; j < n; ++j) {
-      const uint32_t e = static_cast<uint32_t>(list[j]);
+      const uint32_t e = e_next;  // list entries run one tile ahead
+      if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
       int c_lo = 0, c_hi = 128;
       if (e & kPartialBit) {
         const int k0 = static_cast<int>(e & kIndexMask) * kTileN;

@@ -25,6 +25,7 @@ struct PlanDev {
   uint32_t* status;
   int32_t* qpos;      // [Lq]
   int32_t* doc_lo;    // [B][Lq]
+  int32_t* doc_hi;    // [B][S] end (exclusive) of each key position's document
   int32_t* chunk_order;
   uint8_t* tile_class;  // [B][nQt][nKt]
   int32_t* row_cnt;   // [B*nQt]
@@ -40,7 +41,7 @@ struct PlanDev {
 };
 
 struct WorkspaceLayout {
-  size_t status, qpos, doc_lo, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
+  size_t status, qpos, doc_lo, doc_hi, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
       col_ptr, col_idx, fwd_order, bwd_order, delta, v16, total;
 };
 

@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(256, 1)
     const float sl2 = p.scale_log2;
     const uint32_t p_addr = smem_u32(sP);
     float m_run = -INFINITY, l_run = 0.f;
+    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
@@ -296,7 +297,8 @@ __global__ void __launch_bounds__(256, 1)
       }
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
-      const uint32_t e = static_cast<uint32_t>(list[j]);
+      const uint32_t e = e_next;  // list entries run one tile ahead
+      if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
       if (e & kPartialBit) {
         const int k0 = static_cast<int>(e & kIndexMask) * kTileN;
         const int lo_c = lo_r - k0, hi_c = qabs - k0;

@@ -75,6 +75,22 @@ __global__ void plan_positions_kernel(PlanDev p, const int32_t* __restrict__ cu,
     if (start > pos) start = pos;
     p.doc_lo[i] = static_cast<int32_t>(start);
   }
+
+  // --- end (exclusive) of the document of every key position of every sample
+  const long long nk = static_cast<long long>(p.batch) * S;
+  for (long long i = tid; i < nk; i += nthreads) {
+    const int b = static_cast<int>(i / S);
+    const int pos = static_cast<int>(i % S);
+    int lo = 0, hi = n_docs - 1;  // last d with cu[d] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    long long end = static_cast<long long>(cu[lo + 1]) - static_cast<long long>(b) * S;
+    if (end <= pos) end = pos + 1;  // malformed table: keep the range sane
+    if (end > S) end = S;
+    p.doc_hi[i] = static_cast<int32_t>(end);
+  }
 }
 
 // grid (n_qtiles, batch), block 128
@@ -241,7 +257,7 @@ cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   e = cudaMemsetAsync(p.col_cnt, 0, sizeof(int32_t) * p.batch * p.n_ktiles, s);
   if (e != cudaSuccess) return e;
-  const long long n = static_cast<long long>(p.batch) * p.local_len;
+  const long long n = static_cast<long long>(p.batch) * p.seq_len;
   int blocks = static_cast<int>((n + 255) / 256);
   if (blocks > 4 * pl.num_sms) blocks = 4 * pl.num_sms;
   if (blocks < 1) blocks = 1;
