@@ -29,6 +29,7 @@ EXPORTED = [
     "dma_plan_check", "dma_plan_destroy", "dma_status_str", "dma_cp_gather",
     "dma_cp_scatter", "dma_plan_get_view", "dma_plan_set_wait_timeout",
     "dma_debug_wait_probe", "dma_attn_bwd_delta", "dma_attn_bwd_dkdv", "dma_attn_bwd_dq",
+    "dma_attn_fwd_noalloc",
 ]
 
 
@@ -73,6 +74,8 @@ def _load():
         "dma_attn_bwd_delta": (i32, [vp] * 4),
         "dma_attn_bwd_dkdv": (i32, [vp] * 9),
         "dma_attn_bwd_dq": (i32, [vp] * 8),
+        "dma_attn_fwd_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, i32, f32] +
+                                 [vp] * 7),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)

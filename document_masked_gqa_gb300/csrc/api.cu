@@ -401,3 +401,120 @@ dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev, void*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.
+//
+// For callers that cannot allocate device memory at all: code running where
+// the allocator is off limits (inside a framework's memory pool that it must
+// not grow, a plugin host that forbids cudaMalloc, or a process that has to
+// keep its footprint fixed).  Every other entry point needs a caller-owned
+// plan workspace; this one builds the plan and the fp16 copy of V in a fixed
+// scratch array compiled into the library instead.
+namespace {
+
+// 64 MiB of scratch per device, held by every GPU that loads the library
+// until the process exits.  Fits the plan plus the fp16 V copy of, e.g., an
+// 8K-token batch of 2 with 8 K/V heads of 128, or one 128K-token sample with
+// one K/V head of 128.
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// In host code `g_noalloc_scratch` is only a stand-in for the symbol, not a
+// device address: its device address is looked up once per device, with
+// that device current.
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_ptr[kNoAllocMaxDevices];
+cudaError_t g_noalloc_err[kNoAllocMaxDevices];
+std::once_flag g_noalloc_once[kNoAllocMaxDevices];
+
+}  // namespace
+
+extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_docs, int batch,
+                                           int seq_len, int cp_size, int cp_rank, int n_heads,
+                                           int n_kv_heads, int head_dim, float softmax_scale,
+                                           const dma_bf16* q, const dma_bf16* k,
+                                           const dma_bf16* v, float* o, float* lse,
+                                           uint32_t* status_dev, void* stream) {
+  const dma_status sh = check_shape(batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim);
+  if (sh != DMA_OK) return sh;
+  if (batch == 0) return DMA_OK;
+  if (!cu_doc_lens || n_docs < 1 || !q || !k || !v || !o || !lse) return DMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return DMA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return DMA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = layout_for(batch, seq_len, cp_size, n_heads, n_kv_heads, head_dim);
+  if (w.total > kNoAllocScratchBytes) return DMA_ERR_WORKSPACE;  // shape needs > 64 MiB
+  const dma_status dv = check_device();
+  if (dv != DMA_OK) return dv;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DMA_ERR_UNSUPPORTED;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+  });
+  if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return DMA_ERR_CUDA;
+
+  // the plan lives on this stack frame and in the scratch array
+  dma_plan_s pl{};
+  dma::PlanDev& p = pl.d;
+  p.batch = batch;
+  p.seq_len = seq_len;
+  p.cp_size = cp_size;
+  p.cp_rank = cp_rank;
+  p.n_heads = n_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.head_dim = head_dim;
+  p.chunk = seq_len / (2 * cp_size);
+  p.local_len = 2 * p.chunk;
+  p.group = n_heads / n_kv_heads;
+  p.tile_pos = dma::kTileM / p.group;
+  p.n_qtiles = p.local_len / p.tile_pos;
+  p.n_ktiles = seq_len / dma::kTileN;
+  p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.timeout_ns = 2000000000ull;
+  if (const char* env = std::getenv("DMA_WAIT_TIMEOUT_NS")) {
+    const unsigned long long t = std::strtoull(env, nullptr, 10);
+    if (t > 0) p.timeout_ns = t;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(g_noalloc_ptr[dev]);
+  p.status = reinterpret_cast<uint32_t*>(ws + w.status);
+  p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
+  p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
+  p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);
+  p.chunk_order = reinterpret_cast<int32_t*>(ws + w.chunk_order);
+  p.tile_class = ws + w.tile_class;
+  p.row_cnt = reinterpret_cast<int32_t*>(ws + w.row_cnt);
+  p.row_ptr = reinterpret_cast<int32_t*>(ws + w.row_ptr);
+  p.row_idx = reinterpret_cast<int32_t*>(ws + w.row_idx);
+  p.col_cnt = reinterpret_cast<int32_t*>(ws + w.col_cnt);
+  p.col_ptr = reinterpret_cast<int32_t*>(ws + w.col_ptr);
+  p.col_idx = reinterpret_cast<int32_t*>(ws + w.col_idx);
+  p.fwd_order = reinterpret_cast<int32_t*>(ws + w.fwd_order);
+  p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
+  p.delta = reinterpret_cast<float*>(ws + w.delta);
+  p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+  pl.cu = cu_doc_lens;
+  pl.n_docs = n_docs;
+  pl.device = dev;
+  if (cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DMA_ERR_CUDA;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the plan kernels clear what must start at zero (status word, column
+  // counts) and write every other array before it is read
+  if (dma::launch_plan_kernels(pl, s) != cudaSuccess) return DMA_ERR_CUDA;
+  CUtensorMap tq, tk, tv16;
+  dma_status st;
+  if ((st = map_rows_heads(&tq, q, p, p.n_heads, p.batch * p.local_len)) != DMA_OK) return st;
+  if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
+  if ((st = map_kv(&tv16, p.v16, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != DMA_OK) return st;
+  if (dma::launch_v_to_f16(pl, v, s) != cudaSuccess) return DMA_ERR_CUDA;
+  if (dma::launch_fwd(pl, tq, tk, tv16, o, lse, s) != cudaSuccess) return DMA_ERR_CUDA;
+  if (status_dev &&
+      cudaMemcpyAsync(status_dev, p.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess)
+    return DMA_ERR_CUDA;
+  return DMA_OK;
+}

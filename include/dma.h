@@ -237,6 +237,35 @@ dma_status dma_plan_set_wait_timeout(dma_plan_t plan, uint64_t timeout_ns);
 dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev,
                                 void* stream);
 
+/*
+ * Allocation-free forward (the pages have no counterpart: this is a
+ * convenience of this library).  For callers that may not allocate device
+ * memory at all -- code that must not grow or step outside a fixed memory
+ * pool, or hosts that forbid cudaMalloc -- and so cannot provide the plan
+ * workspace the other entry points need.  It does what dma_plan followed by
+ * dma_attn_fwd does, with all scratch (the plan and the fp16 copy of v) in a
+ * 64 MiB array compiled into the library; the caller passes only inputs and
+ * outputs.
+ *   - Every GPU that loads the library holds the 64 MiB until the process
+ *     exits.  Shapes whose scratch exceeds it return DMA_ERR_WORKSPACE
+ *     (dma_plan_workspace_bytes gives the size a shape needs).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call outside any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, or different host threads) race and corrupt each
+ *     other; serialize them (one stream is enough).
+ *   - status_dev (optional, device uint32) receives the plan's status word
+ *     (DMA_OK, DMA_ERR_BAD_DOCS, DMA_ERR_TIMEOUT) in stream order; on a
+ *     malformed cu_doc_lens, o and lse are left unwritten.
+ *   - It calls no allocator: no cudaMalloc, no cudaFree, no host heap.
+ */
+dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_docs, int batch,
+                                int seq_len, int cp_size, int cp_rank, int n_heads,
+                                int n_kv_heads, int head_dim, float softmax_scale,
+                                const dma_bf16* q, const dma_bf16* k,
+                                const dma_bf16* v, float* o, float* lse,
+                                uint32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
