@@ -15,11 +15,9 @@
 //   dkdv_kernel   one CTA per (key tile, K/V head): K and V stay in shared
 //                 memory; the CTA walks the column list of query tiles (all g
 //                 heads of the group packed in each 128-row tile, so the GQA
-//                 reduction over the group happens inside the accumulation).
-//                 TMEM: dV, dK accumulators + S^T and dP^T of the current
-//                 query tile.  Warps 4-7 and 8-11: thread r of each owns key
-//                 r, the first warpgroup columns 0-63 of the query tile, the
-//                 second columns 64-127.
+//                 reduction over the group happens inside the accumulation),
+//                 each split in two 64-row halves handled by two ping-ponging
+//                 warpgroups; dV, dK accumulate in TMEM.
 //   dq_kernel     one CTA per (query tile, K/V head): Q and dO stay in shared
 //                 memory; the CTA walks the row list of key tiles.  TMEM: S,
 //                 dP and the dQ accumulator.  Warps 4-7 and 8-11: thread r of
@@ -58,19 +56,6 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
 // Warp-uniform bounded wait (every lane waits; all agree on the outcome).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
-}
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
-}
-
-__device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint32_t* pk) {
-  // one 128-element bf16 row (64 packed words) into a K-major 128-byte
-  // swizzled [128 rows][128 cols] tile made of two 64-column regions
-#pragma unroll
-  for (int ch = 0; ch < 16; ++ch) {
-    const uint32_t addr = base + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-    st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-  }
 }
 
 __device__ __forceinline__ void store_half_row_sw128(uint32_t region, int r, const uint32_t* pk) {
@@ -117,6 +102,15 @@ __global__ void delta_kernel(const float* __restrict__ o, const __nv_bfloat16* _
 }
 
 // ---------------------------------------------------------------- dK / dV
+//
+// Work is done in half steps: half h of query tile i is its rows
+// [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads).  The two
+// element-wise warpgroups ping-pong: warpgroup h owns half h of every tile
+// and its own TMEM buffer (S^T | dP^T, 64 + 64 columns).  It overwrites the
+// columns it has read with P^T and dS^T (bf16, two per 32-bit column), which
+// the tensor core takes straight from TMEM as the A operand of dV += P^T dO_h
+// and dK += dS^T Q_h.  While one warpgroup computes, the tensor core works on
+// the other's half.
 
 template <int D>
 struct DkdvCfg {
@@ -127,14 +121,15 @@ struct DkdvCfg {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;         // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;    // 2 stages
-  static constexpr int kPS = kDO + 2 * kTile;   // P^T, then dS^T (128 x 128 bf16)
-  static constexpr int kCOL = kPS + 128 * 128 * 2;  // 2 stages x (lse*log2e, Delta), column order
-  static constexpr int kBar = kCOL + 2 * 1024;
-  static constexpr int kNumBars = 16;
+  static constexpr int kCOL = kDO + 2 * kTile;  // [warpgroup][2][64 LSE*log2e, 64 Delta]
+  static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
-  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384;
+  // TMEM: dV [0,128), dK [128,256); warpgroup h's buffer at 256 + 128h:
+  // S^T in its first 64 columns, dP^T in the next 64
+  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemBuf = 256;
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
 
@@ -159,8 +154,7 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
   // longest column lists first; the K/V heads of one key tile run side by
-  // side (measured faster than a head-major order, which crowds the
-  // resident CTAs onto the same query tiles)
+  // side (measured faster than a head-major order)
   const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
   const int bk = p.bwd_order[ord];
   const int b = bk / p.n_ktiles, kt = bk % p.n_ktiles;
@@ -172,21 +166,18 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sV = smem + Cfg::kV;
   uint8_t* sQ = smem + Cfg::kQ;
   uint8_t* sDO = smem + Cfg::kDO;
-  uint8_t* sPS = smem + Cfg::kPS;
   float* sCOL = reinterpret_cast<float*>(smem + Cfg::kCOL);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;    // [2]
-  uint64_t* q_empty = bars + 3;   // [2]
-  uint64_t* do_full = bars + 5;   // [2]
-  uint64_t* do_empty = bars + 7;  // [2]
-  uint64_t* sdp_full = bars + 9;
-  uint64_t* st_free = bars + 10;
-  uint64_t* p_full = bars + 11;
-  uint64_t* pv_done = bars + 12;
-  uint64_t* ds_full = bars + 13;
-  uint64_t* ds_done = bars + 14;
-  uint64_t* col_ready = bars + 15;
+  uint64_t* q_full = bars + 1;     // [2] per query-tile stage
+  uint64_t* q_empty = bars + 3;    // [2]
+  uint64_t* do_full = bars + 5;    // [2]
+  uint64_t* do_empty = bars + 7;   // [2]
+  uint64_t* sdp_full = bars + 9;   // [2] per warpgroup buffer: S^T, dP^T computed
+  uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them
+  uint64_t* buf_free = bars + 13;  // [2] dV, dK of that half step done
+  uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
+  uint64_t* acc_done = bars + 17;  // every MMA done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -197,14 +188,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&pds_full[i], 128);
+      mbar_init(&buf_free[i], 1);
+      mbar_init(&col_ready[i], 128);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(st_free, 256);
-    mbar_init(col_ready, 256);
-    mbar_init(p_full, 256);
-    mbar_init(pv_done, 1);
-    mbar_init(ds_full, 256);
-    mbar_init(ds_done, 1);
+    mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -275,202 +264,190 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       // --------------------------------------------------------- MMA issuer
-      // per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T into TMEM;
-      // then, once the key-row warps have turned tile i into P^T and dS^T,
-      // dV += P^T dO_i and dK += dS^T Q_i.  S^T / dP^T of tile i+1 are
-      // issued as soon as tile i's have been read, ahead of tile i's dV and
-      // dK, so the tensor pipe works while the key rows compute.
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      // half step s = 2i + h: S^T = K Q_h^T and dP^T = V dO_h^T into buffer
+      // h; once warpgroup h has written P^T, dS^T over them: dV += P^T dO_h,
+      // dK += dS^T Q_h (A operands from TMEM).  The next S^T / dP^T of buffer
+      // h (half step s+2) go out once those two have read it.
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ps_addr = smem_u32(sPS);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const int steps = 2 * n;
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = mbar_wait(kv_full, 0, ctl);
-      auto issue_sdp = [&](int i) -> bool {
-        const int st = i & 1;
+      auto issue_sdp = [&](int s) -> bool {
+        const int i = s >> 1, h = s & 1, st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (!mbar_wait(&q_full[st], ph, ctl)) return false;
-        if (i > 0 && !mbar_wait(st_free, (i - 1) & 1, ctl)) return false;
         tc_fence_after();
-        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+        const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
+        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
+          mma_bf16_ss(buf, sdesc_sw128(k_addr + off, 16, 1024),
                       sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
         if (!mbar_wait(&do_full[st], ph, ctl)) return false;
         tc_fence_after();
-        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
+          mma_bf16_ss(buf + 64, sdesc_sw128(v_addr + off, 16, 1024),
                       sdesc_sw128(do_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(sdp_full);
-        last_commit = sdp_full;
+        mma_commit(&sdp_full[h]);
+        last_commit = &sdp_full[h];
         last_parity = i & 1;
         return true;
       };
       if (ok) ok = issue_sdp(0);
-      for (int i = 0; ok && i < n; ++i) {
-        const int st = i & 1;
-        if (i + 1 < n && !issue_sdp(i + 1)) { ok = false; break; }
-        // dV += P^T dO_i
-        if (!mbar_wait(p_full, i & 1, ctl)) { ok = false; break; }
+      if (ok && steps > 1) ok = issue_sdp(1);
+      for (int s = 0; ok && s < steps; ++s) {
+        const int i = s >> 1, h = s & 1, st = i & 1;
+        const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
+        if (!mbar_wait(&pds_full[h], i & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
+        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemDV, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done);
-        mma_commit(&do_empty[st]);
-        last_commit = pv_done;
-        last_parity = i & 1;
-        // dK += dS^T Q_i
-        if (!mbar_wait(ds_full, i & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+        for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h; K = the half's 64 rows
+          mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk,
+                     sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                     (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(ps_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemDK, a, bd, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(ds_done);
-        mma_commit(&q_empty[st]);
-        last_commit = ds_done;
+        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
+          mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk,
+                     sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                     (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&buf_free[h]);
+        last_commit = &buf_free[h];
         last_parity = i & 1;
+        if (h == 1) {
+          mma_commit(&do_empty[st]);
+          mma_commit(&q_empty[st]);
+        }
+        if (s + 2 < steps) {
+          // buffer h is read by the MMAs just issued: wait for them
+          if (!mbar_wait(&buf_free[h], i & 1, ctl)) { ok = false; break; }
+          if (!issue_sdp(s + 2)) { ok = false; break; }
+        }
+      }
+      if (ok) {
+        mma_commit(acc_done);
+        last_commit = acc_done;
+        last_parity = 0;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- key rows
-    // two warpgroups: thread (r, half) owns key r and query-tile columns
-    // [64*half, 64*half + 64), i.e. exactly one 64-column swizzle region
-    // barriers by shared-window offset (fewer registers than generic pointers)
-    const uint32_t b_col = smem_u32(col_ready), b_sdp = smem_u32(sdp_full),
-                   b_st = smem_u32(st_free), b_dsd = smem_u32(ds_done), b_pf = smem_u32(p_full),
-                   b_pv = smem_u32(pv_done), b_dsf = smem_u32(ds_full);
-    const int r = (threadIdx.x - 128) & 127;
-    const int half = (threadIdx.x - 128) >> 7;
-    const int cbase = 64 * half;
+    // warpgroup h: thread r owns key r for half h of every query tile
+    const int t = threadIdx.x - 128;
+    const int r = t & 127, h = t >> 7;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
     const int lg = 31 - __clz(g);
     const int key = kt * kTileN + r;  // position within the sample
     const float sl2 = p.scale_log2;
-    const uint32_t ps_region = smem_u32(sPS) + half * Cfg::kRegion;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
     // queries that may attend this key: positions [key, doc_end)
     const int doc_end = p.doc_hi[static_cast<long long>(b) * p.seq_len + key];
-    // column r of every query tile is query row (position r >> lg, head r & (g-1));
-    // warpgroup 0 stages LSE of column r, warpgroup 1 stages Delta
+    // statistics of half h, column j (query row 64h + j): thread r < 64
+    // stages LSE of column r, thread r >= 64 Delta of column r - 64
+    const int scol = r & 63;
+    const int qrow = 64 * h + scol;
+    const float* stat_src = (r < 64) ? lse : p.delta;
+    const float stat_mul = (r < 64) ? kLog2e : 1.f;
     const long long stat_base =
-        (static_cast<long long>(b) * p.n_heads + kvh * g + (r & (g - 1))) * Lq + (r >> lg);
-    const float* stat_src = half ? p.delta : lse;
-    const float stat_mul = half ? 1.f : kLog2e;
-    // list entries run two tiles ahead, statistics one tile ahead
-    uint32_t e_next = n > 1 ? static_cast<uint32_t>(list[1]) : 0u;
-    uint32_t e = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
-    float nxt = 0.f;
-    if (n > 0) nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
+        (static_cast<long long>(b) * p.n_heads + kvh * g + (qrow & (g - 1))) * Lq + (qrow >> lg);
+    float* col = sCOL + h * 256;  // [2][128] floats per warpgroup
+    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
+    float nxt = n > 0 ? stat_src[stat_base + static_cast<int>(e_next & kIndexMask) * P] : 0.f;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int st = i & 1;
-      const int qt = static_cast<int>(e & kIndexMask);
-      // allowed query positions of this key in the tile: [key, doc_end), i.e.
-      // tile positions p_first .. p_end-1 = columns p_first*g .. p_end*g - 1
-      int c_lo = 0, c_hi = 128;
-      if (e & kPartialBit) {
-        const int l0 = qt * P;
-        const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
-        c_lo = max(0, key - q0) << lg;
-        c_hi = min(P, max(0, doc_end - q0)) << lg;
-      }
-      e = e_next;
-      if (i + 2 < n) e_next = static_cast<uint32_t>(list[i + 2]);
-      {  // column-ordered row statistics of this tile, prefetched one ahead
+      const uint32_t e = e_next;  // list entries and statistics run one tile ahead
+      if (i + 1 < n) e_next = static_cast<uint32_t>(list[i + 1]);
+      {
         const float cur = nxt;
-        if (i + 1 < n) nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
-        sCOL[st * 256 + half * 128 + r] = cur * stat_mul;
-        mbar_arrive(b_col);  // 256 arrivals per tile: a bounded barrier
-        if (!warp_wait(b_col, i & 1, ctl)) { ok = false; break; }
+        if (i + 1 < n) nxt = stat_src[stat_base + static_cast<int>(e_next & kIndexMask) * P];
+        col[(i & 1) * 128 + r] = cur * stat_mul;
+        mbar_arrive(&col_ready[h]);
+        if (!warp_wait(&col_ready[h], i & 1, ctl)) { ok = false; break; }
       }
-      const float4* lse_c = reinterpret_cast<const float4*>(sCOL + st * 256);
-      const float4* del_c = reinterpret_cast<const float4*>(sCOL + st * 256 + 128);
-      if (!warp_wait(b_sdp, i & 1, ctl)) { ok = false; break; }
+      // allowed query positions of this key in the tile: [key, doc_end);
+      // in columns of this half: [lo_c, hi_c)
+      int lo_c = 0, hi_c = 64;
+      if (e & kPartialBit) {
+        const int l0 = static_cast<int>(e & kIndexMask) * P;
+        const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
+        lo_c = (max(0, key - q0) << lg) - 64 * h;
+        hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h;
+      }
+      const float4* lse_c = reinterpret_cast<const float4*>(col + (i & 1) * 128);
+      const float4* del_c = reinterpret_cast<const float4*>(col + (i & 1) * 128 + 64);
+      if (!warp_wait(&sdp_full[h], i & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      // one pass: P^T = exp(scale S^T - LSE), dS^T = P^T (dP^T - Delta)
-      uint32_t pk[32], pd[32];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) {
-        const int cg = cbase + c0;  // column of the query tile
         uint32_t su[16], du[16];
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDP + cg, du);
+        tmem_ld16_nowait(buf + c0, su);
+        tmem_ld16_nowait(buf + 64 + c0, du);
         tmem_wait_ld();
         reg_fence16(su);
         reg_fence16(du);
-        const uint32_t allow = range_bits(c_lo - cg, c_hi - cg);
+        const uint32_t allow = range_bits(lo_c - c0, hi_c - c0);
+        uint32_t pk[8], pd[8];
 #pragma unroll
-        for (int t = 0; t < 16; t += 4) {
-          const float4 l4 = lse_c[(cg + t) >> 2];
-          const float4 d4 = del_c[(cg + t) >> 2];
+        for (int q = 0; q < 16; q += 4) {
+          const float4 l4 = lse_c[(c0 + q) >> 2];
+          const float4 d4 = del_c[(c0 + q) >> 2];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], dv4[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            pv[u] = ((allow >> (t + u)) & 1u)
-                        ? ex2(fmaf(__uint_as_float(su[t + u]), sl2, -lv[u]))
+            pv[u] = ((allow >> (q + u)) & 1u)
+                        ? ex2(fmaf(__uint_as_float(su[q + u]), sl2, -lv[u]))
                         : 0.f;
-            dv4[u] = pv[u] * (__uint_as_float(du[t + u]) - dl[u]);
+            dv4[u] = pv[u] * (__uint_as_float(du[q + u]) - dl[u]);
           }
-          pk[(c0 + t) >> 1] = pack_bf16(pv[0], pv[1]);
-          pk[((c0 + t) >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          pd[(c0 + t) >> 1] = pack_bf16(dv4[0], dv4[1]);
-          pd[((c0 + t) >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
+          pk[q >> 1] = pack_bf16(pv[0], pv[1]);
+          pk[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+          pd[q >> 1] = pack_bf16(dv4[0], dv4[1]);
+          pd[(q >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
         }
-        reg_fence8(pk + (c0 >> 1));
-        reg_fence8(pd + (c0 >> 1));
+        // P^T and dS^T of these 16 columns over the 8 columns already read
+        tmem_st8_nowait(buf + (c0 >> 1), pk);
+        tmem_st8_nowait(buf + 64 + (c0 >> 1), pd);
       }
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(b_st);  // S^T and dP^T of this tile have been read
-      if (i > 0 && !warp_wait(b_dsd, (i - 1) & 1, ctl)) { ok = false; break; }
-      store_half_row_sw128(ps_region, r, pk);
-      fence_proxy_async_smem();
-      mbar_arrive(b_pf);
-      if (!warp_wait(b_pv, i & 1, ctl)) { ok = false; break; }
-      store_half_row_sw128(ps_region, r, pd);
-      fence_proxy_async_smem();
-      mbar_arrive(b_dsf);
+      mbar_arrive(&pds_full[h]);
     }
     // warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
     const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
-    float4* dst = reinterpret_cast<float4*>((half ? dk : dv) + out_row * D);
+    float4* dst = reinterpret_cast<float4*>((h ? dk : dv) + out_row * D);
     if (n == 0) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int c = 0; c < D / 4; ++c) dst[c] = z;
-    } else if (ok && warp_wait(b_dsd, (n - 1) & 1, ctl)) {
+      for (int q = 0; q < D / 4; ++q) dst[q] = z;
+    } else if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
-      const float sc = half ? p.scale : 1.f;
-      const uint32_t acc = tmem + lane_base + (half ? Cfg::kTmemDK : Cfg::kTmemDV);
+      const float sc = h ? p.scale : 1.f;
+      const uint32_t acc = tmem + lane_base + (h ? Cfg::kTmemDK : Cfg::kTmemDV);
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t t[16];
-        tmem_ld16_nowait(acc + c0, t);
+        uint32_t tt[16];
+        tmem_ld16_nowait(acc + c0, tt);
         tmem_wait_ld();
-        reg_fence16(t);
+        reg_fence16(tt);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          dst[c0 / 4 + q4] =
-              make_float4(__uint_as_float(t[4 * q4]) * sc, __uint_as_float(t[4 * q4 + 1]) * sc,
-                          __uint_as_float(t[4 * q4 + 2]) * sc, __uint_as_float(t[4 * q4 + 3]) * sc);
+          dst[c0 / 4 + q4] = make_float4(
+              __uint_as_float(tt[4 * q4]) * sc, __uint_as_float(tt[4 * q4 + 1]) * sc,
+              __uint_as_float(tt[4 * q4 + 2]) * sc, __uint_as_float(tt[4 * q4 + 3]) * sc);
       }
     }
   }
