@@ -14,13 +14,16 @@
 //   warp 0      TMA producer: Q once, then K tiles into a 3-stage ring
 //   warp 2      TMA producer: V tiles into a 2-stage ring (decoupled from K,
 //               so a K load never queues behind the release of a V slot)
-//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers,
-//               O += P V into a TMEM accumulator; owns the TMEM allocation
+//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers (Q
+//               copied once into TMEM as the A operand), O += P V into a
+//               TMEM accumulator with P taken from TMEM; owns the allocation
 //   warps 2-3   load the tile's positions / document starts first
 //   warps 4-7   softmax: thread r owns row r (TMEM lane r): masks partial
-//               tiles, exponentiates in base 2, writes P (fp16) to shared
-//               memory in the 128-byte-swizzled K-major layout, rescales O in
-//               TMEM when its reference max moves, and writes O (fp32) and LSE.
+//               tiles, exponentiates in base 2, writes P (fp16 pairs) back
+//               over the S columns it has read, rescales O in TMEM when its
+//               reference max moves, and writes O (fp32) and LSE.
+// Keeping Q and P in TMEM leaves the tensor core only K and V to read from
+// shared memory, which halves the shared-memory traffic per tile.
 // P V runs in fp16 against an fp16 copy of V made once per call
 // (v_to_f16_kernel): fp16's 11-bit significand keeps the rounding of the
 // probabilities 8x below bf16's, so O meets a 1e-2 absolute bound even on
@@ -38,22 +41,22 @@ namespace {
 template <int D>
 struct FwdCfg {
   static constexpr int kStagesK = 3;
-  static constexpr int kStagesV = 2;
+  static constexpr int kStagesV = 3;
   static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
   static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (bf16)
+  static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (16-bit)
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
-  static constexpr int kP = kV + kStagesV * kTileBytes;
-  static constexpr int kPBytes = 128 * 128 * 2;
-  static constexpr int kBar = kP + kPBytes;
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2;
+  static constexpr int kBar = kV + kStagesV * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+  // TMEM: S buffers (128 columns each; P overwrites their first 64 as fp16
+  // pairs), the O accumulator, and Q as bf16 pairs (the A operand of Q K^T)
+  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
   static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
 };
 
@@ -63,6 +66,28 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// Row r of the Q tile (K-major, 128-byte swizzled, D/64 regions of 16 KB)
+// into TMEM lane r as bf16 pairs: columns [0, D/2).
+template <int D>
+__device__ __forceinline__ void q_row_to_tmem(uint32_t tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      uint32_t w[8];
+      const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
+      const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(a0));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                   : "r"(a1));
+      tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
+    }
   }
 }
 
@@ -94,17 +119,16 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* sQ = smem + Cfg::kQ;
   uint8_t* sK = smem + Cfg::kK;
   uint8_t* sV = smem + Cfg::kV;
-  uint8_t* sP = smem + Cfg::kP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_full = bars;          // Q in shared memory
+  uint64_t* q_tmem = bars + 1;      // Q copied into TMEM
+  uint64_t* k_full = bars + 2;
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  uint64_t* s_full = v_empty + SV;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
+  uint64_t* s_full = v_empty + SV;  // [2]
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 1;    // P V of a tile done (its S buffer is free)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   int* s_qpos = reinterpret_cast<int*>(smem + Cfg::kMisc + 16);
@@ -112,6 +136,7 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_tmem, 128);
     for (int i = 0; i < SK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -120,10 +145,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
     *abort_flag = 0;
@@ -208,14 +230,16 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && n > 0) {
       // --------------------------------------------------------- MMA issuer
+      // S_j = Q K_j^T into TMEM buffer j%2 (A = Q from TMEM); once the
+      // softmax has written P_j (fp16) over S_j: O += P_j V_j (A = P_j from
+      // TMEM).  Buffer j%2 is reused for S_{j+2} once P_j V_j has completed.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
-      bool ok = mbar_wait(q_full, 0, ctl);
+      bool ok = mbar_wait(q_tmem, 0, ctl);
       auto issue_pv = [&](int i) -> bool {
         const int st = i % SV;
         const uint32_t ph = (i / SV) & 1;
@@ -223,13 +247,12 @@ __global__ void __launch_bounds__(256, 1)
         if (!mbar_wait(&v_full[st], ph, ctl)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
+        const uint32_t pb = tmem + ((i & 1) ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t a =
-              sdesc_sw128(p_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemO, a, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk,
+                     sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
+                     (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(&v_empty[st]);
         last_commit = o_done;
@@ -241,16 +264,16 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t ph = (j / SK) & 1;
         const int sb = j & 1;
         if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
-        if (!mbar_wait(&s_free[sb], ((j >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
+        // buffer sb last held P_{j-2}: wait until P_{j-2} V_{j-2} has read it
+        if (j >= 2 && !mbar_wait(o_done, (j - 2) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Cfg::kTileBytes);
         const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(d_s, sdesc_sw128(q_addr + off, 16, 1024),
-                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16_ts(d_s, tmem + Cfg::kTmemQ + 8 * kk,
+                     sdesc_sw128(k_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024),
+                     idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(&s_full[sb]);
         mma_commit(&k_empty[st]);
         last_commit = &s_full[sb];
@@ -268,11 +291,20 @@ __global__ void __launch_bounds__(256, 1)
     const int pos = r >> lg, h = r & (g - 1);
     const int qabs = s_qpos[pos], lo_r = s_lo[pos];
     const float sl2 = p.scale_log2;
-    const uint32_t p_addr = smem_u32(sP);
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    if (n > 0) {  // row r of Q into TMEM (bf16 pairs), the A operand of Q K^T
+      if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, ctl))) {
+        ok = false;
+      } else {
+        q_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(q_tmem);
+      }
+    }
+    for (int j = 0; ok && j < n; ++j) {
       const int sb = j & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, ctl))) {
         ok = false;
@@ -295,8 +327,6 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
       const uint32_t e = e_next;  // list entries run one tile ahead
       if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
       if (e & kPartialBit) {
@@ -331,21 +361,19 @@ __global__ void __launch_bounds__(256, 1)
         pk[c >> 1] = pack_f16(e0, e1);
       }
       l_run = l_run * alpha + (sum0 + sum1);
-      if (j >= 1) {
+      // P (fp16 pairs) over the first 64 columns of this tile's S buffer
+      {
+        const uint32_t pb = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tmem_st8_nowait(pb + 8 * q, pk + 8 * q);
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // the reference max moved: rescale O once P_{j-1} V_{j-1} is in
         if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      // P row r -> shared memory, 128-byte swizzle, K-major, two 64-key regions
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint32_t addr = p_addr + (ch >> 3) * Cfg::kRegion + r * 128 +
-                              ((((ch & 7) ^ (r & 7))) << 4);
-        st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float t[32];
@@ -356,7 +384,7 @@ __global__ void __launch_bounds__(256, 1)
           tmem_st32(oc, t);
         }
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
       m_run = m_new;
