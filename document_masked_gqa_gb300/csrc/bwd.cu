@@ -102,6 +102,33 @@ __global__ void delta_kernel(const float* __restrict__ o, const __nv_bfloat16* _
 }
 
 // ---------------------------------------------------------------- dK / dV
+
+// 32 columns of one key row: P = exp2(S * scale*log2e - LSE*log2e) (zero where
+// the mask bit is clear when kMasked), dS = P (dP - Delta), both packed bf16.
+template <bool kMasked>
+__device__ __forceinline__ void p_ds_chunk32(const uint32_t* su, const uint32_t* du,
+                                             const float4* lse_c, const float4* del_c,
+                                             uint32_t allow, float sl2, uint32_t* pk,
+                                             uint32_t* pd) {
+#pragma unroll
+  for (int q = 0; q < 32; q += 4) {
+    const float4 l4 = lse_c[q >> 2];
+    const float4 d4 = del_c[q >> 2];
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+    float pv[4], dv4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pv[u] = ex2(fmaf(__uint_as_float(su[q + u]), sl2, -lv[u]));
+      if (kMasked && !((allow >> (q + u)) & 1u)) pv[u] = 0.f;
+      dv4[u] = pv[u] * (__uint_as_float(du[q + u]) - dl[u]);
+    }
+    pk[q >> 1] = pack_bf16(pv[0], pv[1]);
+    pk[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+    pd[q >> 1] = pack_bf16(dv4[0], dv4[1]);
+    pd[(q >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
+  }
+}
 //
 // Work is done in half steps: half h of query tile i is its rows
 // [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads).  The two
@@ -173,8 +200,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_empty = bars + 3;    // [2]
   uint64_t* do_full = bars + 5;    // [2]
   uint64_t* do_empty = bars + 7;   // [2]
-  uint64_t* sdp_full = bars + 9;   // [2] per warpgroup buffer: S^T, dP^T computed
-  uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them
+  uint64_t* sdp_full = bars + 9;   // [2] per buffer: S^T and dP^T computed (two commits)
+  uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them (both warpgroups)
   uint64_t* buf_free = bars + 13;  // [2] dV, dK of that half step done
   uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
   uint64_t* acc_done = bars + 17;  // every MMA done
@@ -188,8 +215,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&pds_full[i], 128);
+      mbar_init(&sdp_full[i], 2);
+      mbar_init(&pds_full[i], 256);
       mbar_init(&buf_free[i], 1);
       mbar_init(&col_ready[i], 128);
     }
@@ -210,15 +237,16 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
-      // ------------------------------------------- producer: K, V, then Q
+      // --------------------------------------- producer: K, V, then Q, dO
       tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tdo);
       mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c) {
         tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, kvh * D + c * 64, krow0);
         tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, kvh * D + c * 64, krow0);
       }
-      int last0 = -1, last1 = -1;
+      int last_q = -1, last_do = -1;
       bool ok = true;
       for (int i = 0; i < n; ++i) {
         const int st = i & 1;
@@ -230,80 +258,71 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64, kvh * g,
                       b * Lq + qt * P);
-        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
-      }
-      if (!ok) {
-        drain_wait(kv_full, 0, 100000000ull);
-        if (last0 >= 0) drain_wait(&q_full[0], last0, 100000000ull);
-        if (last1 >= 0) drain_wait(&q_full[1], last1, 100000000ull);
-      }
-    }
-  } else if (warp == 2) {
-    if (lane == 0 && n > 0) {
-      // ------------------------------------------------------ producer: dO
-      tma_prefetch_desc(&tdo);
-      int last0 = -1, last1 = -1;
-      bool ok = true;
-      for (int i = 0; i < n; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        const int qt = static_cast<int>(static_cast<uint32_t>(list[i]) & kIndexMask);
+        last_q = i;
         if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
                       kvh * g, b * Lq + qt * P);
-        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
+        last_do = i;
       }
       if (!ok) {
-        if (last0 >= 0) drain_wait(&do_full[0], last0, 100000000ull);
-        if (last1 >= 0) drain_wait(&do_full[1], last1, 100000000ull);
+        drain_wait(kv_full, 0, 100000000ull);
+        for (int ii = max(0, last_q - 1); ii <= last_q; ++ii)
+          drain_wait(&q_full[ii & 1], (ii >> 1) & 1, 100000000ull);
+        for (int ii = max(0, last_do - 1); ii <= last_do; ++ii)
+          drain_wait(&do_full[ii & 1], (ii >> 1) & 1, 100000000ull);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0 && n > 0) {
-      // --------------------------------------------------------- MMA issuer
-      // half step s = 2i + h: S^T = K Q_h^T and dP^T = V dO_h^T into buffer
-      // h; once warpgroup h has written P^T, dS^T over them: dV += P^T dO_h,
-      // dK += dS^T Q_h (A operands from TMEM).  The next S^T / dP^T of buffer
-      // h (half step s+2) go out once those two have read it.
+      // ------------------------------- MMA issuers: S^T (warp 1), dP^T (warp 2)
+      // half step s = 2i + h (query tile i, rows 64h..64h+63): S^T = K Q_h^T
+      // and dP^T = V dO_h^T into buffer h, once dV / dK of half step s-2
+      // have read that buffer.  Each commits once to sdp_full[h].
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
-      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const bool is_s = warp == 1;
+      const uint32_t a_addr = smem_u32(is_s ? sK : sV);
+      uint8_t* b_tiles = is_s ? sQ : sDO;
+      uint64_t* b_full = is_s ? q_full : do_full;
+      const uint32_t d_off = is_s ? 0u : 64u;
       const int steps = 2 * n;
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = mbar_wait(kv_full, 0, ctl);
-      auto issue_sdp = [&](int s) -> bool {
+      for (int s = 0; ok && s < steps; ++s) {
         const int i = s >> 1, h = s & 1, st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(&q_full[st], ph, ctl)) return false;
+        if (s >= 2 && !mbar_wait(&buf_free[h], (i - 1) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait(&b_full[st], ph, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
-        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
+        const uint32_t d = tmem + Cfg::kTmemBuf + 128 * h + d_off;
+        const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile) + h * 8192;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(buf, sdesc_sw128(k_addr + off, 16, 1024),
-                      sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        if (!mbar_wait(&do_full[st], ph, ctl)) return false;
-        tc_fence_after();
-        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(buf + 64, sdesc_sw128(v_addr + off, 16, 1024),
-                      sdesc_sw128(do_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&sdp_full[h]);
         last_commit = &sdp_full[h];
         last_parity = i & 1;
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      if (ok && steps > 1) ok = issue_sdp(1);
+      }
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp == 3) {
+    if (lane == 0 && n > 0) {
+      // -------------------------------------------------- MMA issuer: dV, dK
+      // once both warpgroups have written P^T, dS^T over buffer h:
+      // dV += P^T dO_h, dK += dS^T Q_h (A operands from TMEM).  A second
+      // issuing thread keeps these queued behind the S^T / dP^T products
+      // instead of waiting for them.
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
+      const int steps = 2 * n;
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = true;
       for (int s = 0; ok && s < steps; ++s) {
         const int i = s >> 1, h = s & 1, st = i & 1;
         const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
@@ -311,14 +330,16 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
         const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
+        // warpgroup w left its 32 query columns of P^T at buf + 32w (16
+        // packed columns) and of dS^T at buf + 64 + 32w
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h; K = the half's 64 rows
-          mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk,
+          mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk + (kk >= 2 ? 16 : 0),
                      sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                      (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
-          mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk,
+          mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk + (kk >= 2 ? 16 : 0),
                      sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                      (s > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&buf_free[h]);
@@ -327,11 +348,6 @@ __global__ void __launch_bounds__(384, 1)
         if (h == 1) {
           mma_commit(&do_empty[st]);
           mma_commit(&q_empty[st]);
-        }
-        if (s + 2 < steps) {
-          // buffer h is read by the MMAs just issued: wait for them
-          if (!mbar_wait(&buf_free[h], i & 1, ctl)) { ok = false; break; }
-          if (!issue_sdp(s + 2)) { ok = false; break; }
         }
       }
       if (ok) {
@@ -343,90 +359,87 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- key rows
-    // warpgroup h: thread r owns key r for half h of every query tile
+    // thread r of warpgroup w owns key r and, in every half step, the 32
+    // query columns [32w, 32w + 32) of that half
     const int t = threadIdx.x - 128;
-    const int r = t & 127, h = t >> 7;
+    const int r = t & 127, w = t >> 7;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
     const int lg = 31 - __clz(g);
     const int key = kt * kTileN + r;  // position within the sample
     const float sl2 = p.scale_log2;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
     // queries that may attend this key: positions [key, doc_end)
     const int doc_end = p.doc_hi[static_cast<long long>(b) * p.seq_len + key];
-    // statistics of half h, column j (query row 64h + j): thread r < 64
-    // stages LSE of column r, thread r >= 64 Delta of column r - 64
-    const int scol = r & 63;
-    const int qrow = 64 * h + scol;
-    const float* stat_src = (r < 64) ? lse : p.delta;
-    const float stat_mul = (r < 64) ? kLog2e : 1.f;
-    const long long stat_base =
-        (static_cast<long long>(b) * p.n_heads + kvh * g + (qrow & (g - 1))) * Lq + (qrow >> lg);
-    float* col = sCOL + h * 256;  // [2][128] floats per warpgroup
-    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
-    float nxt = n > 0 ? stat_src[stat_base + static_cast<int>(e_next & kIndexMask) * P] : 0.f;
+    // statistics of this warpgroup's columns: thread r < 32 stages LSE of
+    // column 32w + r, thread 32 <= r < 64 Delta of column 32w + r - 32
+    const int qsub = 32 * w + (r & 31);
+    const bool stager = r < 64;
+    const float* stat_src = (r < 32) ? lse : p.delta;
+    const float stat_mul = (r < 32) ? kLog2e : 1.f;
+    auto stat_row = [&](int hh) -> long long {
+      const int qrow = 64 * hh + qsub;
+      return (static_cast<long long>(b) * p.n_heads + kvh * g + (qrow & (g - 1))) * Lq +
+             (qrow >> lg);
+    };
+    const long long stat_base0 = stat_row(0), stat_base1 = stat_row(1);
+    float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
+    const int steps = 2 * n;
+    uint32_t e = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
+    float nxt = (n > 0 && stager) ? stat_src[stat_base0 + static_cast<int>(e & kIndexMask) * P] : 0.f;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const uint32_t e = e_next;  // list entries and statistics run one tile ahead
-      if (i + 1 < n) e_next = static_cast<uint32_t>(list[i + 1]);
+    for (int s = 0; s < steps; ++s) {
+      const int i = s >> 1, h = s & 1;
+      if (s > 0 && h == 0) e = static_cast<uint32_t>(list[i]);
       {
+        // stage this step's statistics, fetch the next step's
         const float cur = nxt;
-        if (i + 1 < n) nxt = stat_src[stat_base + static_cast<int>(e_next & kIndexMask) * P];
-        col[(i & 1) * 128 + r] = cur * stat_mul;
-        mbar_arrive(&col_ready[h]);
-        if (!warp_wait(&col_ready[h], i & 1, ctl)) { ok = false; break; }
+        if (stager && s + 1 < steps) {
+          const int s1 = s + 1;
+          const uint32_t e1 = (s1 & 1) ? e : static_cast<uint32_t>(list[s1 >> 1]);
+          nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
+        }
+        if (stager) col[(s & 1) * 128 + r] = cur * stat_mul;
+        mbar_arrive(&col_ready[w]);
+        if (!warp_wait(&col_ready[w], s & 1, ctl)) { ok = false; break; }
       }
       // allowed query positions of this key in the tile: [key, doc_end);
-      // in columns of this half: [lo_c, hi_c)
-      int lo_c = 0, hi_c = 64;
+      // in this warpgroup's columns of half h: [lo_c, hi_c)
+      int lo_c = 0, hi_c = 32;
       if (e & kPartialBit) {
         const int l0 = static_cast<int>(e & kIndexMask) * P;
         const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
-        lo_c = (max(0, key - q0) << lg) - 64 * h;
-        hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h;
+        lo_c = (max(0, key - q0) << lg) - 64 * h - 32 * w;
+        hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h - 32 * w;
       }
-      const float4* lse_c = reinterpret_cast<const float4*>(col + (i & 1) * 128);
-      const float4* del_c = reinterpret_cast<const float4*>(col + (i & 1) * 128 + 64);
+      const float4* lse_c = reinterpret_cast<const float4*>(col + (s & 1) * 128);
+      const float4* del_c = reinterpret_cast<const float4*>(col + (s & 1) * 128 + 32);
+      const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
       if (!warp_wait(&sdp_full[h], i & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t su[16], du[16];
-        tmem_ld16_nowait(buf + c0, su);
-        tmem_ld16_nowait(buf + 64 + c0, du);
+      {
+        uint32_t su[32], du[32];
+        tmem_ld32_nowait(buf + 32 * w, su);
+        tmem_ld32_nowait(buf + 64 + 32 * w, du);
         tmem_wait_ld();
-        reg_fence16(su);
-        reg_fence16(du);
-        const uint32_t allow = range_bits(lo_c - c0, hi_c - c0);
-        uint32_t pk[8], pd[8];
-#pragma unroll
-        for (int q = 0; q < 16; q += 4) {
-          const float4 l4 = lse_c[(c0 + q) >> 2];
-          const float4 d4 = del_c[(c0 + q) >> 2];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dv4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            pv[u] = ((allow >> (q + u)) & 1u)
-                        ? ex2(fmaf(__uint_as_float(su[q + u]), sl2, -lv[u]))
-                        : 0.f;
-            dv4[u] = pv[u] * (__uint_as_float(du[q + u]) - dl[u]);
-          }
-          pk[q >> 1] = pack_bf16(pv[0], pv[1]);
-          pk[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          pd[q >> 1] = pack_bf16(dv4[0], dv4[1]);
-          pd[(q >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
-        }
-        // P^T and dS^T of these 16 columns over the 8 columns already read
-        tmem_st8_nowait(buf + (c0 >> 1), pk);
-        tmem_st8_nowait(buf + 64 + (c0 >> 1), pd);
+        reg_fence32(su);
+        reg_fence32(du);
+        uint32_t pk[16], pd[16];
+        if (e & kPartialBit)
+          p_ds_chunk32<true>(su, du, lse_c, del_c, range_bits(lo_c, hi_c), sl2, pk, pd);
+        else
+          p_ds_chunk32<false>(su, du, lse_c, del_c, 0u, sl2, pk, pd);
+        // P^T and dS^T of these 32 columns over the first 16 columns read
+        tmem_st8_nowait(buf + 32 * w, pk);
+        tmem_st8_nowait(buf + 32 * w + 8, pk + 8);
+        tmem_st8_nowait(buf + 64 + 32 * w, pd);
+        tmem_st8_nowait(buf + 64 + 32 * w + 8, pd + 8);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&pds_full[h]);
     }
     // warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
+    const int h = w;
     const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
     float4* dst = reinterpret_cast<float4*>((h ? dk : dv) + out_row * D);
     if (n == 0) {
@@ -467,17 +480,24 @@ struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kRegion = 16384;
   static constexpr int kChunks = D / 64;
-  static constexpr int kQ = 0;
-  static constexpr int kDO = kQ + kTile;
-  static constexpr int kK = kDO + kTile;       // 2 stages
-  static constexpr int kV = kK + 2 * kTile;    // 2 stages
-  static constexpr int kDS = kV + 2 * kTile;   // dS (128 x 128 bf16)
+  // Q and dO arrive through the dS buffer and K stage 2 (both unused until
+  // Q and dO have been copied into TMEM)
+  static constexpr int kStagesK = 3;
+  static constexpr int kK = 0;                       // 3 stages
+  static constexpr int kV = kK + kStagesK * kTile;   // 2 stages
+  static constexpr int kDS = kV + 2 * kTile;         // dS (128 x 128 bf16)
+  static constexpr int kQ = kDS;
+  static constexpr int kDO = kK + 2 * kTile;
   static constexpr int kBar = kDS + 128 * 128 * 2;
-  static constexpr int kNumBars = 13;
+  static constexpr int kNumBars = 18;
+  static_assert(kTile <= 128 * 128 * 2, "Q staging exceeds the dS buffer");
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
+  // S, dP, dQ accumulators (fp32), then Q and dO as bf16 pairs (A operands)
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
+  static constexpr uint32_t kTmemQ = 384, kTmemDO = 384 + D / 2;
+  static_assert(kTmemDO + D / 2 <= 512, "dQ TMEM layout exceeds 512 columns");
   static_assert(kNeed <= kMaxSmem, "dQ shared-memory layout exceeds 227 KB");
 };
 
@@ -514,30 +534,38 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sV = smem + Cfg::kV;
   uint8_t* sDS = smem + Cfg::kDS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_full = bars;       // Q and dO
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* sdp_full = bars + 9;
-  uint64_t* st_free = bars + 10;
-  uint64_t* ds_full = bars + 11;
-  uint64_t* ds_done = bars + 12;
+  uint64_t* q_full = bars;        // Q and dO
+  uint64_t* v_full = bars + 1;    // [2]
+  uint64_t* v_empty = bars + 3;   // [2]
+  uint64_t* s_full = bars + 5;    // S of the current key tile computed
+  uint64_t* s_free = bars + 6;    // the row warps have read S
+  uint64_t* ds_full = bars + 7;   // dS written to shared memory
+  uint64_t* ds_done = bars + 8;   // dQ += dS K done reading dS
+  uint64_t* qd_tmem = bars + 9;   // Q and dO copied into TMEM
+  uint64_t* dp_full = bars + 10;  // dP computed
+  uint64_t* dp_free = bars + 11;  // the row warps have read dP
+  uint64_t* k_full = bars + 12;   // [3]
+  uint64_t* k_empty = bars + 15;  // [3]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(st_free, 256);
+    for (int i = 0; i < Cfg::kStagesK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 256);
     mbar_init(ds_full, 256);
     mbar_init(ds_done, 1);
+    mbar_init(qd_tmem, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -553,114 +581,125 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
-      // ------------------------------------------ producer: Q, dO, then K
+      // ---------------------------------------- producer: Q, dO, then K, V
       tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
       mbar_arrive_expect_tx(q_full, 2 * Cfg::kTile);
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c) {
         tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
         tma_load_3d(sDO + c * Cfg::kRegion, &tdo, q_full, c * 64, kvh * g, b * Lq + l0);
       }
-      int last0 = -1, last1 = -1;
+      int last_k = -1, last_v = -1;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
         const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&k_full[st], Cfg::kTile);
+        const int krow = b * p.seq_len + kt * kTileN;
+        {
+          const int st = j % Cfg::kStagesK;
+          const uint32_t ph = (j / Cfg::kStagesK) & 1;
+          // stage 2 first holds dO: wait until it has been copied into TMEM
+          if (j == 2 && !mbar_wait(qd_tmem, 0, ctl)) { ok = false; break; }
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[st], Cfg::kTile);
 #pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_2d(sK + st * Cfg::kTile + c * Cfg::kRegion, &tk, &k_full[st], kvh * D + c * 64,
-                      b * p.seq_len + kt * kTileN);
-        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_2d(sK + st * Cfg::kTile + c * Cfg::kRegion, &tk, &k_full[st],
+                        kvh * D + c * 64, krow);
+          last_k = j;
+        }
+        {
+          const int st = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[st], Cfg::kTile);
+#pragma unroll
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_2d(sV + st * Cfg::kTile + c * Cfg::kRegion, &tv, &v_full[st],
+                        kvh * D + c * 64, krow);
+          last_v = j;
+        }
       }
       if (!ok) {
         drain_wait(q_full, 0, 100000000ull);
-        if (last0 >= 0) drain_wait(&k_full[0], last0, 100000000ull);
-        if (last1 >= 0) drain_wait(&k_full[1], last1, 100000000ull);
+        for (int jj = max(0, last_k - Cfg::kStagesK + 1); jj <= last_k; ++jj)
+          drain_wait(&k_full[jj % Cfg::kStagesK], (jj / Cfg::kStagesK) & 1, 100000000ull);
+        for (int jj = max(0, last_v - 1); jj <= last_v; ++jj)
+          drain_wait(&v_full[jj & 1], (jj >> 1) & 1, 100000000ull);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp <= 3) {
     if (lane == 0 && n > 0) {
-      // ------------------------------------------------------ producer: V
-      tma_prefetch_desc(&tv);
-      int last0 = -1, last1 = -1;
-      bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&v_full[st], Cfg::kTile);
-#pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_2d(sV + st * Cfg::kTile + c * Cfg::kRegion, &tv, &v_full[st], kvh * D + c * 64,
-                      b * p.seq_len + kt * kTileN);
-        if (st) last1 = static_cast<int>(ph); else last0 = static_cast<int>(ph);
-      }
-      if (!ok) {
-        if (last0 >= 0) drain_wait(&v_full[0], last0, 100000000ull);
-        if (last1 >= 0) drain_wait(&v_full[1], last1, 100000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      // --------------------------------------------------------- MMA issuer
-      // per key tile j: S = Q K_j^T and dP = dO V_j^T into TMEM; once the row
-      // warps have turned them into dS: dQ += dS K_j.  S / dP of tile j+1 go
-      // out as soon as tile j's have been read, ahead of tile j's dQ.
+      // ------------------------------------------------------ MMA issuers
+      // per key tile j: S = Q K_j^T (warp 1) and dP = dO V_j^T (warp 2) into
+      // TMEM with Q and dO as TMEM A operands; once the row warps have
+      // written dS: dQ += dS K_j (warp 3).  S and dP have separate buffers,
+      // each reissued as soon as the row warps have read it.  One issuing
+      // thread per product on its own warp scheduler keeps the tensor pipe
+      // fed while the row warps keep the schedulers busy.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), ds_addr = smem_u32(sDS);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
-      bool ok = mbar_wait(q_full, 0, ctl);
-      auto issue_sdp = [&](int j) -> bool {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_full[st], ph, ctl)) return false;
-        if (j > 0 && !mbar_wait(st_free, (j - 1) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+      bool ok = true;
+      if (warp == 1) {
+        ok = mbar_wait(qd_tmem, 0, ctl);
+        for (int j = 0; ok && j < n; ++j) {
+          const int st = j % Cfg::kStagesK;
+          if (!mbar_wait(&k_full[st], (j / Cfg::kStagesK) & 1, ctl)) { ok = false; break; }
+          if (j > 0 && !mbar_wait(s_free, (j - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(q_addr + off, 16, 1024),
-                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
+            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+            mma_f16_ts(tmem + Cfg::kTmemS, tmem + Cfg::kTmemQ + 8 * kk,
+                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(s_full);
+          last_commit = s_full;
+          last_parity = j & 1;
         }
-        if (!mbar_wait(&v_full[st], ph, ctl)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTile);
+      } else if (warp == 2) {
+        ok = mbar_wait(qd_tmem, 0, ctl);
+        for (int j = 0; ok && j < n; ++j) {
+          const int st = j & 1;
+          if (!mbar_wait(&v_full[st], (j >> 1) & 1, ctl)) { ok = false; break; }
+          if (j > 0 && !mbar_wait(dp_free, (j - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sV + st * Cfg::kTile);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(do_addr + off, 16, 1024),
-                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
+            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+            mma_f16_ts(tmem + Cfg::kTmemDP, tmem + Cfg::kTmemDO + 8 * kk,
+                       sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(dp_full);
+          mma_commit(&v_empty[st]);
+          last_commit = dp_full;
+          last_parity = j & 1;
         }
-        mma_commit(sdp_full);
-        mma_commit(&v_empty[st]);
-        last_commit = sdp_full;
-        last_parity = j & 1;
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      for (int j = 0; ok && j < n; ++j) {
-        const int st = j & 1;
-        if (j + 1 < n && !issue_sdp(j + 1)) { ok = false; break; }
-        if (!mbar_wait(ds_full, j & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+      } else {
+        // S_j has completed before dS_j exists, so the K stage is free once
+        // this product is done
+        const uint32_t ds_addr = smem_u32(sDS);
+        for (int j = 0; ok && j < n; ++j) {
+          const int st = j % Cfg::kStagesK;
+          if (!mbar_wait(ds_full, j & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
-          mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // dQ += dS K
+            const uint64_t a =
+                sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
+            mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(ds_done);
+          mma_commit(&k_empty[st]);
+          last_commit = ds_done;
+          last_parity = j & 1;
         }
-        mma_commit(ds_done);
-        mma_commit(&k_empty[st]);
-        last_commit = ds_done;
-        last_parity = j & 1;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
@@ -685,8 +724,19 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     const uint32_t ds_region = smem_u32(sDS) + half * Cfg::kRegion;
     bool ok = true;
+    if (n > 0) {
+      // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
+      ok = warp_wait(q_full, 0, ctl);
+      if (ok) {
+        sw128_row_to_tmem<D>(smem_u32(half ? sDO : sQ), r,
+                             tmem + lane_base + (half ? Cfg::kTmemDO : Cfg::kTmemQ));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(qd_tmem);
+      }
+    }
     uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; ok && j < n; ++j) {
       const uint32_t e = e_next;  // list entries run one tile ahead
       if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
       int c_lo = 0, c_hi = 128;
@@ -695,35 +745,44 @@ __global__ void __launch_bounds__(384, 1)
         c_lo = lo_r - k0;
         c_hi = qabs - k0 + 1;
       }
-      if (!warp_wait(sdp_full, j & 1, ctl)) { ok = false; break; }
+      // P = exp2(S * scale*log2e - LSE*log2e) for this thread's 64 columns
+      if (!warp_wait(s_full, j & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      const bool masked = (e & kPartialBit) != 0;
+      float pv[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        const int cg = cbase + c0;
+        uint32_t su[32];
+        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
+        tmem_wait_ld();
+        reg_fence32(su);
+        const uint32_t allow = masked ? range_bits(c_lo - cg, c_hi - cg) : 0xFFFFFFFFu;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const float pj = ex2(fmaf(__uint_as_float(su[t]), sl2, -lse2));
+          pv[c0 + t] = ((allow >> t) & 1u) ? pj : 0.f;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      // dS = P (dP - Delta)
+      if (!warp_wait(dp_full, j & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       uint32_t pk[32];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        const int cg = cbase + c0;
-        uint32_t su[16], du[16];
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDP + cg, du);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t du[32];
+        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase + c0, du);
         tmem_wait_ld();
-        reg_fence16(su);
-        reg_fence16(du);
-        const uint32_t allow = range_bits(c_lo - cg, c_hi - cg);
+        reg_fence32(du);
 #pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-          float dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float pj = ((allow >> (t + u)) & 1u)
-                                 ? ex2(fmaf(__uint_as_float(su[t + u]), sl2, -lse2))
-                                 : 0.f;
-            dsv[u] = pj * (__uint_as_float(du[t + u]) - del);
-          }
-          pk[(c0 + t) >> 1] = pack_bf16(dsv[0], dsv[1]);
-        }
-        reg_fence8(pk + (c0 >> 1));
+        for (int t = 0; t < 32; t += 2)
+          pk[(c0 + t) >> 1] = pack_bf16(pv[c0 + t] * (__uint_as_float(du[t]) - del),
+                                        pv[c0 + t + 1] * (__uint_as_float(du[t + 1]) - del));
       }
       tc_fence_before();
-      mbar_arrive(st_free);
+      mbar_arrive(dp_free);
       if (j > 0 && !warp_wait(ds_done, (j - 1) & 1, ctl)) { ok = false; break; }
       store_half_row_sw128(ds_region, r, pk);
       fence_proxy_async_smem();

@@ -49,7 +49,7 @@ struct FwdCfg {
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
   static constexpr int kSmemBytes = kEnd + 1024;
@@ -66,28 +66,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > limit_ns) return;
-  }
-}
-
-// Row r of the Q tile (K-major, 128-byte swizzled, D/64 regions of 16 KB)
-// into TMEM lane r as bf16 pairs: columns [0, D/2).
-template <int D>
-__device__ __forceinline__ void q_row_to_tmem(uint32_t tile, int r, uint32_t taddr) {
-#pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-#pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      uint32_t w[8];
-      const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
-      const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                   : "r"(a0));
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                   : "r"(a1));
-      tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
-    }
   }
 }
 
@@ -127,8 +105,10 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
   uint64_t* s_full = v_empty + SV;  // [2]
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;    // P V of a tile done (its S buffer is free)
+  // per S buffer (tile parity), so that no waiter can fall two phases behind
+  // while the S and P V issuers run independently
+  uint64_t* p_full = s_full + 2;    // [2] P written over S
+  uint64_t* o_done = p_full + 2;    // [2] P V of a tile done (its S buffer is free)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   int* s_qpos = reinterpret_cast<int*>(smem + Cfg::kMisc + 16);
@@ -146,8 +126,10 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -231,41 +213,20 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      // --------------------------------------------------------- MMA issuer
-      // S_j = Q K_j^T into TMEM buffer j%2 (A = Q from TMEM); once the
-      // softmax has written P_j (fp16) over S_j: O += P_j V_j (A = P_j from
-      // TMEM).  Buffer j%2 is reused for S_{j+2} once P_j V_j has completed.
+      // ------------------------------------------------------ MMA issuer: S
+      // S_j = Q K_j^T into TMEM buffer j%2 (A = Q from TMEM); the buffer is
+      // reused for S_{j+2} once P_j V_j (which reads P_j from it) has
+      // completed.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_tmem, 0, ctl);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % SV;
-        const uint32_t ph = (i / SV) & 1;
-        if (!mbar_wait(p_full, i & 1, ctl)) return false;
-        if (!mbar_wait(&v_full[st], ph, ctl)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
-        const uint32_t pb = tmem + ((i & 1) ? Cfg::kTmemS1 : Cfg::kTmemS0);
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk,
-                     sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(o_done);
-        mma_commit(&v_empty[st]);
-        last_commit = o_done;
-        last_parity = i & 1;
-        return true;
-      };
       for (int j = 0; ok && j < n; ++j) {
         const int st = j % SK;
         const uint32_t ph = (j / SK) & 1;
         const int sb = j & 1;
         if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
-        // buffer sb last held P_{j-2}: wait until P_{j-2} V_{j-2} has read it
-        if (j >= 2 && !mbar_wait(o_done, (j - 2) & 1, ctl)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Cfg::kTileBytes);
         const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
@@ -278,9 +239,37 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&k_empty[st]);
         last_commit = &s_full[sb];
         last_parity = (j >> 1) & 1;
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
-      if (ok && n > 0) ok = issue_pv(n - 1);
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp == 3) {
+    if (lane == 0 && n > 0) {
+      // ----------------------------------------------------- MMA issuer: P V
+      // once the softmax has written P_j (fp16) over S_j: O += P_j V_j with
+      // A = P_j from TMEM.  A second issuing thread keeps this product queued
+      // while the S issuer waits.
+      constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % SV;
+        const uint32_t ph = (i / SV) & 1;
+        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait(&v_full[st], ph, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
+        const uint32_t pb = tmem + ((i & 1) ? Cfg::kTmemS1 : Cfg::kTmemS0);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk,
+                     sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&o_done[i & 1]);
+        mma_commit(&v_empty[st]);
+        last_commit = &o_done[i & 1];
+        last_parity = (i >> 1) & 1;
+      }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp >= 4) {
@@ -298,7 +287,7 @@ __global__ void __launch_bounds__(256, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, ctl))) {
         ok = false;
       } else {
-        q_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ);
+        sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(q_tmem);
@@ -369,7 +358,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // the reference max moved: rescale O once P_{j-1} V_{j-1} is in
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, ctl))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl))) {
           ok = false;
           break;
         }
@@ -386,10 +375,10 @@ __global__ void __launch_bounds__(256, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[j & 1]);
       m_run = m_new;
     }
-    if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, ctl))) {
+    if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, ctl))) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       const int hq = kvh * g + h;

@@ -285,6 +285,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 
 // ---------------------------------------------------------------- descriptors
 
+// Row r of a 128-row tile (K-major, 128-byte swizzled, D/64 regions of 16 KB)
+// into TMEM lane r as packed 16-bit pairs: columns [0, D/2).  The caller
+// waits for the stores (tmem_wait_st).
+template <int D>
+__device__ __forceinline__ void sw128_row_to_tmem(uint32_t tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      uint32_t w[8];
+      const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
+      const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(a0));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                   : "r"(a1));
+      tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
+    }
+  }
+}
+
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 at bit 46, swizzle
 // mode at bits 61-63 (2 = 128-byte swizzle).  Tiles are 1024-byte aligned,
