@@ -275,14 +275,15 @@ dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq))
     return DMA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   dma_status st;
   const int rows = p.batch * p.local_len;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
+  if ((st = map_rows_heads(&tdq, dq, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  return dma::launch_dq(*plan, lse, tq, tk, tv, tdo, dq, static_cast<cudaStream_t>(stream)) ==
+  return dma::launch_dq(*plan, lse, tq, tk, tv, tdo, tdq, dq, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;

@@ -58,14 +58,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
 }
 
-__device__ __forceinline__ void store_half_row_sw128(uint32_t region, int r, const uint32_t* pk) {
-  // 64 bf16 values (32 packed words) of row r into one 64-column region of a
-  // K-major 128-byte swizzled tile
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const uint32_t addr = region + r * 128 + ((ch ^ (r & 7)) << 4);
-    st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-  }
+// One arrival per warp: every lane has finished its TMEM accesses
+// (tcgen05.wait + fence before the thread sync), then lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // ---------------------------------------------------------------- Delta
@@ -384,18 +382,23 @@ __global__ void __launch_bounds__(384, 1)
     const long long stat_base0 = stat_row(0), stat_base1 = stat_row(1);
     float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
     const int steps = 2 * n;
+    // list entries of this tile (e) and the next (e_nx), loaded a tile ahead
     uint32_t e = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
+    uint32_t e_nx = n > 1 ? static_cast<uint32_t>(list[1]) : 0u;
     float nxt = (n > 0 && stager) ? stat_src[stat_base0 + static_cast<int>(e & kIndexMask) * P] : 0.f;
     bool ok = true;
     for (int s = 0; s < steps; ++s) {
       const int i = s >> 1, h = s & 1;
-      if (s > 0 && h == 0) e = static_cast<uint32_t>(list[i]);
+      if (s > 0 && h == 0) {
+        e = e_nx;
+        if (i + 1 < n) e_nx = static_cast<uint32_t>(list[i + 1]);
+      }
       {
         // stage this step's statistics, fetch the next step's
         const float cur = nxt;
         if (stager && s + 1 < steps) {
           const int s1 = s + 1;
-          const uint32_t e1 = (s1 & 1) ? e : static_cast<uint32_t>(list[s1 >> 1]);
+          const uint32_t e1 = (s1 & 1) ? e : e_nx;
           nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
         }
         if (stager) col[(s & 1) * 128 + r] = cur * stat_mul;
@@ -480,17 +483,12 @@ struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kRegion = 16384;
   static constexpr int kChunks = D / 64;
-  // Q and dO arrive through the dS buffer and K stage 2 (both unused until
-  // Q and dO have been copied into TMEM)
-  static constexpr int kStagesK = 3;
-  static constexpr int kK = 0;                       // 3 stages
-  static constexpr int kV = kK + kStagesK * kTile;   // 2 stages
-  static constexpr int kDS = kV + 2 * kTile;         // dS (128 x 128 bf16)
-  static constexpr int kQ = kDS;
-  static constexpr int kDO = kK + 2 * kTile;
+  // one ring of tile-sized slots carries every load in stream order: per
+  // work item Q, dO, then K_j, V_j for each key tile j of its row list
+  static constexpr int kSlots = (D == 128) ? 6 : 8;
+  static constexpr int kDS = kSlots * kTile;     // dS (128 x 128 bf16)
   static constexpr int kBar = kDS + 128 * 128 * 2;
-  static constexpr int kNumBars = 18;
-  static_assert(kTile <= 128 * 128 * 2, "Q staging exceeds the dS buffer");
+  static constexpr int kNumBars = 2 * kSlots + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -501,12 +499,38 @@ struct DqCfg {
   static_assert(kNeed <= kMaxSmem, "dQ shared-memory layout exceeds 227 KB");
 };
 
+// Work item `item` of the dQ pass: (sample, query tile) in longest-list-first
+// order times K/V head.
+struct DqItem {
+  int b, kvh, l0, n;
+  const int32_t* list;
+};
+__device__ __forceinline__ DqItem dq_item(const PlanDev& p, int item) {
+  DqItem it;
+  const int ord = item / p.n_kv_heads;
+  it.kvh = item % p.n_kv_heads;
+  const int bq = p.fwd_order[ord];
+  it.b = bq / p.n_qtiles;
+  it.l0 = (bq % p.n_qtiles) * p.tile_pos;
+  const int rp0 = p.row_ptr[bq];
+  it.n = p.row_ptr[bq + 1] - rp0;
+  it.list = p.row_idx + rp0;
+  return it;
+}
+
+// Persistent: CTA c takes work items c, c + gridDim.x, ...  Counters that
+// every role keeps identically across items: the stream index of the next
+// slot load (sidx), the number of key tiles processed so far (tbase, which
+// fixes the parity of every per-tile barrier) and the number of non-empty
+// items so far (ibase, the parity of qd_tmem).
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(640, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-              const PlanDev p, const float* __restrict__ lse, __nv_bfloat16* __restrict__ dq) {
+              const __grid_constant__ CUtensorMap tdq, const PlanDev p,
+              const float* __restrict__ lse, __nv_bfloat16* __restrict__ dq, int n_items) {
   using Cfg = DqCfg<D>;
+  constexpr int NS = Cfg::kSlots;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (__syncthreads_or(threadIdx.x == 0 &&
@@ -519,53 +543,40 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = smem_raw + pad;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
-  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
-  const int bq = p.fwd_order[ord];
-  const int b = bq / p.n_qtiles, qt = bq % p.n_qtiles;
-  const int l0 = qt * P;
-  const int rp0 = p.row_ptr[bq];
-  const int n = p.row_ptr[bq + 1] - rp0;
-  const int32_t* list = p.row_idx + rp0;
+  const int g = p.group, Lq = p.local_len;
 
-  uint8_t* sQ = smem + Cfg::kQ;
-  uint8_t* sDO = smem + Cfg::kDO;
-  uint8_t* sK = smem + Cfg::kK;
-  uint8_t* sV = smem + Cfg::kV;
   uint8_t* sDS = smem + Cfg::kDS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_full = bars;        // Q and dO
-  uint64_t* v_full = bars + 1;    // [2]
-  uint64_t* v_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;    // S of the current key tile computed
-  uint64_t* s_free = bars + 6;    // the row warps have read S
-  uint64_t* ds_full = bars + 7;   // dS written to shared memory
-  uint64_t* ds_done = bars + 8;   // dQ += dS K done reading dS
-  uint64_t* qd_tmem = bars + 9;   // Q and dO copied into TMEM
-  uint64_t* dp_full = bars + 10;  // dP computed
-  uint64_t* dp_free = bars + 11;  // the row warps have read dP
-  uint64_t* k_full = bars + 12;   // [3]
-  uint64_t* k_empty = bars + 15;  // [3]
+  uint64_t* slot_full = bars;           // [NS]
+  uint64_t* slot_empty = bars + NS;     // [NS]
+  uint64_t* s_full = bars + 2 * NS;     // S of a key tile computed
+  uint64_t* s_free = s_full + 1;        // the row warps have read S
+  uint64_t* dp_full = s_full + 2;       // dP computed
+  uint64_t* dp_free = s_full + 3;       // the row warps have read dP
+  uint64_t* ds_full = s_full + 4;       // dS written to shared memory
+  uint64_t* ds_done = s_full + 5;       // dQ += dS K done reading dS
+  uint64_t* qd_tmem = s_full + 6;       // Q and dO of an item copied into TMEM
+  uint64_t* epi_full = s_full + 7;      // an item's dQ tile staged in the dS buffer
+  uint64_t* epi_free = s_full + 8;      // its store has read the dS buffer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
+  auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTile; };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&slot_full[i], 1);
+      mbar_init(&slot_empty[i], 1);
     }
-    for (int i = 0; i < Cfg::kStagesK; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-    }
+    // the row warps arrive once per warp: 16 warps, of which the first 8 copy Q / dO
     mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
+    mbar_init(s_free, 16);
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 256);
-    mbar_init(ds_full, 256);
+    mbar_init(dp_free, 16);
+    mbar_init(ds_full, 16);
     mbar_init(ds_done, 1);
-    mbar_init(qd_tmem, 256);
+    mbar_init(qd_tmem, 8);
+    mbar_init(epi_full, 16);
+    mbar_init(epi_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -580,58 +591,61 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
   if (warp == 0) {
-    if (lane == 0 && n > 0) {
-      // ---------------------------------------- producer: Q, dO, then K, V
+    if (lane == 0) {
+      // ------------------------------------------------ producer: the stream
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tdo);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(q_full, 2 * Cfg::kTile);
-#pragma unroll
-      for (int c = 0; c < Cfg::kChunks; ++c) {
-        tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
-        tma_load_3d(sDO + c * Cfg::kRegion, &tdo, q_full, c * 64, kvh * g, b * Lq + l0);
-      }
-      int last_k = -1, last_v = -1;
+      int sidx = 0;
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        const int krow = b * p.seq_len + kt * kTileN;
-        {
-          const int st = j % Cfg::kStagesK;
-          const uint32_t ph = (j / Cfg::kStagesK) & 1;
-          // stage 2 first holds dO: wait until it has been copied into TMEM
-          if (j == 2 && !mbar_wait(qd_tmem, 0, ctl)) { ok = false; break; }
-          if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&k_full[st], Cfg::kTile);
+      auto acquire = [&](int idx) -> bool {
+        if (!mbar_wait(&slot_empty[idx % NS], ((idx / NS) & 1) ^ 1u, ctl)) return false;
+        mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTile);
+        return true;
+      };
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const DqItem it = dq_item(p, item);
+        if (it.n == 0) continue;
+        const int qrow = it.b * Lq + it.l0;
+        if (!acquire(sidx)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(slot_ptr(sidx) + c * Cfg::kRegion, &tq, &slot_full[sidx % NS], c * 64,
+                      it.kvh * g, qrow);
+        ++sidx;
+        if (!acquire(sidx)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(slot_ptr(sidx) + c * Cfg::kRegion, &tdo, &slot_full[sidx % NS], c * 64,
+                      it.kvh * g, qrow);
+        ++sidx;
+        for (int j = 0; j < it.n; ++j) {
+          const int kt = static_cast<int>(static_cast<uint32_t>(it.list[j]) & kIndexMask);
+          const int krow = it.b * p.seq_len + kt * kTileN;
+          if (!acquire(sidx)) { ok = false; break; }
 #pragma unroll
           for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_2d(sK + st * Cfg::kTile + c * Cfg::kRegion, &tk, &k_full[st],
-                        kvh * D + c * 64, krow);
-          last_k = j;
-        }
-        {
-          const int st = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&v_full[st], Cfg::kTile);
+            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tk, &slot_full[sidx % NS],
+                        it.kvh * D + c * 64, krow);
+          ++sidx;
+          if (!acquire(sidx)) { ok = false; break; }
 #pragma unroll
           for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_2d(sV + st * Cfg::kTile + c * Cfg::kRegion, &tv, &v_full[st],
-                        kvh * D + c * 64, krow);
-          last_v = j;
+            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tv, &slot_full[sidx % NS],
+                        it.kvh * D + c * 64, krow);
+          ++sidx;
         }
       }
-      if (!ok) {
-        drain_wait(q_full, 0, 100000000ull);
-        for (int jj = max(0, last_k - Cfg::kStagesK + 1); jj <= last_k; ++jj)
-          drain_wait(&k_full[jj % Cfg::kStagesK], (jj / Cfg::kStagesK) & 1, 100000000ull);
-        for (int jj = max(0, last_v - 1); jj <= last_v; ++jj)
-          drain_wait(&v_full[jj & 1], (jj >> 1) & 1, 100000000ull);
+      if (!ok) {  // drain this CTA's copies still in flight
+        for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
+          drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
       }
     }
   } else if (warp <= 3) {
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       // ------------------------------------------------------ MMA issuers
-      // per key tile j: S = Q K_j^T (warp 1) and dP = dO V_j^T (warp 2) into
+      // per key tile: S = Q K_j^T (warp 1) and dP = dO V_j^T (warp 2) into
       // TMEM with Q and dO as TMEM A operands; once the row warps have
       // written dS: dQ += dS K_j (warp 3).  S and dP have separate buffers,
       // each reissued as soon as the row warps have read it.  One issuing
@@ -642,178 +656,238 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
-      if (warp == 1) {
-        ok = mbar_wait(qd_tmem, 0, ctl);
-        for (int j = 0; ok && j < n; ++j) {
-          const int st = j % Cfg::kStagesK;
-          if (!mbar_wait(&k_full[st], (j / Cfg::kStagesK) & 1, ctl)) { ok = false; break; }
-          if (j > 0 && !mbar_wait(s_free, (j - 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
-            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_f16_ts(tmem + Cfg::kTmemS, tmem + Cfg::kTmemQ + 8 * kk,
-                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      int sidx = 0, tbase = 0, ibase = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const DqItem it = dq_item(p, item);
+        if (it.n == 0) continue;
+        if (warp == 1 || warp == 2) {
+          if (!mbar_wait(qd_tmem, ibase & 1, ctl)) { ok = false; break; }
+          // Q and dO are in TMEM: their slots go back to the producer
+          if (warp == 1) {
+            mbar_arrive(&slot_empty[sidx % NS]);
+            mbar_arrive(&slot_empty[(sidx + 1) % NS]);
           }
-          mma_commit(s_full);
-          last_commit = s_full;
-          last_parity = j & 1;
         }
-      } else if (warp == 2) {
-        ok = mbar_wait(qd_tmem, 0, ctl);
-        for (int j = 0; ok && j < n; ++j) {
-          const int st = j & 1;
-          if (!mbar_wait(&v_full[st], (j >> 1) & 1, ctl)) { ok = false; break; }
-          if (j > 0 && !mbar_wait(dp_free, (j - 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(sV + st * Cfg::kTile);
+        for (int j = 0; j < it.n; ++j) {
+          const int t = tbase + j;
+          const int kidx = sidx + 2 + 2 * j, vidx = kidx + 1;
+          if (warp == 1) {
+            if (!mbar_wait(&slot_full[kidx % NS], (kidx / NS) & 1, ctl)) { ok = false; break; }
+            if (t > 0 && !mbar_wait(s_free, (t - 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(slot_ptr(kidx));
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
-            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_f16_ts(tmem + Cfg::kTmemDP, tmem + Cfg::kTmemDO + 8 * kk,
-                       sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(dp_full);
-          mma_commit(&v_empty[st]);
-          last_commit = dp_full;
-          last_parity = j & 1;
-        }
-      } else {
-        // S_j has completed before dS_j exists, so the K stage is free once
-        // this product is done
-        const uint32_t ds_addr = smem_u32(sDS);
-        for (int j = 0; ok && j < n; ++j) {
-          const int st = j % Cfg::kStagesK;
-          if (!mbar_wait(ds_full, j & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + st * Cfg::kTile);
+            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
+              const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+              mma_f16_ts(tmem + Cfg::kTmemS, tmem + Cfg::kTmemQ + 8 * kk,
+                         sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full);
+            last_commit = s_full;
+            last_parity = t & 1;
+          } else if (warp == 2) {
+            if (!mbar_wait(&slot_full[vidx % NS], (vidx / NS) & 1, ctl)) { ok = false; break; }
+            if (t > 0 && !mbar_wait(dp_free, (t - 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(slot_ptr(vidx));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dQ += dS K
-            const uint64_t a =
-                sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
-            mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
+              const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+              mma_f16_ts(tmem + Cfg::kTmemDP, tmem + Cfg::kTmemDO + 8 * kk,
+                         sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(dp_full);
+            mma_commit(&slot_empty[vidx % NS]);
+            last_commit = dp_full;
+            last_parity = t & 1;
+          } else {
+            // S_j has completed before dS_j exists, so K_j's slot is free
+            // once this product is done
+            if (!mbar_wait(ds_full, t & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ds_addr = smem_u32(sDS);
+            const uint32_t k_addr = smem_u32(slot_ptr(kidx));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // dQ += dS K
+              const uint64_t a =
+                  sdesc_sw128(ds_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(k_addr + kk * 2048, Cfg::kRegion, 1024);
+              mma_bf16_ss(tmem + Cfg::kTmemDQ, a, bd, idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(ds_done);
+            mma_commit(&slot_empty[kidx % NS]);
+            last_commit = ds_done;
+            last_parity = t & 1;
           }
-          mma_commit(ds_done);
-          mma_commit(&k_empty[st]);
-          last_commit = ds_done;
-          last_parity = j & 1;
         }
+        if (ok && warp == 3) {
+          // the row warps staged this item's dQ tile (bf16, the layout a
+          // Q tile load produces) in the dS buffer: store it, and hand the
+          // buffer back once the store has read it
+          if (!mbar_wait(epi_full, ibase & 1, ctl)) { ok = false; break; }
+#pragma unroll
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_store_3d(&tdq, sDS + c * Cfg::kRegion, c * 64, it.kvh * g, it.b * Lq + it.l0);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(epi_free);
+        }
+        sidx += 2 + 2 * it.n;
+        tbase += it.n;
+        ++ibase;
       }
+      if (warp == 3) bulk_wait_all();
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
-  } else if (warp >= 4) {
+  } else {
     // ----------------------------------------------------------- query rows
-    // two warpgroups: thread (r, half) owns query row r and key columns
-    // [64*half, 64*half + 64) of each key tile (one 64-column swizzle region)
+    // four warpgroups: thread (r, q) owns query row r and key columns
+    // [32q, 32q + 32) of each key tile
     const int r = (threadIdx.x - 128) & 127;
-    const int half = (threadIdx.x - 128) >> 7;
-    const int cbase = 64 * half;
+    const int q = (threadIdx.x - 128) >> 7;
+    const int cbase = 32 * q;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
     const int pos = r >> lg, h = r & (g - 1);
-    const int l = l0 + pos;
     const int C = p.chunk;
-    const int qabs = (l < C) ? (p.cp_rank * C + l) : ((2 * p.cp_size - 1 - p.cp_rank) * C + l - C);
-    const int lo_r = p.doc_lo[static_cast<long long>(b) * Lq + l];
-    const int hq = kvh * g + h;
-    const long long stat = (static_cast<long long>(b) * p.n_heads + hq) * Lq + l;
-    const float lse2 = lse[stat] * kLog2e;
-    const float del = p.delta[stat];
     const float sl2 = p.scale_log2;
-    const uint32_t ds_region = smem_u32(sDS) + half * Cfg::kRegion;
+    // this thread's 64 bytes of dS row r: one half of a 64-column region
+    const uint32_t ds_row = smem_u32(sDS) + (q >> 1) * Cfg::kRegion + r * 128;
+    const int ch0 = (q & 1) * 4;
+    constexpr int DQ = D / 4;  // head_dim columns of dQ this warpgroup writes
     bool ok = true;
-    if (n > 0) {
-      // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
-      ok = warp_wait(q_full, 0, ctl);
-      if (ok) {
-        sw128_row_to_tmem<D>(smem_u32(half ? sDO : sQ), r,
-                             tmem + lane_base + (half ? Cfg::kTmemDO : Cfg::kTmemQ));
+    int sidx = 0, tbase = 0, ibase = 0;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const DqItem it = dq_item(p, item);
+      const int l = it.l0 + pos;
+      const int hq = it.kvh * g + h;
+      uint4* dst = reinterpret_cast<uint4*>(
+          dq + ((static_cast<long long>(it.b) * Lq + l) * p.n_heads + hq) * D + q * DQ);
+      if (it.n == 0) {
+#pragma unroll
+        for (int c = 0; c < DQ / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const int qabs =
+          (l < C) ? (p.cp_rank * C + l) : ((2 * p.cp_size - 1 - p.cp_rank) * C + l - C);
+      const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + l];
+      const long long stat = (static_cast<long long>(it.b) * p.n_heads + hq) * Lq + l;
+      const float lse2 = lse[stat] * kLog2e;
+      const float del = p.delta[stat];
+      if (q < 2) {
+        // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
+        // (the previous item's S and dP products have all completed)
+        const int idx = sidx + q;
+        if (!warp_wait(&slot_full[idx % NS], (idx / NS) & 1, ctl)) { ok = false; break; }
+        sw128_row_to_tmem<D>(smem_u32(slot_ptr(idx)), r,
+                             tmem + lane_base + (q ? Cfg::kTmemDO : Cfg::kTmemQ));
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(qd_tmem);
+        warp_arrive(qd_tmem);
       }
-    }
-    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
-    for (int j = 0; ok && j < n; ++j) {
-      const uint32_t e = e_next;  // list entries run one tile ahead
-      if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
-      int c_lo = 0, c_hi = 128;
-      if (e & kPartialBit) {
-        const int k0 = static_cast<int>(e & kIndexMask) * kTileN;
-        c_lo = lo_r - k0;
-        c_hi = qabs - k0 + 1;
+      uint32_t e_next = static_cast<uint32_t>(it.list[0]);
+      for (int j = 0; j < it.n; ++j) {
+        const int t = tbase + j;
+        const uint32_t e = e_next;  // list entries run one tile ahead
+        if (j + 1 < it.n) e_next = static_cast<uint32_t>(it.list[j + 1]);
+        uint32_t allow = 0xFFFFFFFFu;
+        if (e & kPartialBit) {
+          const int k0 = static_cast<int>(e & kIndexMask) * kTileN + cbase;
+          allow = range_bits(lo_r - k0, qabs - k0 + 1);
+        }
+        // P = exp2(S * scale*log2e - LSE*log2e) for this thread's 32 columns
+        if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        float pv[32];
+        {
+          uint32_t su[32];
+          tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemS + cbase, su);
+          tmem_wait_ld();
+          reg_fence32(su);
+          const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(-lse2, -lse2);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t x = f2_fma(f2(__uint_as_float(su[c]), __uint_as_float(su[c + 1])),
+                                      sl2x2, nlse2x2);
+            float x0, x1;
+            f2_split(x, x0, x1);
+            pv[c] = ex2(x0);
+            pv[c + 1] = ex2(x1);
+          }
+          if (allow != 0xFFFFFFFFu) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!((allow >> c) & 1u)) pv[c] = 0.f;
+          }
+        }
+        warp_arrive(s_free);
+        // dS = P (dP - Delta)
+        if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pk[16];
+        {
+          uint32_t du[32];
+          tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase, du);
+          tmem_wait_ld();
+          reg_fence32(du);
+          const uint64_t delx2 = f2(del, del);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t d = f2_mul(f2(pv[c], pv[c + 1]),
+                                      f2_sub(f2(__uint_as_float(du[c]), __uint_as_float(du[c + 1])),
+                                             delx2));
+            float d0, d1;
+            f2_split(d, d0, d1);
+            pk[c >> 1] = pack_bf16(d0, d1);
+          }
+        }
+        warp_arrive(dp_free);
+        if (t > 0 && !warp_wait(ds_done, (t - 1) & 1, ctl)) { ok = false; break; }
+        // the dS buffer may still be read by the store of the previous dQ tile
+        if (j == 0 && ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(ds_row + (((ch0 + c) ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                       pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
       }
-      // P = exp2(S * scale*log2e - LSE*log2e) for this thread's 64 columns
-      if (!warp_wait(s_full, j & 1, ctl)) { ok = false; break; }
+      if (!ok) break;
+      // epilogue: dQ (scaled, bf16) staged in the dS buffer in the layout of
+      // a Q tile load (64-column regions, row r = 128 bytes, 16-byte chunks
+      // swizzled by r & 7); the dQ issuer stores it with one TMA store per
+      // region.  Warpgroup q stages head_dim columns [q*D/4, (q+1)*D/4).
+      const int t_last = tbase + it.n - 1;
+      if (!warp_wait(ds_done, t_last & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      const bool masked = (e & kPartialBit) != 0;
-      float pv[64];
+      {
+        const float sc = p.scale;
+        const uint32_t row = smem_u32(sDS) + ((q * DQ) / 64) * Cfg::kRegion + r * 128;
+        const int chb = ((q * DQ) % 64) / 8;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        const int cg = cbase + c0;
-        uint32_t su[32];
-        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemS + cg, su);
-        tmem_wait_ld();
-        reg_fence32(su);
-        const uint32_t allow = masked ? range_bits(c_lo - cg, c_hi - cg) : 0xFFFFFFFFu;
+        for (int c0 = 0; c0 < DQ; c0 += 16) {
+          uint32_t u[16];
+          tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDQ + q * DQ + c0, u);
+          tmem_wait_ld();
+          reg_fence16(u);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const float pj = ex2(fmaf(__uint_as_float(su[t]), sl2, -lse2));
-          pv[c0 + t] = ((allow >> t) & 1u) ? pj : 0.f;
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int ch = chb + c0 / 8 + q2;
+            st_shared_v4(row + ((ch ^ (r & 7)) << 4),
+                         pack_bf16(__uint_as_float(u[8 * q2 + 0]) * sc, __uint_as_float(u[8 * q2 + 1]) * sc),
+                         pack_bf16(__uint_as_float(u[8 * q2 + 2]) * sc, __uint_as_float(u[8 * q2 + 3]) * sc),
+                         pack_bf16(__uint_as_float(u[8 * q2 + 4]) * sc, __uint_as_float(u[8 * q2 + 5]) * sc),
+                         pack_bf16(__uint_as_float(u[8 * q2 + 6]) * sc, __uint_as_float(u[8 * q2 + 7]) * sc));
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(s_free);
-      // dS = P (dP - Delta)
-      if (!warp_wait(dp_full, j & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t du[32];
-        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase + c0, du);
-        tmem_wait_ld();
-        reg_fence32(du);
-#pragma unroll
-        for (int t = 0; t < 32; t += 2)
-          pk[(c0 + t) >> 1] = pack_bf16(pv[c0 + t] * (__uint_as_float(du[t]) - del),
-                                        pv[c0 + t + 1] * (__uint_as_float(du[t + 1]) - del));
-      }
-      tc_fence_before();
-      mbar_arrive(dp_free);
-      if (j > 0 && !warp_wait(ds_done, (j - 1) & 1, ctl)) { ok = false; break; }
-      store_half_row_sw128(ds_region, r, pk);
       fence_proxy_async_smem();
-      mbar_arrive(ds_full);
-    }
-    // each warpgroup writes half of the row's head_dim columns
-    constexpr int DH = D / 2;
-    uint4* dst = reinterpret_cast<uint4*>(
-        dq + ((static_cast<long long>(b) * Lq + l) * p.n_heads + hq) * D + half * DH);
-    if (n == 0) {
-#pragma unroll
-      for (int c = 0; c < DH / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-    } else if (ok && warp_wait(ds_done, (n - 1) & 1, ctl)) {
-      tc_fence_after();
-      const float sc = p.scale;
-#pragma unroll
-      for (int c0 = 0; c0 < DH; c0 += 16) {
-        uint32_t u[16];
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDQ + half * DH + c0, u);
-        tmem_wait_ld();
-        reg_fence16(u);
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(u[8 * q2 + 0]) * sc, __uint_as_float(u[8 * q2 + 1]) * sc);
-          w.y = pack_bf16(__uint_as_float(u[8 * q2 + 2]) * sc, __uint_as_float(u[8 * q2 + 3]) * sc);
-          w.z = pack_bf16(__uint_as_float(u[8 * q2 + 4]) * sc, __uint_as_float(u[8 * q2 + 5]) * sc);
-          w.w = pack_bf16(__uint_as_float(u[8 * q2 + 6]) * sc, __uint_as_float(u[8 * q2 + 7]) * sc);
-          dst[c0 / 8 + q2] = w;
-        }
-      }
+      // the next item's first dQ product overwrites the accumulator only
+      // after every warp has arrived on ds_full for it, i.e. after this read
+      warp_arrive(epi_full);
+      sidx += 2 + 2 * it.n;
+      tbase += it.n;
+      ++ibase;
     }
   }
 
@@ -855,15 +929,17 @@ cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensor
 template <int D>
 cudaError_t launch_dq_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        dma_bf16* dq, cudaStream_t s) {
+                        const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  const int grid = p.batch * p.n_qtiles * p.n_kv_heads;
-  if (grid == 0) return cudaSuccess;
+  const int items = p.batch * p.n_qtiles * p.n_kv_heads;
+  if (items == 0) return cudaSuccess;
+  // persistent: one CTA per SM (TMEM and shared memory allow no more)
+  const int grid = items < pl.num_sms ? items : pl.num_sms;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DqCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dq_kernel<D><<<grid, 384, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse,
-                                                   reinterpret_cast<__nv_bfloat16*>(dq));
+  dq_kernel<D><<<grid, 640, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdq, p, lse,
+                                                   reinterpret_cast<__nv_bfloat16*>(dq), items);
   return cudaGetLastError();
 }
 
@@ -884,9 +960,9 @@ cudaError_t launch_dkdv(const dma_plan_s& pl, const float* lse, const CUtensorMa
 
 cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      dma_bf16* dq, cudaStream_t s) {
-  return pl.d.head_dim == 128 ? launch_dq_d<128>(pl, lse, tq, tk, tv, tdo, dq, s)
-                              : launch_dq_d<64>(pl, lse, tq, tk, tv, tdo, dq, s);
+                      const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_dq_d<128>(pl, lse, tq, tk, tv, tdo, tdq, dq, s)
+                              : launch_dq_d<64>(pl, lse, tq, tk, tv, tdo, tdq, dq, s);
 }
 
 }  // namespace dma

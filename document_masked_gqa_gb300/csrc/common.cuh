@@ -70,6 +70,6 @@ cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap
                         float* dk, float* dv, cudaStream_t s);
 cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      dma_bf16* dq, cudaStream_t s);
+                      const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 }  // namespace dma
