@@ -58,14 +58,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
 }
 
-// One arrival per warp: every lane has finished its TMEM accesses
-// (tcgen05.wait + fence before the thread sync), then lane 0 arrives.
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-  tc_fence_before();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 // ---------------------------------------------------------------- Delta
 
 // Delta[(b*Hq + h)*Lq + l] = sum_d dO[b,l,h,d] * O[b,l,h,d] (O fp32, dO bf16);
@@ -757,6 +749,7 @@ __global__ void __launch_bounds__(640, 1)
     constexpr int DQ = D / 4;  // head_dim columns of dQ this warpgroup writes
     bool ok = true;
     int sidx = 0, tbase = 0, ibase = 0;
+    int copied = -1;  // item whose Q / dO are already in TMEM
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const DqItem it = dq_item(p, item);
       const int l = it.l0 + pos;
@@ -774,16 +767,19 @@ __global__ void __launch_bounds__(640, 1)
       const long long stat = (static_cast<long long>(it.b) * p.n_heads + hq) * Lq + l;
       const float lse2 = lse[stat] * kLog2e;
       const float del = p.delta[stat];
-      if (q < 2) {
-        // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
-        // (the previous item's S and dP products have all completed)
-        const int idx = sidx + q;
-        if (!warp_wait(&slot_full[idx % NS], (idx / NS) & 1, ctl)) { ok = false; break; }
+      // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
+      // (the previous item's S and dP products have all completed); after
+      // the first item this happened already, ahead of the previous epilogue
+      auto copy_qdo = [&](int slot_idx) -> bool {
+        const int idx = slot_idx + q;
+        if (!warp_wait(&slot_full[idx % NS], (idx / NS) & 1, ctl)) return false;
         sw128_row_to_tmem<D>(smem_u32(slot_ptr(idx)), r,
                              tmem + lane_base + (q ? Cfg::kTmemDO : Cfg::kTmemQ));
         tmem_wait_st();
         warp_arrive(qd_tmem);
-      }
+        return true;
+      };
+      if (q < 2 && copied != item && !copy_qdo(sidx)) { ok = false; break; }
       uint32_t e_next = static_cast<uint32_t>(it.list[0]);
       for (int j = 0; j < it.n; ++j) {
         const int t = tbase + j;
@@ -853,6 +849,17 @@ __global__ void __launch_bounds__(640, 1)
         if (lane == 0) mbar_arrive(ds_full);
       }
       if (!ok) break;
+      // the last S and dP of this item have been read: bring in the next
+      // non-empty item's Q and dO now, so that its first products overlap
+      // this epilogue
+      {
+        int nx = item + gridDim.x;
+        while (nx < n_items && dq_item(p, nx).n == 0) nx += gridDim.x;
+        if (nx < n_items) {
+          if (q < 2 && !copy_qdo(sidx + 2 + 2 * it.n)) { ok = false; break; }
+          copied = nx;
+        }
+      }
       // epilogue: dQ (scaled, bf16) staged in the dS buffer in the layout of
       // a Q tile load (64-column regions, row r = 128 bytes, 16-byte chunks
       // swizzled by r & 7); the dQ issuer stores it with one TMA store per

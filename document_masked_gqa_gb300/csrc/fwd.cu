@@ -49,7 +49,7 @@ struct FwdCfg {
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 3;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
   static constexpr int kSmemBytes = kEnd + 1024;
@@ -70,7 +70,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const PlanDev p,
                float* __restrict__ o, float* __restrict__ lse) {
@@ -109,14 +109,17 @@ __global__ void __launch_bounds__(256, 1)
   // while the S and P V issuers run independently
   uint64_t* p_full = s_full + 2;    // [2] P written over S
   uint64_t* o_done = p_full + 2;    // [2] P V of a tile done (its S buffer is free)
+  uint64_t* mx_ready = o_done + 2;  // [2] both softmax warpgroups posted a tile's row maxima
+  uint64_t* l_ready = mx_ready + 2; // both posted their partial row sums
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   int* s_qpos = reinterpret_cast<int*>(smem + Cfg::kMisc + 16);
   int* s_lo = s_qpos + 128;
 
   if (threadIdx.x == 0) {
+    // the softmax warps arrive once per warp (8 warps; 4 of them copy Q)
     mbar_init(q_full, 1);
-    mbar_init(q_tmem, 128);
+    mbar_init(q_tmem, 4);
     for (int i = 0; i < SK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -127,9 +130,11 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 8);
       mbar_init(&o_done[i], 1);
+      mbar_init(&mx_ready[i], 8);
     }
+    mbar_init(l_ready, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -261,8 +266,8 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
         const uint32_t pb = tmem + ((i & 1) ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk,
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
+          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
                      sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
                      (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&o_done[i & 1]);
@@ -274,23 +279,32 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax
-    const int r = threadIdx.x - 128;
+    // two warpgroups; thread (r, w) owns row r and key columns [64w, 64w+64)
+    // of every tile.  Per tile the two post their partial row maxima and
+    // take the same reference max; each keeps its own partial row sum and
+    // writes its half of P (fp16 pairs) over the first 32 columns of the S
+    // columns it read, so neither overwrites what the other still reads.
+    const int r = (threadIdx.x - 128) & 127;
+    const int w = (threadIdx.x - 128) >> 7;
+    const int cw = 64 * w;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
     const int pos = r >> lg, h = r & (g - 1);
     const int qabs = s_qpos[pos], lo_r = s_lo[pos];
     const float sl2 = p.scale_log2;
+    // row maxima / sums exchange in the Q buffer, free once Q is in TMEM
+    float* xmax = reinterpret_cast<float*>(sQ);        // [2 tiles][2 warpgroups][128]
+    float* xsum = xmax + 2 * 2 * 128;                  // [2 warpgroups][128]
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
     bool ok = true;
-    if (n > 0) {  // row r of Q into TMEM (bf16 pairs), the A operand of Q K^T
+    if (n > 0 && w == 0) {  // row r of Q into TMEM (bf16 pairs), the A operand of Q K^T
       if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, ctl))) {
         ok = false;
       } else {
         sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ);
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(q_tmem);
+        warp_arrive(q_tmem);
       }
     }
     for (int j = 0; ok && j < n; ++j) {
@@ -300,49 +314,54 @@ __global__ void __launch_bounds__(256, 1)
         break;
       }
       tc_fence_after();
-      float s[128];
+      const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0) + cw;
+      float s[64];
       {
-        const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
-        uint32_t u[128];
+        uint32_t u[64];
         tmem_ld32_nowait(sc, u);
         tmem_ld32_nowait(sc + 32, u + 32);
-        tmem_ld32_nowait(sc + 64, u + 64);
-        tmem_ld32_nowait(sc + 96, u + 96);
         tmem_wait_ld();
         reg_fence32(u);
         reg_fence32(u + 32);
-        reg_fence32(u + 64);
-        reg_fence32(u + 96);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+        for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
       }
       const uint32_t e = e_next;  // list entries run one tile ahead
       if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
       if (e & kPartialBit) {
-        const int k0 = static_cast<int>(e & kIndexMask) * kTileN;
+        const int k0 = static_cast<int>(e & kIndexMask) * kTileN + cw;
         const int lo_c = lo_r - k0, hi_c = qabs - k0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c < lo_c || c > hi_c) s[c] = -INFINITY;
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
+      for (int c = 4; c < 64; c += 4) {
         mx0 = fmaxf(mx0, s[c]);
         mx1 = fmaxf(mx1, s[c + 1]);
         mx2 = fmaxf(mx2, s[c + 2]);
         mx3 = fmaxf(mx3, s[c + 3]);
       }
-      const float mxl2 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      xmax[(sb * 2 + w) * 128 + r] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mx_ready[sb]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&mx_ready[sb], (j >> 1) & 1, ctl))) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xmax[(sb * 2 + (w ^ 1)) * 128 + r]);
+      const float mxl2 = mx * sl2;
       const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2(m_run - m_ref);
       // P enters the P V product in fp16 (11-bit significand) against an
       // fp16 copy of V; its values lie in [0, 2^8] thanks to the lazy max.
       float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
+      for (int c = 0; c < 64; c += 2) {
         const float e0 = ex2(fmaf(s[c], sl2, -m_ref));
         const float e1 = ex2(fmaf(s[c + 1], sl2, -m_ref));
         sum0 += e0;
@@ -350,23 +369,20 @@ __global__ void __launch_bounds__(256, 1)
         pk[c >> 1] = pack_f16(e0, e1);
       }
       l_run = l_run * alpha + (sum0 + sum1);
-      // P (fp16 pairs) over the first 64 columns of this tile's S buffer
-      {
-        const uint32_t pb = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) tmem_st8_nowait(pb + 8 * q, pk + 8 * q);
-      }
+      for (int q = 0; q < 4; ++q) tmem_st8_nowait(sc + 8 * q, pk + 8 * q);
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // the reference max moved: rescale O once P_{j-1} V_{j-1} is in
+        // the reference max moved: rescale this warpgroup's half of O once
+        // P_{j-1} V_{j-1} is in
         if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
           float t[32];
-          const uint32_t oc = tmem + lane_base + Cfg::kTmemO + c0;
+          const uint32_t oc = tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0;
           tmem_ld32(oc, t);
 #pragma unroll
           for (int i = 0; i < 32; ++i) t[i] *= alpha;
@@ -374,27 +390,34 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      warp_arrive(&p_full[sb]);
       m_run = m_new;
+    }
+    if (ok && n > 0) {
+      xsum[w * 128 + r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(l_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(l_ready, 0, ctl));
     }
     if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, ctl))) {
       tc_fence_after();
-      const float inv = 1.f / l_run;
+      const float l_tot = xsum[r] + xsum[128 + r];
+      const float inv = 1.f / l_tot;
       const int hq = kvh * g + h;
       const long long row = static_cast<long long>(b) * Lq + l0 + pos;
-      float4* dst = reinterpret_cast<float4*>(o + (row * p.n_heads + hq) * D);
+      float4* dst = reinterpret_cast<float4*>(o + (row * p.n_heads + hq) * D + w * (D / 2));
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         float t[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemO + c0, t);
+        tmem_ld32(tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0, t);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
           dst[c0 / 4 + q4] = make_float4(t[4 * q4] * inv, t[4 * q4 + 1] * inv,
                                          t[4 * q4 + 2] * inv, t[4 * q4 + 3] * inv);
       }
-      lse[(static_cast<long long>(b) * p.n_heads + hq) * Lq + l0 + pos] =
-          (m_run + lg2(l_run)) * 0.6931471805599453f;
+      if (w == 0)
+        lse[(static_cast<long long>(b) * p.n_heads + hq) * Lq + l0 + pos] =
+            (m_run + lg2(l_tot)) * 0.6931471805599453f;
     }
   }
 
@@ -434,7 +457,7 @@ cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUte
   const int smem = FwdCfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D><<<grid, 256, smem, s>>>(tq, tk, tv16, p, o, lse);
+  fwd_kernel<D><<<grid, 384, smem, s>>>(tq, tk, tv16, p, o, lse);
   return cudaGetLastError();
 }
 

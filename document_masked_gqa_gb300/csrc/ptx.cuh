@@ -181,6 +181,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// One arrival per warp: every lane has finished its TMEM accesses
+// (tcgen05.wait + fence before the thread sync), then lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T-ish per the descriptors; f16-family kinds.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
