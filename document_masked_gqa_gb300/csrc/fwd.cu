@@ -40,21 +40,21 @@ namespace {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStagesK = 3;
-  static constexpr int kStagesV = 3;
   static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (16-bit)
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + kStagesK * kTileBytes;
-  static constexpr int kBar = kV + kStagesV * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 3;
+  // one ring of tile-sized slots carries every load in stream order: per
+  // work item Q, then K_j, V_j for each key tile j of its row list
+  static constexpr int kSlots = (D == 128) ? 6 : 10;
+  static constexpr int kStage = kSlots * kTileBytes;  // O epilogue staging, 2 KB per softmax warp
+  static constexpr int kXchg = kStage + 8 * 2048;     // row maxima [2][2][128], row sums [2][2][128]
+  static constexpr int kBar = kXchg + (2 * 2 * 128 + 2 * 2 * 128) * 4;
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kEnd = kMisc + 16 + 2 * 128 * 4;
+  static constexpr int kEnd = kMisc + 16;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM: S buffers (128 columns each; P overwrites their first 64 as fp16
+  // TMEM: S buffers (128 columns each; P overwrites part of them as fp16
   // pairs), the O accumulator, and Q as bf16 pairs (the A operand of Q K^T)
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
   static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
@@ -69,13 +69,37 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
+// Work item `item`: (sample, query tile) in longest-list-first order times
+// K/V head.
+struct FwdItem {
+  int b, kvh, l0, n;
+  const int32_t* list;
+};
+__device__ __forceinline__ FwdItem fwd_item(const PlanDev& p, int item) {
+  FwdItem it;
+  const int ord = item / p.n_kv_heads;
+  it.kvh = item % p.n_kv_heads;
+  const int bq = p.fwd_order[ord];
+  it.b = bq / p.n_qtiles;
+  it.l0 = (bq % p.n_qtiles) * p.tile_pos;
+  const int rp0 = p.row_ptr[bq];
+  it.n = p.row_ptr[bq + 1] - rp0;
+  it.list = p.row_idx + rp0;
+  return it;
+}
+
+// Persistent: CTA c takes work items c, c + gridDim.x, ...  Every role keeps
+// the same counters across items: the stream index of the next slot load
+// (sidx), the key tiles processed so far (tbase: S buffer t & 1 and every
+// per-tile barrier parity follow from the global tile index t) and the
+// items so far (ibase: parity of q_tmem and l_ready).
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const PlanDev p,
-               float* __restrict__ o, float* __restrict__ lse) {
+               float* __restrict__ o, float* __restrict__ lse, int n_items) {
   using Cfg = FwdCfg<D>;
-  constexpr int SK = Cfg::kStagesK, SV = Cfg::kStagesV;
+  constexpr int NS = Cfg::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
@@ -85,68 +109,43 @@ __global__ void __launch_bounds__(384, 1)
     return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
-  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
-  const int bq = p.fwd_order[ord];
-  const int b = bq / p.n_qtiles, qt = bq % p.n_qtiles;
-  const int l0 = qt * P;
-  const int rp0 = p.row_ptr[bq];
-  const int n = p.row_ptr[bq + 1] - rp0;
-  const int32_t* list = p.row_idx + rp0;
+  const int g = p.group, Lq = p.local_len;
 
-  uint8_t* sQ = smem + Cfg::kQ;
-  uint8_t* sK = smem + Cfg::kK;
-  uint8_t* sV = smem + Cfg::kV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_full = bars;          // Q in shared memory
-  uint64_t* q_tmem = bars + 1;      // Q copied into TMEM
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = k_full + SK;
-  uint64_t* v_full = k_empty + SK;
-  uint64_t* v_empty = v_full + SV;
-  uint64_t* s_full = v_empty + SV;  // [2]
+  uint64_t* slot_full = bars;          // [NS]
+  uint64_t* slot_empty = bars + NS;    // [NS]
+  uint64_t* s_full = bars + 2 * NS;    // [2] S computed in buffer t & 1
   // per S buffer (tile parity), so that no waiter can fall two phases behind
   // while the S and P V issuers run independently
-  uint64_t* p_full = s_full + 2;    // [2] P written over S
-  uint64_t* o_done = p_full + 2;    // [2] P V of a tile done (its S buffer is free)
-  uint64_t* mx_ready = o_done + 2;  // [2] both softmax warpgroups posted a tile's row maxima
-  uint64_t* l_ready = mx_ready + 2; // both posted their partial row sums
+  uint64_t* p_full = s_full + 2;       // [2] P written over S
+  uint64_t* o_done = p_full + 2;       // [2] P V of a tile done (its S buffer is free)
+  uint64_t* mx_ready = o_done + 2;     // [2] both softmax warpgroups posted a tile's row maxima
+  uint64_t* l_ready = mx_ready + 2;    // both posted an item's partial row sums
+  uint64_t* q_tmem = l_ready + 1;      // an item's Q copied into TMEM
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
-  int* s_qpos = reinterpret_cast<int*>(smem + Cfg::kMisc + 16);
-  int* s_lo = s_qpos + 128;
+  auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTileBytes; };
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&slot_full[i], 1);
+      mbar_init(&slot_empty[i], 1);
+    }
     // the softmax warps arrive once per warp (8 warps; 4 of them copy Q)
-    mbar_init(q_full, 1);
-    mbar_init(q_tmem, 4);
-    for (int i = 0; i < SK; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < SV; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
       mbar_init(&o_done[i], 1);
       mbar_init(&mx_ready[i], 8);
     }
     mbar_init(l_ready, 8);
+    mbar_init(q_tmem, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, Cfg::kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == 2 || warp == 3) {
-    for (int r = threadIdx.x - 64; r < P; r += 64) {
-      s_qpos[r] = p.qpos[l0 + r];
-      s_lo[r] = p.doc_lo[static_cast<long long>(b) * Lq + l0 + r];
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -156,124 +155,107 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------- producer: Q, then K
+      // ------------------------------------------------ producer: the stream
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
-      int last_k[SK];
-#pragma unroll
-      for (int i = 0; i < SK; ++i) last_k[i] = -1;
-      mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < Cfg::kChunks; ++c)
-        tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, kvh * g, b * Lq + l0);
-      bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % SK;
-        const uint32_t ph = (j / SK) & 1;
-        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&k_full[st], Cfg::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_2d(sK + st * Cfg::kTileBytes + c * Cfg::kRegion, &tk, &k_full[st],
-                      kvh * D + c * 64, b * p.seq_len + kt * kTileN);
-#pragma unroll
-        for (int i = 0; i < SK; ++i)
-          if (i == st) last_k[i] = static_cast<int>(ph);
-      }
-      if (!ok) {  // drain our own copies before the CTA exits
-        drain_wait(q_full, 0, 100000000ull);
-#pragma unroll
-        for (int i = 0; i < SK; ++i)
-          if (last_k[i] >= 0) drain_wait(&k_full[i], last_k[i], 100000000ull);
-      }
-    }
-  } else if (warp == 2) {
-    if (lane == 0) {
-      // ------------------------------------------------------ producer: V
       tma_prefetch_desc(&tv);
-      int last_v[SV];
-#pragma unroll
-      for (int i = 0; i < SV; ++i) last_v[i] = -1;
+      int sidx = 0;
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % SV;
-        const uint32_t ph = (j / SV) & 1;
-        const int kt = static_cast<int>(static_cast<uint32_t>(list[j]) & kIndexMask);
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&v_full[st], Cfg::kTileBytes);
+      auto acquire = [&](int idx) -> bool {
+        if (!mbar_wait(&slot_empty[idx % NS], ((idx / NS) & 1) ^ 1u, ctl)) return false;
+        mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTileBytes);
+        return true;
+      };
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const FwdItem it = fwd_item(p, item);
+        if (it.n == 0) continue;
+        if (!acquire(sidx)) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_2d(sV + st * Cfg::kTileBytes + c * Cfg::kRegion, &tv, &v_full[st],
-                      kvh * D + c * 64, b * p.seq_len + kt * kTileN);
+          tma_load_3d(slot_ptr(sidx) + c * Cfg::kRegion, &tq, &slot_full[sidx % NS], c * 64,
+                      it.kvh * g, it.b * Lq + it.l0);
+        ++sidx;
+        for (int j = 0; j < it.n; ++j) {
+          const int kt = static_cast<int>(static_cast<uint32_t>(it.list[j]) & kIndexMask);
+          const int krow = it.b * p.seq_len + kt * kTileN;
+          if (!acquire(sidx)) { ok = false; break; }
 #pragma unroll
-        for (int i = 0; i < SV; ++i)
-          if (i == st) last_v[i] = static_cast<int>(ph);
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tk, &slot_full[sidx % NS],
+                        it.kvh * D + c * 64, krow);
+          ++sidx;
+          if (!acquire(sidx)) { ok = false; break; }
+#pragma unroll
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tv, &slot_full[sidx % NS],
+                        it.kvh * D + c * 64, krow);
+          ++sidx;
+        }
       }
-      if (!ok) {
-#pragma unroll
-        for (int i = 0; i < SV; ++i)
-          if (last_v[i] >= 0) drain_wait(&v_full[i], last_v[i], 100000000ull);
+      if (!ok) {  // drain this CTA's copies still in flight
+        for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
+          drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      // ------------------------------------------------------ MMA issuer: S
-      // S_j = Q K_j^T into TMEM buffer j%2 (A = Q from TMEM); the buffer is
-      // reused for S_{j+2} once P_j V_j (which reads P_j from it) has
-      // completed.
+  } else if (warp == 1 || warp == 3) {
+    if (lane == 0) {
+      // ------------------------------------------------------ MMA issuers
+      // warp 1: S_t = Q K_t^T into TMEM buffer t & 1 (A = Q from TMEM); the
+      // buffer is reused for S_{t+2} once P_t V_t (which reads P_t from it)
+      // has completed.  warp 3: once the softmax has written P_t over S_t:
+      // O += P_t V_t with A = P_t from TMEM.  Two issuing threads keep the
+      // tensor pipe fed while the softmax warps keep the schedulers busy.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      uint64_t* last_commit = nullptr;
-      uint32_t last_parity = 0;
-      bool ok = mbar_wait(q_tmem, 0, ctl);
-      for (int j = 0; ok && j < n; ++j) {
-        const int st = j % SK;
-        const uint32_t ph = (j / SK) & 1;
-        const int sb = j & 1;
-        if (!mbar_wait(&k_full[st], ph, ctl)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * Cfg::kTileBytes);
-        const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16_ts(d_s, tmem + Cfg::kTmemQ + 8 * kk,
-                     sdesc_sw128(k_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024),
-                     idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[st]);
-        last_commit = &s_full[sb];
-        last_parity = (j >> 1) & 1;
-      }
-      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
-    }
-  } else if (warp == 3) {
-    if (lane == 0 && n > 0) {
-      // ----------------------------------------------------- MMA issuer: P V
-      // once the softmax has written P_j (fp16) over S_j: O += P_j V_j with
-      // A = P_j from TMEM.  A second issuing thread keeps this product queued
-      // while the S issuer waits.
       constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
-      for (int i = 0; ok && i < n; ++i) {
-        const int st = i % SV;
-        const uint32_t ph = (i / SV) & 1;
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, ctl)) { ok = false; break; }
-        if (!mbar_wait(&v_full[st], ph, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + st * Cfg::kTileBytes);
-        const uint32_t pb = tmem + ((i & 1) ? Cfg::kTmemS1 : Cfg::kTmemS0);
+      int sidx = 0, tbase = 0, ibase = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const FwdItem it = fwd_item(p, item);
+        if (it.n == 0) continue;
+        if (warp == 1) {
+          if (!mbar_wait(q_tmem, ibase & 1, ctl)) { ok = false; break; }
+          mbar_arrive(&slot_empty[sidx % NS]);  // Q is in TMEM: its slot goes back
+        }
+        for (int j = 0; j < it.n; ++j) {
+          const int t = tbase + j, sb = t & 1;
+          const int kidx = sidx + 1 + 2 * j, vidx = kidx + 1;
+          if (warp == 1) {
+            if (!mbar_wait(&slot_full[kidx % NS], (kidx / NS) & 1, ctl)) { ok = false; break; }
+            if (t >= 2 && !mbar_wait(&o_done[sb], ((t - 2) >> 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(slot_ptr(kidx));
+            const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
-          mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
-                     sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&o_done[i & 1]);
-        mma_commit(&v_empty[st]);
-        last_commit = &o_done[i & 1];
-        last_parity = (i >> 1) & 1;
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_f16_ts(d_s, tmem + Cfg::kTmemQ + 8 * kk,
+                         sdesc_sw128(k_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024),
+                         idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit(&s_full[sb]);
+            mma_commit(&slot_empty[kidx % NS]);
+            last_commit = &s_full[sb];
+            last_parity = (t >> 1) & 1;
+          } else {
+            if (!mbar_wait(&p_full[sb], (t >> 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&slot_full[vidx % NS], (vidx / NS) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(slot_ptr(vidx));
+            const uint32_t pb = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
+              mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
+                         sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&o_done[sb]);
+            mma_commit(&slot_empty[vidx % NS]);
+            last_commit = &o_done[sb];
+            last_parity = (t >> 1) & 1;
+          }
+        }
+        sidx += 1 + 2 * it.n;
+        tbase += it.n;
+        ++ibase;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
@@ -287,137 +269,192 @@ __global__ void __launch_bounds__(384, 1)
     const int r = (threadIdx.x - 128) & 127;
     const int w = (threadIdx.x - 128) >> 7;
     const int cw = 64 * w;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int wq = warp & 3;  // TMEM lane quarter: rows 32*wq .. 32*wq + 31
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int lg = 31 - __clz(g);
     const int pos = r >> lg, h = r & (g - 1);
-    const int qabs = s_qpos[pos], lo_r = s_lo[pos];
     const float sl2 = p.scale_log2;
-    // row maxima / sums exchange in the Q buffer, free once Q is in TMEM
-    float* xmax = reinterpret_cast<float*>(sQ);        // [2 tiles][2 warpgroups][128]
-    float* xsum = xmax + 2 * 2 * 128;                  // [2 warpgroups][128]
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t e_next = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
+    float* xmax = reinterpret_cast<float*>(smem + Cfg::kXchg);  // [2 tiles][2 warpgroups][128]
+    float* xsum = xmax + 2 * 2 * 128;                           // [2 items][2 warpgroups][128]
+    // O epilogue staging of this warp: 32 rows x 16 fp32, 16-byte chunks
+    // swizzled by row & 3
+    const uint32_t stage = smem_u32(smem + Cfg::kStage) + (warp - 4) * 2048;
     bool ok = true;
-    if (n > 0 && w == 0) {  // row r of Q into TMEM (bf16 pairs), the A operand of Q K^T
-      if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, ctl))) {
-        ok = false;
-      } else {
-        sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ);
-        tmem_wait_st();
-        warp_arrive(q_tmem);
-      }
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, ctl))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0) + cw;
-      float s[64];
-      {
-        uint32_t u[64];
-        tmem_ld32_nowait(sc, u);
-        tmem_ld32_nowait(sc + 32, u + 32);
-        tmem_wait_ld();
-        reg_fence32(u);
-        reg_fence32(u + 32);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
-      }
-      const uint32_t e = e_next;  // list entries run one tile ahead
-      if (j + 1 < n) e_next = static_cast<uint32_t>(list[j + 1]);
-      if (e & kPartialBit) {
-        const int k0 = static_cast<int>(e & kIndexMask) * kTileN + cw;
-        const int lo_c = lo_r - k0, hi_c = qabs - k0;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < lo_c || c > hi_c) s[c] = -INFINITY;
-      }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-      for (int c = 4; c < 64; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
-      }
-      float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      xmax[(sb * 2 + w) * 128 + r] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&mx_ready[sb]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&mx_ready[sb], (j >> 1) & 1, ctl))) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, xmax[(sb * 2 + (w ^ 1)) * 128 + r]);
-      const float mxl2 = mx * sl2;
-      const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m_run - m_ref);
-      // P enters the P V product in fp16 (11-bit significand) against an
-      // fp16 copy of V; its values lie in [0, 2^8] thanks to the lazy max.
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float e0 = ex2(fmaf(s[c], sl2, -m_ref));
-        const float e1 = ex2(fmaf(s[c + 1], sl2, -m_ref));
-        sum0 += e0;
-        sum1 += e1;
-        pk[c >> 1] = pack_f16(e0, e1);
-      }
-      l_run = l_run * alpha + (sum0 + sum1);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_st8_nowait(sc + 8 * q, pk + 8 * q);
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // the reference max moved: rescale this warpgroup's half of O once
-        // P_{j-1} V_{j-1} is in
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl))) {
+    int sidx = 0, tbase = 0, ibase = 0;
+    int copied = -1;  // item whose Q is already in TMEM
+    auto copy_q = [&](int q_idx) -> bool {  // warpgroup 0: row r of Q into TMEM
+      if (!__all_sync(0xffffffffu, mbar_wait(&slot_full[q_idx % NS], (q_idx / NS) & 1, ctl)))
+        return false;
+      sw128_row_to_tmem<D>(smem_u32(slot_ptr(q_idx)), r, tmem + lane_base + Cfg::kTmemQ);
+      tmem_wait_st();
+      warp_arrive(q_tmem);
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const FwdItem it = fwd_item(p, item);
+      if (it.n == 0) continue;
+      const int qabs = p.qpos[it.l0 + pos];
+      const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + it.l0 + pos];
+      if (w == 0 && copied != item && !copy_q(sidx)) { ok = false; break; }
+      float m_run = -INFINITY, l_run = 0.f;
+      uint32_t e_next = static_cast<uint32_t>(it.list[0]);
+      for (int j = 0; j < it.n; ++j) {
+        const int t = tbase + j, sb = t & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (t >> 1) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0) + cw;
+        float s[64];
+        {
+          uint32_t u[64];
+          tmem_ld32_nowait(sc, u);
+          tmem_ld32_nowait(sc + 32, u + 32);
+          tmem_wait_ld();
+          reg_fence32(u);
+          reg_fence32(u + 32);
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          float t[32];
-          const uint32_t oc = tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0;
-          tmem_ld32(oc, t);
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
+        }
+        const uint32_t e = e_next;  // list entries run one tile ahead
+        if (j + 1 < it.n) e_next = static_cast<uint32_t>(it.list[j + 1]);
+        if (e & kPartialBit) {
+          const int k0 = static_cast<int>(e & kIndexMask) * kTileN + cw;
+          const int lo_c = lo_r - k0, hi_c = qabs - k0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) t[i] *= alpha;
-          tmem_st32(oc, t);
+          for (int c = 0; c < 64; ++c)
+            if (c < lo_c || c > hi_c) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 64; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        xmax[(sb * 2 + w) * 128 + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mx_ready[sb]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&mx_ready[sb], (t >> 1) & 1, ctl))) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xmax[(sb * 2 + (w ^ 1)) * 128 + r]);
+        const float mxl2 = mx * sl2;
+        const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
+        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2(m_run - m_ref);
+        // P enters the P V product in fp16 (11-bit significand) against an
+        // fp16 copy of V; its values lie in [0, 2^8] thanks to the lazy max.
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float e0 = ex2(fmaf(s[c], sl2, -m_ref));
+          const float e1 = ex2(fmaf(s[c + 1], sl2, -m_ref));
+          sum0 += e0;
+          sum1 += e1;
+          pk[c >> 1] = pack_f16(e0, e1);
+        }
+        l_run = l_run * alpha + (sum0 + sum1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_st8_nowait(sc + 8 * q, pk + 8 * q);
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // the reference max moved: rescale this warpgroup's half of O
+          // once P_{t-1} V_{t-1} is in
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            float tt[32];
+            const uint32_t oc = tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0;
+            tmem_ld32(oc, tt);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) tt[i] *= alpha;
+            tmem_st32(oc, tt);
+          }
+        }
+        tmem_wait_st();
+        warp_arrive(&p_full[sb]);
+        m_run = m_new;
+      }
+      if (!ok) break;
+      // the last S of this item has been read: bring in the next item's Q
+      // now, so that its first S overlaps this epilogue
+      {
+        int nx = item + gridDim.x;
+        while (nx < n_items && fwd_item(p, nx).n == 0) nx += gridDim.x;
+        if (nx < n_items) {
+          if (w == 0 && !copy_q(sidx + 1 + 2 * it.n)) { ok = false; break; }
+          copied = nx;
         }
       }
-      tmem_wait_st();
-      warp_arrive(&p_full[sb]);
-      m_run = m_new;
-    }
-    if (ok && n > 0) {
-      xsum[w * 128 + r] = l_run;
+      // row sums: each warpgroup holds the sum over its half of the keys
+      float* xs = xsum + (ibase & 1) * 256;
+      xs[w * 128 + r] = l_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(l_ready);
-      ok = __all_sync(0xffffffffu, mbar_wait(l_ready, 0, ctl));
-    }
-    if (ok && n > 0 && __all_sync(0xffffffffu, mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, ctl))) {
+      const int t_last = tbase + it.n - 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
+          !__all_sync(0xffffffffu,
+                      mbar_wait(&o_done[t_last & 1], (t_last >> 1) & 1, ctl))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const float l_tot = xsum[r] + xsum[128 + r];
+      const float l_tot = xs[r] + xs[128 + r];
       const float inv = 1.f / l_tot;
-      const int hq = kvh * g + h;
-      const long long row = static_cast<long long>(b) * Lq + l0 + pos;
-      float4* dst = reinterpret_cast<float4*>(o + (row * p.n_heads + hq) * D + w * (D / 2));
+      // O / l for this warpgroup's half of head_dim, staged per warp and
+      // written with row-contiguous 64-byte runs
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 16) {
+        uint32_t u[16];
+        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0, u);
+        tmem_wait_ld();
+        reg_fence16(u);
+        const int rr = lane;  // row within this warp's quarter
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        float t[32];
-        tmem_ld32(tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0, t);
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(stage + rr * 64 + ((q4 ^ (rr & 3)) << 4),
+                       __float_as_uint(__uint_as_float(u[4 * q4]) * inv),
+                       __float_as_uint(__uint_as_float(u[4 * q4 + 1]) * inv),
+                       __float_as_uint(__uint_as_float(u[4 * q4 + 2]) * inv),
+                       __float_as_uint(__uint_as_float(u[4 * q4 + 3]) * inv));
+        __syncwarp();
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          dst[c0 / 4 + q4] = make_float4(t[4 * q4] * inv, t[4 * q4 + 1] * inv,
-                                         t[4 * q4 + 2] * inv, t[4 * q4 + 3] * inv);
+        for (int i = 0; i < 4; ++i) {
+          const int ci = lane + 32 * i;         // chunk: row ci / 4, part ci % 4
+          const int row = ci >> 2, part = ci & 3;
+          uint32_t a0, a1, a2, a3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                       : "r"(stage + row * 64 + ((part ^ (row & 3)) << 4)));
+          const int tr = 32 * wq + row;  // tile row
+          const long long grow = static_cast<long long>(it.b) * Lq + it.l0 + (tr >> lg);
+          float4* dst = reinterpret_cast<float4*>(
+              o + (grow * p.n_heads + it.kvh * g + (tr & (g - 1))) * D + w * (D / 2) + c0 +
+              4 * part);
+          *dst = make_float4(__uint_as_float(a0), __uint_as_float(a1), __uint_as_float(a2),
+                             __uint_as_float(a3));
+        }
+        __syncwarp();
       }
       if (w == 0)
-        lse[(static_cast<long long>(b) * p.n_heads + hq) * Lq + l0 + pos] =
+        lse[(static_cast<long long>(it.b) * p.n_heads + it.kvh * g + h) * Lq + it.l0 + pos] =
             (m_run + lg2(l_tot)) * 0.6931471805599453f;
+      // the next item's first P V overwrites O only after every softmax
+      // warp has arrived on p_full for it, i.e. after these reads
+      tc_fence_before();
+      sidx += 1 + 2 * it.n;
+      tbase += it.n;
+      ++ibase;
     }
   }
 
@@ -452,12 +489,14 @@ template <int D>
 cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv16, float* o, float* lse, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  const int grid = p.batch * p.n_qtiles * p.n_kv_heads;
-  if (grid == 0) return cudaSuccess;
+  const int items = p.batch * p.n_qtiles * p.n_kv_heads;
+  if (items == 0) return cudaSuccess;
+  // persistent: one CTA per SM (TMEM and shared memory allow no more)
+  const int grid = items < pl.num_sms ? items : pl.num_sms;
   const int smem = FwdCfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D><<<grid, 384, smem, s>>>(tq, tk, tv16, p, o, lse);
+  fwd_kernel<D><<<grid, 384, smem, s>>>(tq, tk, tv16, p, o, lse, items);
   return cudaGetLastError();
 }
 
