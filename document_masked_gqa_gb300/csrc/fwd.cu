@@ -46,10 +46,12 @@ struct FwdCfg {
   // one ring of tile-sized slots carries every load in stream order: per
   // work item Q, then K_j, V_j for each key tile j of its row list
   static constexpr int kSlots = (D == 128) ? 6 : 10;
-  static constexpr int kStage = kSlots * kTileBytes;  // O epilogue staging, 2 KB per softmax warp
-  static constexpr int kXchg = kStage + 8 * 2048;     // row maxima [2][2][128], row sums [2][2][128]
-  static constexpr int kBar = kXchg + (2 * 2 * 128 + 2 * 2 * 128) * 4;
-  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kStage = kSlots * kTileBytes;  // O epilogue staging, 2 KB per epilogue warp
+  // row maxima [2 tiles][2 warpgroups][128], then per item parity: row sums
+  // [2][2 warpgroups][128] and reference maxima [2][128]
+  static constexpr int kXchg = kStage + 4 * 2048;
+  static constexpr int kBar = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kSmemBytes = kEnd + 1024;
@@ -94,7 +96,7 @@ __device__ __forceinline__ FwdItem fwd_item(const PlanDev& p, int item) {
 // per-tile barrier parity follow from the global tile index t) and the
 // items so far (ibase: parity of q_tmem and l_ready).
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const PlanDev p,
                float* __restrict__ o, float* __restrict__ lse, int n_items) {
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* mx_ready = o_done + 2;     // [2] both softmax warpgroups posted a tile's row maxima
   uint64_t* l_ready = mx_ready + 2;    // both posted an item's partial row sums
   uint64_t* q_tmem = l_ready + 1;      // an item's Q copied into TMEM
+  uint64_t* o_free = q_tmem + 1;       // the epilogue warps have read an item's O
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTileBytes; };
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(l_ready, 8);
     mbar_init(q_tmem, 4);
+    mbar_init(o_free, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -237,6 +241,9 @@ __global__ void __launch_bounds__(384, 1)
             last_commit = &s_full[sb];
             last_parity = (t >> 1) & 1;
           } else {
+            // the item's first P V overwrites O: the previous item's O must
+            // have been read out by the epilogue warps
+            if (j == 0 && ibase > 0 && !mbar_wait(o_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
             if (!mbar_wait(&p_full[sb], (t >> 1) & 1, ctl)) { ok = false; break; }
             if (!mbar_wait(&slot_full[vidx % NS], (vidx / NS) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- softmax
     // two warpgroups; thread (r, w) owns row r and key columns [64w, 64w+64)
     // of every tile.  Per tile the two post their partial row maxima and
@@ -272,13 +279,11 @@ __global__ void __launch_bounds__(384, 1)
     const int wq = warp & 3;  // TMEM lane quarter: rows 32*wq .. 32*wq + 31
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int lg = 31 - __clz(g);
-    const int pos = r >> lg, h = r & (g - 1);
+    const int pos = r >> lg;
     const float sl2 = p.scale_log2;
     float* xmax = reinterpret_cast<float*>(smem + Cfg::kXchg);  // [2 tiles][2 warpgroups][128]
     float* xsum = xmax + 2 * 2 * 128;                           // [2 items][2 warpgroups][128]
-    // O epilogue staging of this warp: 32 rows x 16 fp32, 16-byte chunks
-    // swizzled by row & 3
-    const uint32_t stage = smem_u32(smem + Cfg::kStage) + (warp - 4) * 2048;
+    float* xm = xsum + 2 * 2 * 128;                             // [2 items][128]
     bool ok = true;
     int sidx = 0, tbase = 0, ibase = 0;
     int copied = -1;  // item whose Q is already in TMEM
@@ -396,11 +401,42 @@ __global__ void __launch_bounds__(384, 1)
           copied = nx;
         }
       }
-      // row sums: each warpgroup holds the sum over its half of the keys
-      float* xs = xsum + (ibase & 1) * 256;
-      xs[w * 128 + r] = l_run;
+      // post this item's row statistics for the epilogue warps: each
+      // warpgroup's partial row sum, and the reference max (the same in
+      // both).  Only once the epilogue has taken the previous item (its O
+      // released): l_ready then never runs two phases ahead of the epilogue,
+      // and the buffers of this parity (last read for item ibase - 2) are free.
+      if (ibase >= 1 && !__all_sync(0xffffffffu, mbar_wait(o_free, (ibase - 1) & 1, ctl))) {
+        ok = false;
+        break;
+      }
+      xsum[((ibase & 1) * 2 + w) * 128 + r] = l_run;
+      if (w == 0) xm[(ibase & 1) * 128 + r] = m_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(l_ready);
+      sidx += 1 + 2 * it.n;
+      tbase += it.n;
+      ++ibase;
+    }
+  } else if (warp >= 12) {
+    // --------------------------------------------------------------- epilogue
+    // per item: once its last P V is done and the softmax warps have posted
+    // the row statistics, read O out of TMEM (row r = lane of warp w - 12),
+    // hand the accumulator back, then write O / l and the LSE.  O is staged
+    // per warp (16 columns at a time) and written in row-contiguous 64-byte
+    // runs; this overlaps the next item's tiles.
+    const int wq = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int lg = 31 - __clz(g);
+    const int r = 32 * wq + lane;
+    const float* xsum = reinterpret_cast<const float*>(smem + Cfg::kXchg) + 2 * 2 * 128;
+    const float* xm = xsum + 2 * 2 * 128;
+    const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 2048;
+    bool ok = true;
+    int tbase = 0, ibase = 0;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const FwdItem it = fwd_item(p, item);
+      if (it.n == 0) continue;
       const int t_last = tbase + it.n - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
           !__all_sync(0xffffffffu,
@@ -409,28 +445,30 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      const float l_tot = xs[r] + xs[128 + r];
+      const float l_tot = xsum[((ibase & 1) * 2) * 128 + r] + xsum[((ibase & 1) * 2 + 1) * 128 + r];
+      const float m_ref = xm[(ibase & 1) * 128 + r];
       const float inv = 1.f / l_tot;
-      // O / l for this warpgroup's half of head_dim, staged per warp and
-      // written with row-contiguous 64-byte runs
-#pragma unroll 1
-      for (int c0 = 0; c0 < D / 2; c0 += 16) {
-        uint32_t u[16];
-        tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemO + w * (D / 2) + c0, u);
-        tmem_wait_ld();
-        reg_fence16(u);
-        const int rr = lane;  // row within this warp's quarter
+      uint32_t u[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32)
+        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemO + c0, u + c0);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) reg_fence32(u + c0);
+      warp_arrive(o_free);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(stage + rr * 64 + ((q4 ^ (rr & 3)) << 4),
-                       __float_as_uint(__uint_as_float(u[4 * q4]) * inv),
-                       __float_as_uint(__uint_as_float(u[4 * q4 + 1]) * inv),
-                       __float_as_uint(__uint_as_float(u[4 * q4 + 2]) * inv),
-                       __float_as_uint(__uint_as_float(u[4 * q4 + 3]) * inv));
+          st_shared_v4(stage + lane * 64 + ((q4 ^ (lane & 3)) << 4),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 1]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 2]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 3]) * inv));
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int ci = lane + 32 * i;         // chunk: row ci / 4, part ci % 4
+          const int ci = lane + 32 * i;  // chunk: row ci / 4, part ci % 4
           const int row = ci >> 2, part = ci & 3;
           uint32_t a0, a1, a2, a3;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -439,20 +477,14 @@ __global__ void __launch_bounds__(384, 1)
           const int tr = 32 * wq + row;  // tile row
           const long long grow = static_cast<long long>(it.b) * Lq + it.l0 + (tr >> lg);
           float4* dst = reinterpret_cast<float4*>(
-              o + (grow * p.n_heads + it.kvh * g + (tr & (g - 1))) * D + w * (D / 2) + c0 +
-              4 * part);
+              o + (grow * p.n_heads + it.kvh * g + (tr & (g - 1))) * D + c0 + 4 * part);
           *dst = make_float4(__uint_as_float(a0), __uint_as_float(a1), __uint_as_float(a2),
                              __uint_as_float(a3));
         }
         __syncwarp();
       }
-      if (w == 0)
-        lse[(static_cast<long long>(it.b) * p.n_heads + it.kvh * g + h) * Lq + it.l0 + pos] =
-            (m_run + lg2(l_tot)) * 0.6931471805599453f;
-      // the next item's first P V overwrites O only after every softmax
-      // warp has arrived on p_full for it, i.e. after these reads
-      tc_fence_before();
-      sidx += 1 + 2 * it.n;
+      lse[(static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (r & (g - 1))) * Lq + it.l0 +
+          (r >> lg)] = (m_ref + lg2(l_tot)) * 0.6931471805599453f;
       tbase += it.n;
       ++ibase;
     }
@@ -496,7 +528,7 @@ cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUte
   const int smem = FwdCfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D><<<grid, 384, smem, s>>>(tq, tk, tv16, p, o, lse, items);
+  fwd_kernel<D><<<grid, 512, smem, s>>>(tq, tk, tv16, p, o, lse, items);
   return cudaGetLastError();
 }
 
