@@ -121,6 +121,17 @@ dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p,
   return encode(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// dK / dV (fp32 [B*S][Hkv*D]) as TMA store targets: box = 32 columns x 32
+// key rows, 128-byte swizzled (one warp's block of the epilogue).
+dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim,
+                              static_cast<cuuint64_t>(p.batch) * p.seq_len};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim * 4};
+  const cuuint32_t box[2] = {32, 32};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 dma_status check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
@@ -259,7 +270,10 @@ dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16*
   if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, dk, dv,
+  CUtensorMap tdk, tdv;
+  if ((st = map_kv_out_f32(&tdk, dk, p)) != DMA_OK) return st;
+  if ((st = map_kv_out_f32(&tdv, dv, p)) != DMA_OK) return st;
+  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv,
                           static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;

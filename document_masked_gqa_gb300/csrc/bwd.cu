@@ -138,24 +138,50 @@ struct DkdvCfg {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;         // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;    // 2 stages
-  static constexpr int kCOL = kDO + 2 * kTile;  // [warpgroup][2][64 LSE*log2e, 64 Delta]
-  static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 18;
+  // dK / dV staging of the epilogue warps: per warp two 4 KB buffers of
+  // 32 rows x 32 fp32 in the 128-byte swizzled layout of a TMA store
+  static constexpr int kStage = kDO + 2 * kTile;
+  static constexpr int kCOL = kStage + 4 * 2 * 4096;  // [warpgroup][2][32 LSE*log2e, 32 Delta]
+  static constexpr int kBar = kCOL + 2 * 2 * 64 * 4;
+  static constexpr int kNumBars = 22;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
-  // TMEM: dV [0,128), dK [128,256); warpgroup h's buffer at 256 + 128h:
-  // S^T in its first 64 columns, dP^T in the next 64
+  // TMEM: dV [0,128), dK [128,256); buffer h at 256 + 128h: S^T in its
+  // first 64 columns, dP^T in the next 64
   static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemBuf = 256;
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
 
+// Work item `item` of the dK/dV pass: (sample, key tile) in longest-list-first
+// order times K/V head (the heads of one key tile side by side).
+struct DkdvItem {
+  int b, kvh, kt, n;
+  const int32_t* list;
+};
+__device__ __forceinline__ DkdvItem dkdv_item(const PlanDev& p, int item) {
+  DkdvItem it;
+  const int ord = item / p.n_kv_heads;
+  it.kvh = item % p.n_kv_heads;
+  const int bk = p.bwd_order[ord];
+  it.b = bk / p.n_ktiles;
+  it.kt = bk % p.n_ktiles;
+  const int cp0 = p.col_ptr[bk];
+  it.n = p.col_ptr[bk + 1] - cp0;
+  it.list = p.col_idx + cp0;
+  return it;
+}
+
+// Persistent: CTA c takes work items c, c + gridDim.x, ...  Every role keeps
+// the same counters across non-empty items: query tiles so far (tbase: the
+// Q / dO stage and the parity of every per-tile barrier) and items so far
+// (ibase: parity of kv_full, kv_empty, acc_done, acc_free).
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                const PlanDev p, const float* __restrict__ lse, float* __restrict__ dk,
-                float* __restrict__ dv) {
+                const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
+                const PlanDev p, const float* __restrict__ lse, int n_items) {
   using Cfg = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -169,15 +195,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = smem_raw + pad;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = p.n_kv_heads, g = p.group, P = p.tile_pos, Lq = p.local_len;
-  // longest column lists first; the K/V heads of one key tile run side by
-  // side (measured faster than a head-major order)
-  const int ord = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
-  const int bk = p.bwd_order[ord];
-  const int b = bk / p.n_ktiles, kt = bk % p.n_ktiles;
-  const int cp0 = p.col_ptr[bk];
-  const int n = p.col_ptr[bk + 1] - cp0;
-  const int32_t* list = p.col_idx + cp0;
+  const int g = p.group, P = p.tile_pos, Lq = p.local_len;
 
   uint8_t* sK = smem + Cfg::kK;
   uint8_t* sV = smem + Cfg::kV;
@@ -194,7 +212,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them (both warpgroups)
   uint64_t* buf_free = bars + 13;  // [2] dV, dK of that half step done
   uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
-  uint64_t* acc_done = bars + 17;  // every MMA done
+  uint64_t* acc_done = bars + 17;  // an item's dV, dK complete
+  uint64_t* kv_empty = bars + 18;  // an item's last S^T and dP^T done (two commits)
+  uint64_t* acc_free = bars + 19;  // the epilogue warps have read an item's dV, dK
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -211,6 +231,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&col_ready[i], 128);
     }
     mbar_init(acc_done, 1);
+    mbar_init(kv_empty, 2);
+    mbar_init(acc_free, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -223,131 +245,164 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-  const int krow0 = b * p.seq_len + kt * kTileN;
 
   if (warp == 0) {
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       // --------------------------------------- producer: K, V, then Q, dO
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tdo);
-      mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      int last_t = -1, ibase = 0, tbase = 0;
+      bool kv_pending = false, ok = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+        const DkdvItem it = dkdv_item(p, item);
+        if (it.n == 0) continue;
+        const int krow0 = it.b * p.seq_len + it.kt * kTileN;
+        kv_pending = false;
+        // K and V of the previous item are read until its last S^T / dP^T
+        if (ibase > 0 && !mbar_wait(kv_empty, (ibase - 1) & 1, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
 #pragma unroll
-      for (int c = 0; c < Cfg::kChunks; ++c) {
-        tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, kvh * D + c * 64, krow0);
-        tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, kvh * D + c * 64, krow0);
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, it.kvh * D + c * 64, krow0);
+          tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, it.kvh * D + c * 64, krow0);
+        }
+        kv_pending = true;
+        for (int i = 0; i < it.n; ++i) {
+          const int ig = tbase + i, st = ig & 1;
+          const uint32_t ph = (ig >> 1) & 1;
+          const int qt = static_cast<int>(static_cast<uint32_t>(it.list[i]) & kIndexMask);
+          if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
+#pragma unroll
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64,
+                        it.kvh * g, it.b * Lq + qt * P);
+          if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
+#pragma unroll
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
+                        it.kvh * g, it.b * Lq + qt * P);
+          last_t = ig;
+        }
+        tbase += it.n;
+        ++ibase;
       }
-      int last_q = -1, last_do = -1;
-      bool ok = true;
-      for (int i = 0; i < n; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        const int qt = static_cast<int>(static_cast<uint32_t>(list[i]) & kIndexMask);
-        if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
-#pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64, kvh * g,
-                      b * Lq + qt * P);
-        last_q = i;
-        if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
-#pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
-                      kvh * g, b * Lq + qt * P);
-        last_do = i;
-      }
-      if (!ok) {
-        drain_wait(kv_full, 0, 100000000ull);
-        for (int ii = max(0, last_q - 1); ii <= last_q; ++ii)
+      if (!ok) {  // drain this CTA's copies still in flight
+        if (kv_pending) drain_wait(kv_full, ibase & 1, 100000000ull);
+        for (int ii = max(0, last_t - 1); ii <= last_t; ++ii) {
           drain_wait(&q_full[ii & 1], (ii >> 1) & 1, 100000000ull);
-        for (int ii = max(0, last_do - 1); ii <= last_do; ++ii)
           drain_wait(&do_full[ii & 1], (ii >> 1) & 1, 100000000ull);
+        }
       }
     }
   } else if (warp == 1 || warp == 2) {
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       // ------------------------------- MMA issuers: S^T (warp 1), dP^T (warp 2)
-      // half step s = 2i + h (query tile i, rows 64h..64h+63): S^T = K Q_h^T
-      // and dP^T = V dO_h^T into buffer h, once dV / dK of half step s-2
-      // have read that buffer.  Each commits once to sdp_full[h].
+      // half step (tile i, h): S^T = K Q_h^T and dP^T = V dO_h^T into buffer
+      // h, once dV / dK of the previous tile's half h have read that buffer.
+      // Each commits once to sdp_full[h], and once to kv_empty per item.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
       const bool is_s = warp == 1;
       const uint32_t a_addr = smem_u32(is_s ? sK : sV);
       uint8_t* b_tiles = is_s ? sQ : sDO;
       uint64_t* b_full = is_s ? q_full : do_full;
       const uint32_t d_off = is_s ? 0u : 64u;
-      const int steps = 2 * n;
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
-      bool ok = mbar_wait(kv_full, 0, ctl);
-      for (int s = 0; ok && s < steps; ++s) {
-        const int i = s >> 1, h = s & 1, st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (s >= 2 && !mbar_wait(&buf_free[h], (i - 1) & 1, ctl)) { ok = false; break; }
-        if (!mbar_wait(&b_full[st], ph, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + Cfg::kTmemBuf + 128 * h + d_off;
-        const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile) + h * 8192;
+      bool ok = true;
+      int tbase = 0, ibase = 0;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+        const DkdvItem it = dkdv_item(p, item);
+        if (it.n == 0) continue;
+        if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
+        for (int s = 0; s < 2 * it.n; ++s) {
+          const int ig = tbase + (s >> 1), h = s & 1, st = ig & 1;
+          const uint32_t ph = (ig >> 1) & 1;
+          if (ig >= 1 && !mbar_wait(&buf_free[h], (ig - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&b_full[st], ph, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + Cfg::kTmemBuf + 128 * h + d_off;
+          const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile) + h * 8192;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-          mma_bf16_ss(d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+            mma_bf16_ss(d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&sdp_full[h]);
+          last_commit = &sdp_full[h];
+          last_parity = ig & 1;
         }
-        mma_commit(&sdp_full[h]);
-        last_commit = &sdp_full[h];
-        last_parity = i & 1;
+        if (!ok) break;
+        mma_commit(kv_empty);  // this item's K / V reads are done once these complete
+        tbase += it.n;
+        ++ibase;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp == 3) {
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       // -------------------------------------------------- MMA issuer: dV, dK
       // once both warpgroups have written P^T, dS^T over buffer h:
-      // dV += P^T dO_h, dK += dS^T Q_h (A operands from TMEM).  A second
-      // issuing thread keeps these queued behind the S^T / dP^T products
-      // instead of waiting for them.
+      // dV += P^T dO_h, dK += dS^T Q_h (A operands from TMEM).  A separate
+      // issuing thread keeps these queued behind the S^T / dP^T products.
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const int steps = 2 * n;
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
-      for (int s = 0; ok && s < steps; ++s) {
-        const int i = s >> 1, h = s & 1, st = i & 1;
-        const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
-        if (!mbar_wait(&pds_full[h], i & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
-        const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
-        // warpgroup w left its 32 query columns of P^T at buf + 32w (16
-        // packed columns) and of dS^T at buf + 64 + 32w
+      int tbase = 0, ibase = 0;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+        const DkdvItem it = dkdv_item(p, item);
+        if (it.n == 0) continue;
+        for (int s = 0; s < 2 * it.n; ++s) {
+          const int ig = tbase + (s >> 1), h = s & 1, st = ig & 1;
+          const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
+          if (!mbar_wait(&pds_full[h], ig & 1, ctl)) { ok = false; break; }
+          // the item's first products overwrite dV, dK: the previous item's
+          // must have been read out by the epilogue warps
+          if (s == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
+          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
+          // warpgroup w left its 32 query columns of P^T at buf + 32w (16
+          // packed columns) and of dS^T at buf + 64 + 32w
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h; K = the half's 64 rows
-          mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk + (kk >= 2 ? 16 : 0),
-                     sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                     (s > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h; K = the half's 64 rows
+            mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk + (kk >= 2 ? 16 : 0),
+                       sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                       (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
-          mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk + (kk >= 2 ? 16 : 0),
-                     sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                     (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&buf_free[h]);
-        last_commit = &buf_free[h];
-        last_parity = i & 1;
-        if (h == 1) {
-          mma_commit(&do_empty[st]);
-          mma_commit(&q_empty[st]);
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
+            mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk + (kk >= 2 ? 16 : 0),
+                       sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                       (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&buf_free[h]);
+          last_commit = &buf_free[h];
+          last_parity = ig & 1;
+          if (h == 1) {
+            mma_commit(&do_empty[st]);
+            mma_commit(&q_empty[st]);
+          }
         }
-      }
-      if (ok) {
+        if (!ok) break;
         mma_commit(acc_done);
         last_commit = acc_done;
-        last_parity = 0;
+        last_parity = ibase & 1;
+        tbase += it.n;
+        ++ibase;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 12) {
     // ----------------------------------------------------------- key rows
     // thread r of warpgroup w owns key r and, in every half step, the 32
     // query columns [32w, 32w + 32) of that half
@@ -355,109 +410,158 @@ __global__ void __launch_bounds__(384, 1)
     const int r = t & 127, w = t >> 7;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
-    const int key = kt * kTileN + r;  // position within the sample
     const float sl2 = p.scale_log2;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
-    // queries that may attend this key: positions [key, doc_end)
-    const int doc_end = p.doc_hi[static_cast<long long>(b) * p.seq_len + key];
     // statistics of this warpgroup's columns: thread r < 32 stages LSE of
     // column 32w + r, thread 32 <= r < 64 Delta of column 32w + r - 32
     const int qsub = 32 * w + (r & 31);
     const bool stager = r < 64;
     const float* stat_src = (r < 32) ? lse : p.delta;
     const float stat_mul = (r < 32) ? kLog2e : 1.f;
-    auto stat_row = [&](int hh) -> long long {
-      const int qrow = 64 * hh + qsub;
-      return (static_cast<long long>(b) * p.n_heads + kvh * g + (qrow & (g - 1))) * Lq +
-             (qrow >> lg);
-    };
-    const long long stat_base0 = stat_row(0), stat_base1 = stat_row(1);
-    float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
-    const int steps = 2 * n;
-    // list entries of this tile (e) and the next (e_nx), loaded a tile ahead
-    uint32_t e = n > 0 ? static_cast<uint32_t>(list[0]) : 0u;
-    uint32_t e_nx = n > 1 ? static_cast<uint32_t>(list[1]) : 0u;
-    float nxt = (n > 0 && stager) ? stat_src[stat_base0 + static_cast<int>(e & kIndexMask) * P] : 0.f;
+    float* col = sCOL + w * 128;  // [2 stages][64] floats per warpgroup
     bool ok = true;
-    for (int s = 0; s < steps; ++s) {
-      const int i = s >> 1, h = s & 1;
-      if (s > 0 && h == 0) {
-        e = e_nx;
-        if (i + 1 < n) e_nx = static_cast<uint32_t>(list[i + 1]);
-      }
-      {
-        // stage this step's statistics, fetch the next step's
-        const float cur = nxt;
-        if (stager && s + 1 < steps) {
-          const int s1 = s + 1;
-          const uint32_t e1 = (s1 & 1) ? e : e_nx;
-          nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
+    int tbase = 0;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      const DkdvItem it = dkdv_item(p, item);
+      if (it.n == 0) continue;
+      const int key = it.kt * kTileN + r;  // position within the sample
+      // queries that may attend this key: positions [key, doc_end)
+      const int doc_end = p.doc_hi[static_cast<long long>(it.b) * p.seq_len + key];
+      auto stat_row = [&](int hh) -> long long {
+        const int qrow = 64 * hh + qsub;
+        return (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (qrow & (g - 1))) * Lq +
+               (qrow >> lg);
+      };
+      const long long stat_base0 = stat_row(0), stat_base1 = stat_row(1);
+      const int steps = 2 * it.n;
+      // list entries of this tile (e) and the next (e_nx), loaded a tile ahead
+      uint32_t e = static_cast<uint32_t>(it.list[0]);
+      uint32_t e_nx = it.n > 1 ? static_cast<uint32_t>(it.list[1]) : 0u;
+      float nxt = stager ? stat_src[stat_base0 + static_cast<int>(e & kIndexMask) * P] : 0.f;
+      for (int s = 0; s < steps; ++s) {
+        const int i = s >> 1, h = s & 1, ig = tbase + i;
+        if (s > 0 && h == 0) {
+          e = e_nx;
+          if (i + 1 < it.n) e_nx = static_cast<uint32_t>(it.list[i + 1]);
         }
-        if (stager) col[(s & 1) * 128 + r] = cur * stat_mul;
-        mbar_arrive(&col_ready[w]);
-        if (!warp_wait(&col_ready[w], s & 1, ctl)) { ok = false; break; }
+        {
+          // stage this step's statistics, fetch the next step's
+          const float cur = nxt;
+          if (stager && s + 1 < steps) {
+            const int s1 = s + 1;
+            const uint32_t e1 = (s1 & 1) ? e : e_nx;
+            nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
+          }
+          if (stager) col[(s & 1) * 64 + r] = cur * stat_mul;
+          mbar_arrive(&col_ready[w]);
+          if (!warp_wait(&col_ready[w], s & 1, ctl)) { ok = false; break; }
+        }
+        // allowed query positions of this key in the tile: [key, doc_end);
+        // in this warpgroup's columns of half h: [lo_c, hi_c)
+        int lo_c = 0, hi_c = 32;
+        if (e & kPartialBit) {
+          const int l0 = static_cast<int>(e & kIndexMask) * P;
+          const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
+          lo_c = (max(0, key - q0) << lg) - 64 * h - 32 * w;
+          hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h - 32 * w;
+        }
+        const float4* lse_c = reinterpret_cast<const float4*>(col + (s & 1) * 64);
+        const float4* del_c = reinterpret_cast<const float4*>(col + (s & 1) * 64 + 32);
+        const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
+        if (!warp_wait(&sdp_full[h], ig & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t su[32], du[32];
+          tmem_ld32_nowait(buf + 32 * w, su);
+          tmem_ld32_nowait(buf + 64 + 32 * w, du);
+          tmem_wait_ld();
+          reg_fence32(su);
+          reg_fence32(du);
+          uint32_t pk[16], pd[16];
+          if (e & kPartialBit)
+            p_ds_chunk32<true>(su, du, lse_c, del_c, range_bits(lo_c, hi_c), sl2, pk, pd);
+          else
+            p_ds_chunk32<false>(su, du, lse_c, del_c, 0u, sl2, pk, pd);
+          // P^T and dS^T of these 32 columns over the first 16 columns read
+          tmem_st8_nowait(buf + 32 * w, pk);
+          tmem_st8_nowait(buf + 32 * w + 8, pk + 8);
+          tmem_st8_nowait(buf + 64 + 32 * w, pd);
+          tmem_st8_nowait(buf + 64 + 32 * w + 8, pd + 8);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&pds_full[h]);
       }
-      // allowed query positions of this key in the tile: [key, doc_end);
-      // in this warpgroup's columns of half h: [lo_c, hi_c)
-      int lo_c = 0, hi_c = 32;
-      if (e & kPartialBit) {
-        const int l0 = static_cast<int>(e & kIndexMask) * P;
-        const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
-        lo_c = (max(0, key - q0) << lg) - 64 * h - 32 * w;
-        hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h - 32 * w;
-      }
-      const float4* lse_c = reinterpret_cast<const float4*>(col + (s & 1) * 128);
-      const float4* del_c = reinterpret_cast<const float4*>(col + (s & 1) * 128 + 32);
-      const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
-      if (!warp_wait(&sdp_full[h], i & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t su[32], du[32];
-        tmem_ld32_nowait(buf + 32 * w, su);
-        tmem_ld32_nowait(buf + 64 + 32 * w, du);
-        tmem_wait_ld();
-        reg_fence32(su);
-        reg_fence32(du);
-        uint32_t pk[16], pd[16];
-        if (e & kPartialBit)
-          p_ds_chunk32<true>(su, du, lse_c, del_c, range_bits(lo_c, hi_c), sl2, pk, pd);
-        else
-          p_ds_chunk32<false>(su, du, lse_c, del_c, 0u, sl2, pk, pd);
-        // P^T and dS^T of these 32 columns over the first 16 columns read
-        tmem_st8_nowait(buf + 32 * w, pk);
-        tmem_st8_nowait(buf + 32 * w + 8, pk + 8);
-        tmem_st8_nowait(buf + 64 + 32 * w, pd);
-        tmem_st8_nowait(buf + 64 + 32 * w + 8, pd + 8);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&pds_full[h]);
+      tbase += it.n;
     }
-    // warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
-    const int h = w;
-    const long long out_row = (static_cast<long long>(krow0) + r) * p.n_kv_heads + kvh;
-    float4* dst = reinterpret_cast<float4*>((h ? dk : dv) + out_row * D);
-    if (n == 0) {
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int q = 0; q < D / 4; ++q) dst[q] = z;
-    } else if (ok && warp_wait(acc_done, 0, ctl)) {
-      tc_fence_after();
-      const float sc = h ? p.scale : 1.f;
-      const uint32_t acc = tmem + lane_base + (h ? Cfg::kTmemDK : Cfg::kTmemDV);
+  } else {
+    // --------------------------------------------------------------- epilogue
+    // warp w - 12 owns key rows 32 (w - 12) .. + 31 of each item: once its dV
+    // and dK are complete it reads them out of TMEM 32 columns at a time,
+    // stages each block (scaled, fp32, 128-byte swizzled rows) and writes it
+    // with its own TMA store; the accumulators are handed back after the
+    // last read.  Items without queries get zero rows the same way.
+    const int wq = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t stage0 = smem_u32(smem + Cfg::kStage) + wq * 8192;
+    bool ok = true;
+    int ibase = 0, round = 0;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      const DkdvItem it = dkdv_item(p, item);
+      const int row0 = it.b * p.seq_len + it.kt * kTileN + 32 * wq;
+      const bool empty = it.n == 0;
+      if (!empty) {
+        if (!warp_wait(acc_done, ibase & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+      }
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t tt[16];
-        tmem_ld16_nowait(acc + c0, tt);
-        tmem_wait_ld();
-        reg_fence16(tt);
+      for (int blk = 0; blk < 2 * (D / 32); ++blk) {
+        const bool is_dk = blk >= D / 32;
+        const int c0 = (blk % (D / 32)) * 32;
+        uint32_t u[32];
+        if (!empty) {
+          tmem_ld32_nowait(tmem + lane_base + (is_dk ? Cfg::kTmemDK : Cfg::kTmemDV) + c0, u);
+          tmem_wait_ld();
+          reg_fence32(u);
+          if (blk == 2 * (D / 32) - 1) warp_arrive(acc_free);
+        } else {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          dst[c0 / 4 + q4] = make_float4(
-              __uint_as_float(tt[4 * q4]) * sc, __uint_as_float(tt[4 * q4 + 1]) * sc,
-              __uint_as_float(tt[4 * q4 + 2]) * sc, __uint_as_float(tt[4 * q4 + 3]) * sc);
+          for (int c = 0; c < 32; ++c) u[c] = 0u;
+        }
+        const float sc = is_dk ? p.scale : 1.f;
+        // this buffer was last stored two rounds ago: wait until that store
+        // has read it
+        if (lane == 0 && round >= 2) {
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        }
+        __syncwarp();
+        const uint32_t stg = stage0 + (round & 1) * 4096;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                       __float_as_uint(__uint_as_float(u[4 * ch]) * sc),
+                       __float_as_uint(__uint_as_float(u[4 * ch + 1]) * sc),
+                       __float_as_uint(__uint_as_float(u[4 * ch + 2]) * sc),
+                       __float_as_uint(__uint_as_float(u[4 * ch + 3]) * sc));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile(
+              "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                  reinterpret_cast<uint64_t>(is_dk ? &tdk : &tdv)),
+              "r"(stg), "r"(it.kvh * D + c0), "r"(row0)
+              : "memory");
+          bulk_commit();
+        }
+        ++round;
       }
+      if (!empty) ++ibase;
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -596,7 +700,9 @@ __global__ void __launch_bounds__(640, 1)
         mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTile);
         return true;
       };
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
         const DqItem it = dq_item(p, item);
         if (it.n == 0) continue;
         const int qrow = it.b * Lq + it.l0;
@@ -649,7 +755,9 @@ __global__ void __launch_bounds__(640, 1)
       uint32_t last_parity = 0;
       bool ok = true;
       int sidx = 0, tbase = 0, ibase = 0;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
         const DqItem it = dq_item(p, item);
         if (it.n == 0) continue;
         if (warp == 1 || warp == 2) {
@@ -750,7 +858,9 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     int sidx = 0, tbase = 0, ibase = 0;
     int copied = -1;  // item whose Q / dO are already in TMEM
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
       const DqItem it = dq_item(p, item);
       const int l = it.l0 + pos;
       const int hq = it.kvh * g + h;
@@ -853,8 +963,14 @@ __global__ void __launch_bounds__(640, 1)
       // non-empty item's Q and dO now, so that its first products overlap
       // this epilogue
       {
-        int nx = item + gridDim.x;
-        while (nx < n_items && dq_item(p, nx).n == 0) nx += gridDim.x;
+        int nx = n_items;
+        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
+          const int cand = snake_item(kx);
+          if (cand < n_items && dq_item(p, cand).n != 0) {
+            nx = cand;
+            break;
+          }
+        }
         if (nx < n_items) {
           if (q < 2 && !copy_qdo(sidx + 2 + 2 * it.n)) { ok = false; break; }
           copied = nx;
@@ -922,14 +1038,16 @@ cudaError_t launch_delta_d(const dma_plan_s& pl, const float* o, const dma_bf16*
 template <int D>
 cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                          float* dk, float* dv, cudaStream_t s) {
+                          const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  const int grid = p.batch * p.n_ktiles * p.n_kv_heads;
-  if (grid == 0) return cudaSuccess;
+  const int items = p.batch * p.n_ktiles * p.n_kv_heads;
+  if (items == 0) return cudaSuccess;
+  // persistent: one CTA per SM (TMEM and shared memory allow no more)
+  const int grid = items < pl.num_sms ? items : pl.num_sms;
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DkdvCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<grid, 384, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, p, lse, dk, dv);
+  dkdv_kernel<D><<<grid, 512, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, p, lse, items);
   return cudaGetLastError();
 }
 
@@ -960,9 +1078,9 @@ cudaError_t launch_delta(const dma_plan_s& pl, const float* o, const dma_bf16* d
 
 cudaError_t launch_dkdv(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        float* dk, float* dv, cudaStream_t s) {
-  return pl.d.head_dim == 128 ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, dk, dv, s)
-                              : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, dk, dv, s);
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s)
+                              : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s);
 }
 
 cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,

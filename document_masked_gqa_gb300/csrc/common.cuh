@@ -57,6 +57,16 @@ struct dma_plan_s {
 
 namespace dma {
 // Launchers implemented in the .cu files (host side).
+#ifdef __CUDACC__
+// Work item of round k for this CTA of a persistent kernel: rounds alternate
+// direction over the CTAs, so that a longest-first item order spreads its
+// work evenly (CTA c takes c, 2G-1-c, 2G+c, ...).
+__device__ __forceinline__ int snake_item(int k) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+#endif
+
 cudaError_t launch_plan_kernels(const dma_plan_s& p, cudaStream_t s);
 cudaError_t launch_cp_copy(const dma_plan_s& p, const void* src, void* dst, size_t row_bytes,
                            bool gather, cudaStream_t s);
@@ -67,7 +77,7 @@ cudaError_t launch_delta(const dma_plan_s& p, const float* o, const dma_bf16* do
                          cudaStream_t s);
 cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        float* dk, float* dv, cudaStream_t s);
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s);
 cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s);

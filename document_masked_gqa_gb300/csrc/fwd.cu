@@ -170,7 +170,9 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTileBytes);
         return true;
       };
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
         const FwdItem it = fwd_item(p, item);
         if (it.n == 0) continue;
         if (!acquire(sidx)) { ok = false; break; }
@@ -215,7 +217,9 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t last_parity = 0;
       bool ok = true;
       int sidx = 0, tbase = 0, ibase = 0;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
         const FwdItem it = fwd_item(p, item);
         if (it.n == 0) continue;
         if (warp == 1) {
@@ -295,7 +299,9 @@ __global__ void __launch_bounds__(512, 1)
       warp_arrive(q_tmem);
       return true;
     };
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
       const FwdItem it = fwd_item(p, item);
       if (it.n == 0) continue;
       const int qabs = p.qpos[it.l0 + pos];
@@ -394,8 +400,14 @@ __global__ void __launch_bounds__(512, 1)
       // the last S of this item has been read: bring in the next item's Q
       // now, so that its first S overlaps this epilogue
       {
-        int nx = item + gridDim.x;
-        while (nx < n_items && fwd_item(p, nx).n == 0) nx += gridDim.x;
+        int nx = n_items;
+        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
+          const int cand = snake_item(kx);
+          if (cand < n_items && fwd_item(p, cand).n != 0) {
+            nx = cand;
+            break;
+          }
+        }
         if (nx < n_items) {
           if (w == 0 && !copy_q(sidx + 1 + 2 * it.n)) { ok = false; break; }
           copied = nx;
@@ -434,7 +446,9 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 2048;
     bool ok = true;
     int tbase = 0, ibase = 0;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
       const FwdItem it = fwd_item(p, item);
       if (it.n == 0) continue;
       const int t_last = tbase + it.n - 1;
