@@ -95,30 +95,50 @@ __global__ void delta_kernel(const float* __restrict__ o, const __nv_bfloat16* _
 
 // 32 columns of one key row: P = exp2(S * scale*log2e - LSE*log2e) (zero where
 // the mask bit is clear when kMasked), dS = P (dP - Delta), both packed bf16.
+// nlse_c holds -LSE*log2e per column, del_c Delta; pairs of columns go
+// through the packed fp32x2 forms.
 template <bool kMasked>
 __device__ __forceinline__ void p_ds_chunk32(const uint32_t* su, const uint32_t* du,
-                                             const float4* lse_c, const float4* del_c,
+                                             const float4* nlse_c, const float4* del_c,
                                              uint32_t allow, float sl2, uint32_t* pk,
                                              uint32_t* pd) {
+  const uint64_t sl2x2 = f2(sl2, sl2);
 #pragma unroll
   for (int q = 0; q < 32; q += 4) {
-    const float4 l4 = lse_c[q >> 2];
+    const float4 l4 = nlse_c[q >> 2];
     const float4 d4 = del_c[q >> 2];
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-    const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-    float pv[4], dv4[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pv[u] = ex2(fmaf(__uint_as_float(su[q + u]), sl2, -lv[u]));
-      if (kMasked && !((allow >> (q + u)) & 1u)) pv[u] = 0.f;
-      dv4[u] = pv[u] * (__uint_as_float(du[q + u]) - dl[u]);
+    float pv[4];
+    {
+      float x0, x1, x2, x3;
+      f2_split(f2_fma(f2(__uint_as_float(su[q]), __uint_as_float(su[q + 1])), sl2x2, f2(l4.x, l4.y)),
+               x0, x1);
+      f2_split(f2_fma(f2(__uint_as_float(su[q + 2]), __uint_as_float(su[q + 3])), sl2x2,
+                      f2(l4.z, l4.w)),
+               x2, x3);
+      pv[0] = ex2(x0);
+      pv[1] = ex2(x1);
+      pv[2] = ex2(x2);
+      pv[3] = ex2(x3);
     }
+    if (kMasked) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (!((allow >> (q + u)) & 1u)) pv[u] = 0.f;
+    }
+    float d0, d1, d2, d3;
+    f2_split(f2_mul(f2(pv[0], pv[1]), f2_sub(f2(__uint_as_float(du[q]), __uint_as_float(du[q + 1])),
+                                             f2(d4.x, d4.y))),
+             d0, d1);
+    f2_split(f2_mul(f2(pv[2], pv[3]),
+                    f2_sub(f2(__uint_as_float(du[q + 2]), __uint_as_float(du[q + 3])), f2(d4.z, d4.w))),
+             d2, d3);
     pk[q >> 1] = pack_bf16(pv[0], pv[1]);
     pk[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-    pd[q >> 1] = pack_bf16(dv4[0], dv4[1]);
-    pd[(q >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
+    pd[q >> 1] = pack_bf16(d0, d1);
+    pd[(q >> 1) + 1] = pack_bf16(d2, d3);
   }
 }
+
 //
 // Work is done in half steps: half h of query tile i is its rows
 // [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads).  The two
@@ -417,7 +437,7 @@ __global__ void __launch_bounds__(512, 1)
     const int qsub = 32 * w + (r & 31);
     const bool stager = r < 64;
     const float* stat_src = (r < 32) ? lse : p.delta;
-    const float stat_mul = (r < 32) ? kLog2e : 1.f;
+    const float stat_mul = (r < 32) ? -kLog2e : 1.f;  // staged: -LSE*log2e, Delta
     float* col = sCOL + w * 128;  // [2 stages][64] floats per warpgroup
     bool ok = true;
     int tbase = 0;

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&slot_full[i], 1);
       mbar_init(&slot_empty[i], 1);
     }
-    // the softmax warps arrive once per warp (8 warps; 4 of them copy Q)
+    // the softmax warps arrive once per warp (8 warps; both warpgroups copy half of Q)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&mx_ready[i], 8);
     }
     mbar_init(l_ready, 8);
-    mbar_init(q_tmem, 4);
+    mbar_init(q_tmem, 8);
     mbar_init(o_free, 4);
     *abort_flag = 0;
     fence_barrier_init();
@@ -291,10 +291,10 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     int sidx = 0, tbase = 0, ibase = 0;
     int copied = -1;  // item whose Q is already in TMEM
-    auto copy_q = [&](int q_idx) -> bool {  // warpgroup 0: row r of Q into TMEM
+    auto copy_q = [&](int q_idx) -> bool {  // warpgroup w: half w of row r of Q into TMEM
       if (!__all_sync(0xffffffffu, mbar_wait(&slot_full[q_idx % NS], (q_idx / NS) & 1, ctl)))
         return false;
-      sw128_row_to_tmem<D>(smem_u32(slot_ptr(q_idx)), r, tmem + lane_base + Cfg::kTmemQ);
+      sw128_row_to_tmem_half<D>(smem_u32(slot_ptr(q_idx)), r, tmem + lane_base + Cfg::kTmemQ, w);
       tmem_wait_st();
       warp_arrive(q_tmem);
       return true;
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(512, 1)
       if (it.n == 0) continue;
       const int qabs = p.qpos[it.l0 + pos];
       const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + it.l0 + pos];
-      if (w == 0 && copied != item && !copy_q(sidx)) { ok = false; break; }
+      if (copied != item && !copy_q(sidx)) { ok = false; break; }
       float m_run = -INFINITY, l_run = 0.f;
       uint32_t e_next = static_cast<uint32_t>(it.list[0]);
       for (int j = 0; j < it.n; ++j) {
@@ -360,17 +360,23 @@ __global__ void __launch_bounds__(512, 1)
         const float alpha = ex2(m_run - m_ref);
         // P enters the P V product in fp16 (11-bit significand) against an
         // fp16 copy of V; its values lie in [0, 2^8] thanks to the lazy max.
-        float sum0 = 0.f, sum1 = 0.f;
+        // exponent arguments and row sums in packed fp32 pairs
+        const uint64_t sl2x2 = f2(sl2, sl2), nm2 = f2(-m_ref, -m_ref);
+        uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float e0 = ex2(fmaf(s[c], sl2, -m_ref));
-          const float e1 = ex2(fmaf(s[c + 1], sl2, -m_ref));
-          sum0 += e0;
-          sum1 += e1;
+          float x0, x1;
+          f2_split(f2_fma(f2(s[c], s[c + 1]), sl2x2, nm2), x0, x1);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          if (c & 2) acc1 = f2_add(acc1, f2(e0, e1));
+          else acc0 = f2_add(acc0, f2(e0, e1));
           pk[c >> 1] = pack_f16(e0, e1);
         }
-        l_run = l_run * alpha + (sum0 + sum1);
+        float sa, sb2, sc2, sd;
+        f2_split(acc0, sa, sb2);
+        f2_split(acc1, sc2, sd);
+        l_run = l_run * alpha + ((sa + sb2) + (sc2 + sd));
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_st8_nowait(sc + 8 * q, pk + 8 * q);
         if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         if (nx < n_items) {
-          if (w == 0 && !copy_q(sidx + 1 + 2 * it.n)) { ok = false; break; }
+          if (!copy_q(sidx + 1 + 2 * it.n)) { ok = false; break; }
           copied = nx;
         }
       }

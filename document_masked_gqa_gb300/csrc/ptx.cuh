@@ -337,6 +337,30 @@ __device__ __forceinline__ void sw128_row_to_tmem(uint32_t tile, int r, uint32_t
   }
 }
 
+// Half `half` (0 or 1) of the same copy: 16-byte chunk pairs
+// [half * D/32, (half + 1) * D/32) of the row, so that two warpgroups can
+// share it.
+template <int D>
+__device__ __forceinline__ void sw128_row_to_tmem_half(uint32_t tile, int r, uint32_t taddr,
+                                                       int half) {
+  constexpr int kPairs = (D / 64) * 4;
+#pragma unroll
+  for (int i = 0; i < kPairs / 2; ++i) {
+    const int pi = half * (kPairs / 2) + i;
+    const int c = pi >> 2, k = 2 * (pi & 3);
+    uint32_t w[8];
+    const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
+    const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(a0));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "r"(a1));
+    tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
+  }
+}
+
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 at bit 46, swizzle
 // mode at bits 61-63 (2 = 128-byte swizzle).  Tiles are 1024-byte aligned,
@@ -386,6 +410,11 @@ __device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
