@@ -12,19 +12,20 @@
 //
 // Three launches:
 //   delta_kernel  Delta[b, h, l] = sum_d dO * O (HBM-bound, one pass).
-//   dkdv_kernel   one CTA per (key tile, K/V head): K and V stay in shared
-//                 memory; the CTA walks the column list of query tiles (all g
-//                 heads of the group packed in each 128-row tile, so the GQA
-//                 reduction over the group happens inside the accumulation),
-//                 each split in two 64-row halves handled by two ping-ponging
-//                 warpgroups; dV, dK accumulate in TMEM.
-//   dq_kernel     one CTA per (query tile, K/V head): Q and dO stay in shared
-//                 memory; the CTA walks the row list of key tiles.  TMEM: S,
-//                 dP and the dQ accumulator.  Warps 4-7 and 8-11: thread r of
-//                 each owns query row r, split over the key columns 0-63 and
-//                 64-127 of each key tile.
-// Both attention kernels: warps 0 and 2 = TMA producers, warp 1 = tcgen05
-// issuer, the rest = element-wise work, bounded waits everywhere.
+//   dkdv_kernel   work item = (key tile, K/V head): K and V stay in shared
+//                 memory; the item walks the column list of query tiles (all
+//                 g heads of the group packed in each 128-row tile, so the
+//                 GQA reduction over the group happens inside the
+//                 accumulation), each done in two 64-row half steps shared by
+//                 two element-wise warpgroups; dV, dK accumulate in TMEM.
+//   dq_kernel     work item = (query tile, K/V head): Q and dO are copied into
+//                 TMEM; the item walks the row list of key tiles; S, dP and
+//                 the dQ accumulator in TMEM; four row warpgroups split each
+//                 tile's key columns.
+// Both attention kernels are persistent (one CTA per SM) with one TMA
+// producer thread, one tcgen05-issuing thread per product on its own warp,
+// element-wise warpgroups and an epilogue that overlaps the next item;
+// bounded waits everywhere.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -140,15 +141,14 @@ __device__ __forceinline__ void p_ds_chunk32(const uint32_t* su, const uint32_t*
 }
 
 //
-// Work is done in half steps: half h of query tile i is its rows
-// [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads).  The two
-// element-wise warpgroups ping-pong: warpgroup h owns half h of every tile
-// and its own TMEM buffer (S^T | dP^T, 64 + 64 columns).  It overwrites the
-// columns it has read with P^T and dS^T (bf16, two per 32-bit column), which
-// the tensor core takes straight from TMEM as the A operand of dV += P^T dO_h
-// and dK += dS^T Q_h.  While one warpgroup computes, the tensor core works on
-// the other's half.
-
+// dK/dV work is done in half steps: half h of query tile i is its rows
+// [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads), with TMEM
+// buffer h (S^T | dP^T, 64 + 64 columns).  Both element-wise warpgroups take
+// each half step, 32 query columns each, and overwrite the columns they have
+// read with P^T and dS^T (bf16, two per 32-bit column), which the tensor core
+// takes straight from TMEM as the A operand of dV += P^T dO_h and
+// dK += dS^T Q_h.  While they compute one half, the tensor core works on the
+// other buffer.
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;

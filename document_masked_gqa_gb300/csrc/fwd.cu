@@ -1,27 +1,31 @@
 // Forward kernel: causal + document-masked GQA attention for one CP rank.
 //
-// One CTA per (query tile, K/V head).  A query tile is 128 rows: P = 128/g
+// Work item = (query tile, K/V head).  A query tile is 128 rows: P = 128/g
 // consecutive local positions x the g query heads sharing K/V head `kvh`
 // (GQA, "The Llama 3 Herd of Models - part 3/16", 3.3.2, and "Paper notes:
 // The Llama 3 Herd of Models", 8 key-value heads), so one K/V tile feeds g
-// heads at once.  The CTA walks the tile's list of non-skipped key tiles
+// heads at once.  An item walks the tile's list of non-skipped key tiles
 // (built by the block-mask builder) and keeps the online-softmax running max
 // and sum per row, rescaling the partial output, then divides by the sum
 // ("Training Infrastructure and Systems", "FlashAttention: never write the
 // score matrix", sections "Online softmax" and "Tiling").
 //
-// GB300 mapping (sm_103a):
-//   warp 0      TMA producer: Q once, then K tiles into a 3-stage ring
-//   warp 2      TMA producer: V tiles into a 2-stage ring (decoupled from K,
-//               so a K load never queues behind the release of a V slot)
-//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers (Q
-//               copied once into TMEM as the A operand), O += P V into a
-//               TMEM accumulator with P taken from TMEM; owns the allocation
-//   warps 2-3   load the tile's positions / document starts first
-//   warps 4-7   softmax: thread r owns row r (TMEM lane r): masks partial
-//               tiles, exponentiates in base 2, writes P (fp16 pairs) back
-//               over the S columns it has read, rescales O in TMEM when its
-//               reference max moves, and writes O (fp32) and LSE.
+// GB300 mapping (sm_103a), one persistent CTA per SM, 16 warps:
+//   warp 0      TMA producer: per item Q, then K_j and V_j (fp16 copy) for
+//               each key tile, through one ring of tile-sized slots
+//   warp 1      tcgen05 issuer for S = Q K^T into one of two TMEM buffers (Q
+//               copied once per item into TMEM as the A operand); owns the
+//               TMEM allocation
+//   warp 3      tcgen05 issuer for O += P V with P taken from TMEM
+//   warps 4-11  softmax: two warpgroups split each tile's 128 key columns,
+//               thread r of each owns row r (TMEM lane r); they exchange row
+//               maxima, exponentiate in base 2, write their half of P (fp16
+//               pairs) back over the S columns each has read, and rescale
+//               their half of O in TMEM when the reference max moves
+//   warps 12-15 epilogue: O (fp32) and LSE of an item while the softmax
+//               warps start the next one
+// Separate issuing threads keep the tensor pipe fed while the softmax warps
+// keep the warp schedulers busy.
 // Keeping Q and P in TMEM leaves the tensor core only K and V to read from
 // shared memory, which halves the shared-memory traffic per tile.
 // P V runs in fp16 against an fp16 copy of V made once per call
