@@ -47,22 +47,26 @@ struct FwdCfg {
   static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (16-bit)
-  // one ring of tile-sized slots carries every load in stream order: per
-  // work item Q, then K_j, V_j for each key tile j of its row list
-  static constexpr int kSlots = (D == 128) ? 6 : 10;
-  static constexpr int kStage = kSlots * kTileBytes;  // O epilogue staging, 2 KB per epilogue warp
+  // a ring of tile-sized slots carries K_j, V_j for each key tile j of each
+  // work item's row list; Q has a buffer of its own (the next item's Q is
+  // loaded as soon as the current one has been copied into TMEM)
+  static constexpr int kSlots = (D == 128) ? 5 : 10;
+  static constexpr int kQbuf = kSlots * kTileBytes;
+  static constexpr int kStage = kQbuf + kTileBytes;  // O epilogue staging, 2 KB per epilogue warp
   // row maxima [2 tiles][2 warpgroups][128], then per item parity: row sums
   // [2][2 warpgroups][128] and reference maxima [2][128]
   static constexpr int kXchg = kStage + 4 * 2048;
   static constexpr int kBar = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
-  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 1 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM: S buffers (128 columns each; P overwrites part of them as fp16
-  // pairs), the O accumulator, and Q as bf16 pairs (the A operand of Q K^T)
+  // pairs), the O accumulator, and two Q buffers as bf16 pairs (the A
+  // operand of Q K^T; item i uses buffer i % 2)
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
+  static_assert(kTmemQ + D <= 512, "forward TMEM layout exceeds 512 columns");
   static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
 };
 
@@ -127,8 +131,11 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* o_done = p_full + 2;       // [2] P V of a tile done (its S buffer is free)
   uint64_t* mx_ready = o_done + 2;     // [2] both softmax warpgroups posted a tile's row maxima
   uint64_t* l_ready = mx_ready + 2;    // both posted an item's partial row sums
-  uint64_t* q_tmem = l_ready + 1;      // an item's Q copied into TMEM
-  uint64_t* o_free = q_tmem + 1;       // the epilogue warps have read an item's O
+  uint64_t* q_tmem = l_ready + 1;      // [2] an item's Q copied into TMEM Q buffer item % 2
+  uint64_t* o_free = q_tmem + 2;       // the epilogue warps have read an item's O
+  uint64_t* q_full = o_free + 1;       // an item's Q in the Q buffer
+  uint64_t* q_empty = q_full + 1;      // ... copied into TMEM (buffer free)
+  uint8_t* sQ = smem + Cfg::kQbuf;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTileBytes; };
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&slot_full[i], 1);
       mbar_init(&slot_empty[i], 1);
     }
-    // the softmax warps arrive once per warp (8 warps; both warpgroups copy half of Q)
+    // the softmax and epilogue warps arrive once per warp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
@@ -146,8 +153,11 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&mx_ready[i], 8);
     }
     mbar_init(l_ready, 8);
-    mbar_init(q_tmem, 8);
+    mbar_init(&q_tmem[0], 4);
+    mbar_init(&q_tmem[1], 4);
     mbar_init(o_free, 4);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -164,28 +174,54 @@ __global__ void __launch_bounds__(512, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ producer: the stream
+      // K_j, V_j of every item through the slot ring; each item's Q into the
+      // Q buffer, the next one as soon as the current one is in TMEM
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int sidx = 0;
+      int sidx = 0, qn = 0;  // slot loads issued, Q loads issued
       bool ok = true;
       auto acquire = [&](int idx) -> bool {
         if (!mbar_wait(&slot_empty[idx % NS], ((idx / NS) & 1) ^ 1u, ctl)) return false;
         mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTileBytes);
         return true;
       };
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
-        const FwdItem it = fwd_item(p, item);
-        if (it.n == 0) continue;
-        if (!acquire(sidx)) { ok = false; break; }
+      auto load_q = [&](const FwdItem& qi) -> bool {
+        if (qn > 0 && !mbar_wait(q_empty, (qn - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(slot_ptr(sidx) + c * Cfg::kRegion, &tq, &slot_full[sidx % NS], c * 64,
-                      it.kvh * g, it.b * Lq + it.l0);
-        ++sidx;
+          tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, qi.kvh * g, qi.b * Lq + qi.l0);
+        ++qn;
+        return true;
+      };
+      bool first = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
+        const FwdItem it = fwd_item(p, item);
+        if (it.n == 0) continue;
+        if (first) {
+          if (!load_q(it)) { ok = false; break; }
+          first = false;
+        }
+        // the next item's Q: the buffer frees once this item's Q is in TMEM;
+        // issued between K / V loads as soon as that has happened
+        FwdItem nx{};
+        bool q_next = false;
+        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
+          const int cand = snake_item(kx);
+          if (cand >= n_items) continue;
+          nx = fwd_item(p, cand);
+          if (nx.n == 0) continue;
+          q_next = true;
+          break;
+        }
         for (int j = 0; j < it.n; ++j) {
+          if (q_next && mbar_try_wait(q_empty, (qn - 1) & 1)) {
+            if (!load_q(nx)) { ok = false; break; }
+            q_next = false;
+          }
           const int kt = static_cast<int>(static_cast<uint32_t>(it.list[j]) & kIndexMask);
           const int krow = it.b * p.seq_len + kt * kTileN;
           if (!acquire(sidx)) { ok = false; break; }
@@ -201,10 +237,12 @@ __global__ void __launch_bounds__(512, 1)
                         it.kvh * D + c * 64, krow);
           ++sidx;
         }
+        if (ok && q_next && !load_q(nx)) ok = false;
       }
       if (!ok) {  // drain this CTA's copies still in flight
         for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
           drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
+        if (qn > 0) drain_wait(q_full, (qn - 1) & 1, 100000000ull);
       }
     }
   } else if (warp == 1 || warp == 3) {
@@ -226,13 +264,10 @@ __global__ void __launch_bounds__(512, 1)
       if (item >= n_items) continue;
         const FwdItem it = fwd_item(p, item);
         if (it.n == 0) continue;
-        if (warp == 1) {
-          if (!mbar_wait(q_tmem, ibase & 1, ctl)) { ok = false; break; }
-          mbar_arrive(&slot_empty[sidx % NS]);  // Q is in TMEM: its slot goes back
-        }
+        if (warp == 1 && !mbar_wait(&q_tmem[ibase & 1], (ibase >> 1) & 1, ctl)) { ok = false; break; }
         for (int j = 0; j < it.n; ++j) {
           const int t = tbase + j, sb = t & 1;
-          const int kidx = sidx + 1 + 2 * j, vidx = kidx + 1;
+          const int kidx = sidx + 2 * j, vidx = kidx + 1;
           if (warp == 1) {
             if (!mbar_wait(&slot_full[kidx % NS], (kidx / NS) & 1, ctl)) { ok = false; break; }
             if (t >= 2 && !mbar_wait(&o_done[sb], ((t - 2) >> 1) & 1, ctl)) { ok = false; break; }
@@ -241,7 +276,7 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_f16_ts(d_s, tmem + Cfg::kTmemQ + 8 * kk,
+              mma_f16_ts(d_s, tmem + Cfg::kTmemQ + (ibase & 1) * (D / 2) + 8 * kk,
                          sdesc_sw128(k_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024),
                          idesc_s, kk > 0 ? 1u : 0u);
             mma_commit(&s_full[sb]);
@@ -268,7 +303,7 @@ __global__ void __launch_bounds__(512, 1)
             last_parity = (t >> 1) & 1;
           }
         }
-        sidx += 1 + 2 * it.n;
+        sidx += 2 * it.n;
         tbase += it.n;
         ++ibase;
       }
@@ -293,16 +328,7 @@ __global__ void __launch_bounds__(512, 1)
     float* xsum = xmax + 2 * 2 * 128;                           // [2 items][2 warpgroups][128]
     float* xm = xsum + 2 * 2 * 128;                             // [2 items][128]
     bool ok = true;
-    int sidx = 0, tbase = 0, ibase = 0;
-    int copied = -1;  // item whose Q is already in TMEM
-    auto copy_q = [&](int q_idx) -> bool {  // warpgroup w: half w of row r of Q into TMEM
-      if (!__all_sync(0xffffffffu, mbar_wait(&slot_full[q_idx % NS], (q_idx / NS) & 1, ctl)))
-        return false;
-      sw128_row_to_tmem_half<D>(smem_u32(slot_ptr(q_idx)), r, tmem + lane_base + Cfg::kTmemQ, w);
-      tmem_wait_st();
-      warp_arrive(q_tmem);
-      return true;
-    };
+    int tbase = 0, ibase = 0;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
@@ -310,7 +336,6 @@ __global__ void __launch_bounds__(512, 1)
       if (it.n == 0) continue;
       const int qabs = p.qpos[it.l0 + pos];
       const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + it.l0 + pos];
-      if (copied != item && !copy_q(sidx)) { ok = false; break; }
       float m_run = -INFINITY, l_run = 0.f;
       uint32_t e_next = static_cast<uint32_t>(it.list[0]);
       for (int j = 0; j < it.n; ++j) {
@@ -407,22 +432,6 @@ __global__ void __launch_bounds__(512, 1)
         m_run = m_new;
       }
       if (!ok) break;
-      // the last S of this item has been read: bring in the next item's Q
-      // now, so that its first S overlaps this epilogue
-      {
-        int nx = n_items;
-        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
-          const int cand = snake_item(kx);
-          if (cand < n_items && fwd_item(p, cand).n != 0) {
-            nx = cand;
-            break;
-          }
-        }
-        if (nx < n_items) {
-          if (!copy_q(sidx + 1 + 2 * it.n)) { ok = false; break; }
-          copied = nx;
-        }
-      }
       // post this item's row statistics for the epilogue warps: each
       // warpgroup's partial row sum, and the reference max (the same in
       // both).  Only once the epilogue has taken the previous item (its O
@@ -436,7 +445,6 @@ __global__ void __launch_bounds__(512, 1)
       if (w == 0) xm[(ibase & 1) * 128 + r] = m_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(l_ready);
-      sidx += 1 + 2 * it.n;
       tbase += it.n;
       ++ibase;
     }
@@ -456,11 +464,42 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 2048;
     bool ok = true;
     int tbase = 0, ibase = 0;
+    // row r of an item's Q (slot q_idx) into TMEM Q buffer qb.  Buffer qb was
+    // last used by the item two back, whose products completed before its
+    // epilogue, which these warps have done.
+    int qn = 0;  // Q tiles copied so far (the q_full / q_empty phase)
+    auto copy_q = [&](int qb) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(q_full, qn & 1, ctl))) return false;
+      sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ + qb * (D / 2));
+      tmem_wait_st();
+      warp_arrive(&q_tmem[qb]);
+      warp_arrive(q_empty);
+      ++qn;
+      return true;
+    };
+    bool first = true;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
       const FwdItem it = fwd_item(p, item);
       if (it.n == 0) continue;
+      if (first) {
+        if (!copy_q(ibase & 1)) { ok = false; break; }
+        first = false;
+      }
+      // the next item's Q into the other buffer as soon as it has landed, so
+      // that the S products run on into the next item without a gap
+      {
+        int nx = n_items;
+        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
+          const int cand = snake_item(kx);
+          if (cand < n_items && fwd_item(p, cand).n != 0) {
+            nx = cand;
+            break;
+          }
+        }
+        if (nx < n_items && !copy_q((ibase + 1) & 1)) { ok = false; break; }
+      }
       const int t_last = tbase + it.n - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
           !__all_sync(0xffffffffu,
