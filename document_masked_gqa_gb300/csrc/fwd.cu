@@ -56,7 +56,12 @@ struct FwdCfg {
   // row maxima [2 tiles][2 warpgroups][128], then per item parity: row sums
   // [2][2 warpgroups][128] and reference maxima [2][128]
   static constexpr int kXchg = kStage + 4 * 2048;
-  static constexpr int kBar = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
+  // per item parity, staged by the epilogue warps ahead of the item: n, list
+  // offset, first list entry, then per row the query position and its
+  // document's first position
+  static constexpr int kMeta = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
+  static constexpr int kMetaInts = 4 + 2 * 128;
+  static constexpr int kBar = kMeta + 2 * kMetaInts * 4;
   static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 1 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
@@ -322,22 +327,27 @@ __global__ void __launch_bounds__(512, 1)
     const int wq = warp & 3;  // TMEM lane quarter: rows 32*wq .. 32*wq + 31
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int lg = 31 - __clz(g);
-    const int pos = r >> lg;
     const float sl2 = p.scale_log2;
     float* xmax = reinterpret_cast<float*>(smem + Cfg::kXchg);  // [2 tiles][2 warpgroups][128]
     float* xsum = xmax + 2 * 2 * 128;                           // [2 items][2 warpgroups][128]
     float* xm = xsum + 2 * 2 * 128;                             // [2 items][128]
     bool ok = true;
     int tbase = 0, ibase = 0;
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
-      const FwdItem it = fwd_item(p, item);
-      if (it.n == 0) continue;
-      const int qabs = p.qpos[it.l0 + pos];
-      const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + it.l0 + pos];
+    // items in order, as staged by the epilogue warps (n == 0 ends the list)
+    for (;;) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_tmem[ibase & 1], (ibase >> 1) & 1, ctl))) {
+        ok = false;
+        break;
+      }
+      const int* meta = reinterpret_cast<const int*>(smem + Cfg::kMeta) + (ibase & 1) * Cfg::kMetaInts;
+      FwdItem it;
+      it.n = meta[0];
+      if (it.n == 0) break;
+      it.list = p.row_idx + meta[1];
+      const int qabs = meta[4 + r];
+      const int lo_r = meta[4 + 128 + r];
       float m_run = -INFINITY, l_run = 0.f;
-      uint32_t e_next = static_cast<uint32_t>(it.list[0]);
+      uint32_t e_next = static_cast<uint32_t>(meta[2]);
       for (int j = 0; j < it.n; ++j) {
         const int t = tbase + j, sb = t & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (t >> 1) & 1, ctl))) {
@@ -468,7 +478,26 @@ __global__ void __launch_bounds__(512, 1)
     // last used by the item two back, whose products completed before its
     // epilogue, which these warps have done.
     int qn = 0;  // Q tiles copied so far (the q_full / q_empty phase)
-    auto copy_q = [&](int qb) -> bool {
+    // stage item `mi`'s metadata for the softmax warps into buffer qb (the
+    // softmax warps read buffer qb at the top of the item two back, which
+    // they have finished); n = 0 marks the end of this CTA's items
+    auto stage_meta = [&](int qb, const FwdItem* mi) {
+      int* meta = reinterpret_cast<int*>(smem + Cfg::kMeta) + qb * Cfg::kMetaInts;
+      if (mi == nullptr) {
+        if (r == 0) meta[0] = 0;
+        return;
+      }
+      const int rpos = mi->l0 + (r >> lg);
+      meta[4 + r] = p.qpos[rpos];
+      meta[4 + 128 + r] = p.doc_lo[static_cast<long long>(mi->b) * Lq + rpos];
+      if (r == 0) {
+        meta[0] = mi->n;
+        meta[1] = static_cast<int>(mi->list - p.row_idx);
+        meta[2] = mi->list[0];
+      }
+    };
+    auto copy_q = [&](int qb, const FwdItem& mi) -> bool {
+      stage_meta(qb, &mi);
       if (!__all_sync(0xffffffffu, mbar_wait(q_full, qn & 1, ctl))) return false;
       sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ + qb * (D / 2));
       tmem_wait_st();
@@ -484,21 +513,27 @@ __global__ void __launch_bounds__(512, 1)
       const FwdItem it = fwd_item(p, item);
       if (it.n == 0) continue;
       if (first) {
-        if (!copy_q(ibase & 1)) { ok = false; break; }
+        if (!copy_q(ibase & 1, it)) { ok = false; break; }
         first = false;
       }
       // the next item's Q into the other buffer as soon as it has landed, so
       // that the S products run on into the next item without a gap
       {
-        int nx = n_items;
+        bool more = false;
         for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
           const int cand = snake_item(kx);
-          if (cand < n_items && fwd_item(p, cand).n != 0) {
-            nx = cand;
-            break;
-          }
+          if (cand >= n_items) continue;
+          const FwdItem nx = fwd_item(p, cand);
+          if (nx.n == 0) continue;
+          if (!copy_q((ibase + 1) & 1, nx)) ok = false;
+          more = true;
+          break;
         }
-        if (nx < n_items && !copy_q((ibase + 1) & 1)) { ok = false; break; }
+        if (!ok) break;
+        if (!more) {  // end of this CTA's items
+          stage_meta((ibase + 1) & 1, nullptr);
+          warp_arrive(&q_tmem[(ibase + 1) & 1]);
+        }
       }
       const int t_last = tbase + it.n - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
@@ -550,6 +585,10 @@ __global__ void __launch_bounds__(512, 1)
           (r >> lg)] = (m_ref + lg2(l_tot)) * 0.6931471805599453f;
       tbase += it.n;
       ++ibase;
+    }
+    if (ok && first) {  // no items at all: release the softmax warps
+      stage_meta(0, nullptr);
+      warp_arrive(&q_tmem[0]);
     }
   }
 
