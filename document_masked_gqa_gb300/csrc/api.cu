@@ -132,6 +132,19 @@ dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p) {
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// O (fp32 [rows][heads][D]) as a TMA store target: box = 32 columns x g heads
+// x 32/g positions (one epilogue warp's 32 rows), 128-byte swizzled.
+dma_status map_o_f32(CUtensorMap* m, void* base, const dma::PlanDev& p, int rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.head_dim),
+                              static_cast<cuuint64_t>(p.n_heads), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.head_dim) * 4,
+                                 static_cast<cuuint64_t>(p.n_heads) * p.head_dim * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(p.group),
+                             static_cast<cuuint32_t>(32 / p.group)};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 dma_status check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
@@ -233,14 +246,15 @@ dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
   if (!q || !k || !v || !o || !lse) return DMA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return DMA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv16;
+  CUtensorMap tq, tk, tv16, to;
   dma_status st;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, p.batch * p.local_len)) != DMA_OK) return st;
+  if ((st = map_o_f32(&to, o, p, p.batch * p.local_len)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv16, p.v16, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != DMA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dma::launch_v_to_f16(*plan, v, s) != cudaSuccess) return DMA_ERR_CUDA;
-  return dma::launch_fwd(*plan, tq, tk, tv16, o, lse, s) == cudaSuccess ? DMA_OK : DMA_ERR_CUDA;
+  return dma::launch_fwd(*plan, tq, tk, tv16, to, o, lse, s) == cudaSuccess ? DMA_OK : DMA_ERR_CUDA;
 }
 
 dma_status dma_attn_bwd_delta(dma_plan_t plan, const float* o, const dma_bf16* dout,
@@ -520,13 +534,14 @@ extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_doc
   // the plan kernels clear what must start at zero (status word, column
   // counts) and write every other array before it is read
   if (dma::launch_plan_kernels(pl, s) != cudaSuccess) return DMA_ERR_CUDA;
-  CUtensorMap tq, tk, tv16;
+  CUtensorMap tq, tk, tv16, to;
   dma_status st;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, p.batch * p.local_len)) != DMA_OK) return st;
+  if ((st = map_o_f32(&to, o, p, p.batch * p.local_len)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv16, p.v16, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != DMA_OK) return st;
   if (dma::launch_v_to_f16(pl, v, s) != cudaSuccess) return DMA_ERR_CUDA;
-  if (dma::launch_fwd(pl, tq, tk, tv16, o, lse, s) != cudaSuccess) return DMA_ERR_CUDA;
+  if (dma::launch_fwd(pl, tq, tk, tv16, to, o, lse, s) != cudaSuccess) return DMA_ERR_CUDA;
   if (status_dev &&
       cudaMemcpyAsync(status_dev, p.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
           cudaSuccess)

@@ -72,7 +72,8 @@ cudaError_t launch_cp_copy(const dma_plan_s& p, const void* src, void* dst, size
                            bool gather, cudaStream_t s);
 cudaError_t launch_v_to_f16(const dma_plan_s& p, const dma_bf16* v, cudaStream_t s);
 cudaError_t launch_fwd(const dma_plan_s& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv16, float* o, float* lse, cudaStream_t s);
+                       const CUtensorMap& tv16, const CUtensorMap& to, float* o, float* lse,
+                       cudaStream_t s);
 cudaError_t launch_delta(const dma_plan_s& p, const float* o, const dma_bf16* dout,
                          cudaStream_t s);
 cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,

@@ -52,10 +52,12 @@ struct FwdCfg {
   // loaded as soon as the current one has been copied into TMEM)
   static constexpr int kSlots = (D == 128) ? 5 : 10;
   static constexpr int kQbuf = kSlots * kTileBytes;
-  static constexpr int kStage = kQbuf + kTileBytes;  // O epilogue staging, 2 KB per epilogue warp
+  // O epilogue staging: per epilogue warp one 4 KB block of 32 rows x 32
+  // fp32 in the 128-byte swizzled layout of a TMA store
+  static constexpr int kStage = kQbuf + kTileBytes;
   // row maxima [2 tiles][2 warpgroups][128], then per item parity: row sums
   // [2][2 warpgroups][128] and reference maxima [2][128]
-  static constexpr int kXchg = kStage + 4 * 2048;
+  static constexpr int kXchg = kStage + 4 * 4096;
   // per item parity, staged by the epilogue warps ahead of the item: n, list
   // offset, first list entry, then per row the query position and its
   // document's first position
@@ -111,8 +113,8 @@ __device__ __forceinline__ FwdItem fwd_item(const PlanDev& p, int item) {
 template <int D>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tv, const PlanDev p,
-               float* __restrict__ o, float* __restrict__ lse, int n_items) {
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+               const PlanDev p, float* __restrict__ o, float* __restrict__ lse, int n_items) {
   using Cfg = FwdCfg<D>;
   constexpr int NS = Cfg::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -462,16 +464,17 @@ __global__ void __launch_bounds__(512, 1)
     // --------------------------------------------------------------- epilogue
     // per item: once its last P V is done and the softmax warps have posted
     // the row statistics, read O out of TMEM (row r = lane of warp w - 12),
-    // hand the accumulator back, then write O / l and the LSE.  O is staged
-    // per warp (16 columns at a time) and written in row-contiguous 64-byte
-    // runs; this overlaps the next item's tiles.
+    // hand the accumulator back, then write O / l (per warp, TMA stores of
+    // 32 x 32 fp32 blocks) and the LSE; this overlaps the next item's tiles.
+    // Ahead of that, the warps copy the next item's Q into the other TMEM Q
+    // buffer and stage its metadata for the softmax warps.
     const int wq = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int lg = 31 - __clz(g);
     const int r = 32 * wq + lane;
     const float* xsum = reinterpret_cast<const float*>(smem + Cfg::kXchg) + 2 * 2 * 128;
     const float* xm = xsum + 2 * 2 * 128;
-    const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 2048;
+    const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 4096;
     bool ok = true;
     int tbase = 0, ibase = 0;
     // row r of an item's Q (slot q_idx) into TMEM Q buffer qb.  Buffer qb was
@@ -554,32 +557,27 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) reg_fence32(u + c0);
       warp_arrive(o_free);
+      // O / l in blocks of 32 columns x this warp's 32 rows, each written
+      // with one TMA store (rows = 32/g positions x the g heads)
+      const int zrow = it.b * Lq + it.l0 + ((32 * wq) >> lg);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(stage + lane * 64 + ((q4 ^ (lane & 3)) << 4),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 1]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 2]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * q4 + 3]) * inv));
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        // the previous block's store must have read the staging buffer
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ci = lane + 32 * i;  // chunk: row ci / 4, part ci % 4
-          const int row = ci >> 2, part = ci & 3;
-          uint32_t a0, a1, a2, a3;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                       : "r"(stage + row * 64 + ((part ^ (row & 3)) << 4)));
-          const int tr = 32 * wq + row;  // tile row
-          const long long grow = static_cast<long long>(it.b) * Lq + it.l0 + (tr >> lg);
-          float4* dst = reinterpret_cast<float4*>(
-              o + (grow * p.n_heads + it.kvh * g + (tr & (g - 1))) * D + c0 + 4 * part);
-          *dst = make_float4(__uint_as_float(a0), __uint_as_float(a1), __uint_as_float(a2),
-                             __uint_as_float(a3));
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(stage + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 1]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 2]) * inv),
+                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 3]) * inv));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&to, smem + Cfg::kStage + wq * 4096, c0, it.kvh * g, zrow);
+          bulk_commit();
         }
-        __syncwarp();
       }
       lse[(static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (r & (g - 1))) * Lq + it.l0 +
           (r >> lg)] = (m_ref + lg2(l_tot)) * 0.6931471805599453f;
@@ -590,6 +588,7 @@ __global__ void __launch_bounds__(512, 1)
       stage_meta(0, nullptr);
       warp_arrive(&q_tmem[0]);
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -621,7 +620,8 @@ __global__ void v_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict
 
 template <int D>
 cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv16, float* o, float* lse, cudaStream_t s) {
+                         const CUtensorMap& tv16, const CUtensorMap& to, float* o, float* lse,
+                         cudaStream_t s) {
   const PlanDev& p = pl.d;
   const int items = p.batch * p.n_qtiles * p.n_kv_heads;
   if (items == 0) return cudaSuccess;
@@ -630,7 +630,7 @@ cudaError_t launch_fwd_d(const dma_plan_s& pl, const CUtensorMap& tq, const CUte
   const int smem = FwdCfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D><<<grid, 512, smem, s>>>(tq, tk, tv16, p, o, lse, items);
+  fwd_kernel<D><<<grid, 512, smem, s>>>(tq, tk, tv16, to, p, o, lse, items);
   return cudaGetLastError();
 }
 
@@ -648,9 +648,10 @@ cudaError_t launch_v_to_f16(const dma_plan_s& pl, const dma_bf16* v, cudaStream_
 }
 
 cudaError_t launch_fwd(const dma_plan_s& pl, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv16, float* o, float* lse, cudaStream_t s) {
-  if (pl.d.head_dim == 128) return launch_fwd_d<128>(pl, tq, tk, tv16, o, lse, s);
-  return launch_fwd_d<64>(pl, tq, tk, tv16, o, lse, s);
+                       const CUtensorMap& tv16, const CUtensorMap& to, float* o, float* lse,
+                       cudaStream_t s) {
+  if (pl.d.head_dim == 128) return launch_fwd_d<128>(pl, tq, tk, tv16, to, o, lse, s);
+  return launch_fwd_d<64>(pl, tq, tk, tv16, to, o, lse, s);
 }
 
 }  // namespace dma
