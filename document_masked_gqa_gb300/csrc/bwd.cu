@@ -230,11 +230,12 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* do_empty = bars + 7;   // [2]
   uint64_t* sdp_full = bars + 9;   // [2] per buffer: S^T and dP^T computed (two commits)
   uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them (both warpgroups)
-  uint64_t* buf_free = bars + 13;  // [2] dV, dK of that half step done
+  uint64_t* buf_free = bars + 13;  // [2] dK of that half step done (dS^T read)
   uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
   uint64_t* acc_done = bars + 17;  // an item's dV, dK complete
   uint64_t* kv_empty = bars + 18;  // an item's last S^T and dP^T done (two commits)
   uint64_t* acc_free = bars + 19;  // the epilogue warps have read an item's dV, dK
+  uint64_t* dv_free = bars + 20;   // [2] dV of that half step done (P^T read)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sdp_full[i], 2);
       mbar_init(&pds_full[i], 256);
       mbar_init(&buf_free[i], 1);
+      mbar_init(&dv_free[i], 1);
       mbar_init(&col_ready[i], 128);
     }
     mbar_init(acc_done, 1);
@@ -345,7 +347,11 @@ __global__ void __launch_bounds__(512, 1)
         for (int s = 0; s < 2 * it.n; ++s) {
           const int ig = tbase + (s >> 1), h = s & 1, st = ig & 1;
           const uint32_t ph = (ig >> 1) & 1;
-          if (ig >= 1 && !mbar_wait(&buf_free[h], (ig - 1) & 1, ctl)) { ok = false; break; }
+          // S^T overwrites P^T (read by dV), dP^T overwrites dS^T (read by dK)
+          if (ig >= 1 && !mbar_wait(is_s ? &dv_free[h] : &buf_free[h], (ig - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
           if (!mbar_wait(&b_full[st], ph, ctl)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + Cfg::kTmemBuf + 128 * h + d_off;
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(512, 1)
             mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk + (kk >= 2 ? 16 : 0),
                        sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                        (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&dv_free[h]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
             mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk + (kk >= 2 ? 16 : 0),
