@@ -936,6 +936,7 @@ __global__ void __launch_bounds__(640, 1)
           tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemS + cbase, su);
           tmem_wait_ld();
           reg_fence32(su);
+          warp_arrive(s_free);  // S is in registers: the buffer can take the next S
           const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(-lse2, -lse2);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -952,7 +953,6 @@ __global__ void __launch_bounds__(640, 1)
               if (!((allow >> c) & 1u)) pv[c] = 0.f;
           }
         }
-        warp_arrive(s_free);
         // dS = P (dP - Delta)
         if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
         tc_fence_after();
@@ -962,6 +962,7 @@ __global__ void __launch_bounds__(640, 1)
           tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase, du);
           tmem_wait_ld();
           reg_fence32(du);
+          warp_arrive(dp_free);  // dP is in registers: the buffer can take the next dP
           const uint64_t delx2 = f2(del, del);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -973,7 +974,6 @@ __global__ void __launch_bounds__(640, 1)
             pk[c >> 1] = pack_bf16(d0, d1);
           }
         }
-        warp_arrive(dp_free);
         if (t > 0 && !warp_wait(ds_done, (t - 1) & 1, ctl)) { ok = false; break; }
         // the dS buffer may still be read by the store of the previous dQ tile
         if (j == 0 && ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
