@@ -247,10 +247,10 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
       mbar_init(&sdp_full[i], 2);
-      mbar_init(&pds_full[i], 256);
+      mbar_init(&pds_full[i], 8);   // one arrival per element-wise warp
       mbar_init(&buf_free[i], 1);
       mbar_init(&dv_free[i], 1);
-      mbar_init(&col_ready[i], 128);
+      mbar_init(&col_ready[i], 2);  // the two staging warps of the warpgroup
     }
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
@@ -481,8 +481,11 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t e1 = (s1 & 1) ? e : e_nx;
             nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
           }
-          if (stager) col[(s & 1) * 64 + r] = cur * stat_mul;
-          mbar_arrive(&col_ready[w]);
+          if (stager) {
+            col[(s & 1) * 64 + r] = cur * stat_mul;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&col_ready[w]);
+          }
           if (!warp_wait(&col_ready[w], s & 1, ctl)) { ok = false; break; }
         }
         // allowed query positions of this key in the tile: [key, doc_end);
@@ -518,8 +521,7 @@ __global__ void __launch_bounds__(512, 1)
           tmem_st8_nowait(buf + 64 + 32 * w + 8, pd + 8);
         }
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&pds_full[h]);
+        warp_arrive(&pds_full[h]);
       }
       tbase += it.n;
     }
