@@ -477,34 +477,71 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
     h2d = h_k.nbytes + h_v.nbytes + h_cu.nbytes + sum(p[1].nbytes + p[2].nbytes for p in per)
     d2h = sum(sum(t.nbytes for t in p[3].values()) for p in per)
 
+    # Within a step the copies overlap the compute: inputs come in on one
+    # stream (dO after q, k, v, so that the forward starts first), the
+    # results go out on another as soon as the kernel producing them is
+    # done (O and LSE during the backward).  A step starts only after the
+    # previous one has finished, so every step pays for its own copies.
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    stream = torch.cuda.Stream(dev)  # compute; the binding launches on the current stream
+
     def one():
-        cu = h_cu.to(dev, non_blocking=True)
-        k = h_k.to(dev, non_blocking=True)
-        v = h_v.to(dev, non_blocking=True)
-        for r, h_q, h_do, outs in per:
-            q = h_q.to(dev, non_blocking=True)
-            do = h_do.to(dev, non_blocking=True)
+        s_in.wait_stream(stream)
+        with torch.cuda.stream(s_in):
+            cu = h_cu.to(dev, non_blocking=True)
+            k = h_k.to(dev, non_blocking=True)
+            v = h_v.to(dev, non_blocking=True)
+            qs = [h_q.to(dev, non_blocking=True) for _, h_q, _, _ in per]
+            ev_qkv = torch.cuda.Event()
+            ev_qkv.record(s_in)
+            dos = [h_do.to(dev, non_blocking=True) for _, _, h_do, _ in per]
+            ev_do = torch.cuda.Event()
+            ev_do.record(s_in)
+        for t in [cu, k, v] + qs + dos:
+            t.record_stream(stream)
+        stream.wait_event(ev_qkv)
+        fwd_out = []
+        for (r, h_q, h_do, outs), q in zip(per, qs):
             plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
                                 w.head_dim)
             o, lse = dma.dma_attn_fwd(plan, q, k, v)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                outs["o"].copy_(o, non_blocking=True)
+                outs["lse"].copy_(lse, non_blocking=True)
+            o.record_stream(s_out)
+            lse.record_stream(s_out)
+            fwd_out.append((plan, o, lse))
+        stream.wait_event(ev_do)
+        for (r, h_q, h_do, outs), q, do, (plan, o, lse) in zip(per, qs, dos, fwd_out):
             dq, dk, dv = dma.dma_attn_bwd(plan, q, k, v, o, lse, do)
-            outs["o"].copy_(o, non_blocking=True)
-            outs["lse"].copy_(lse, non_blocking=True)
-            outs["dq"].copy_(dq, non_blocking=True)
-            outs["dk"].copy_(dk, non_blocking=True)
-            outs["dv"].copy_(dv, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                outs["dq"].copy_(dq, non_blocking=True)
+                outs["dk"].copy_(dk, non_blocking=True)
+                outs["dv"].copy_(dv, non_blocking=True)
+            for t in (dq, dk, dv):
+                t.record_stream(s_out)
+        stream.wait_stream(s_out)
 
-    for _ in range(2):
-        one()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
     torch.cuda.synchronize(dev)
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
     torch.cuda.synchronize(dev)
     ms = reduce_max(a.elapsed_time(b) / steps, world, dev)
     return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": UNIT,
