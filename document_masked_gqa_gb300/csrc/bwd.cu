@@ -94,61 +94,65 @@ __global__ void delta_kernel(const float* __restrict__ o, const __nv_bfloat16* _
 
 // ---------------------------------------------------------------- dK / dV
 
-// 32 columns of one key row: P = exp2(S * scale*log2e - LSE*log2e) (zero where
-// the mask bit is clear when kMasked), dS = P (dP - Delta), both packed bf16.
-// nlse_c holds -LSE*log2e per column, del_c Delta; pairs of columns go
-// through the packed fp32x2 forms.
+// 32 columns of one key row, first phase: P = exp2(S * scale*log2e -
+// LSE*log2e) (zero where the mask bit is clear when kMasked), packed as bf16
+// pairs: the A operand of dV += P^T dO, and kept for dS = P (dP - Delta).
+// nlse_c holds -LSE*log2e per column.
 template <bool kMasked>
-__device__ __forceinline__ void p_ds_chunk32(const uint32_t* su, const uint32_t* du,
-                                             const float4* nlse_c, const float4* del_c,
-                                             uint32_t allow, float sl2, uint32_t* pk,
-                                             uint32_t* pd) {
+__device__ __forceinline__ void p_chunk32(const uint32_t* su, const float4* nlse_c,
+                                          uint32_t allow, float sl2, uint32_t* pb) {
   const uint64_t sl2x2 = f2(sl2, sl2);
 #pragma unroll
   for (int q = 0; q < 32; q += 4) {
     const float4 l4 = nlse_c[q >> 2];
-    const float4 d4 = del_c[q >> 2];
-    float pv[4];
-    {
-      float x0, x1, x2, x3;
-      f2_split(f2_fma(f2(__uint_as_float(su[q]), __uint_as_float(su[q + 1])), sl2x2, f2(l4.x, l4.y)),
-               x0, x1);
-      f2_split(f2_fma(f2(__uint_as_float(su[q + 2]), __uint_as_float(su[q + 3])), sl2x2,
-                      f2(l4.z, l4.w)),
-               x2, x3);
-      pv[0] = ex2(x0);
-      pv[1] = ex2(x1);
-      pv[2] = ex2(x2);
-      pv[3] = ex2(x3);
-    }
+    float x0, x1, x2, x3;
+    f2_split(f2_fma(f2(__uint_as_float(su[q]), __uint_as_float(su[q + 1])), sl2x2, f2(l4.x, l4.y)),
+             x0, x1);
+    f2_split(f2_fma(f2(__uint_as_float(su[q + 2]), __uint_as_float(su[q + 3])), sl2x2,
+                    f2(l4.z, l4.w)),
+             x2, x3);
+    float pv[4] = {ex2(x0), ex2(x1), ex2(x2), ex2(x3)};
     if (kMasked) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (!((allow >> (q + u)) & 1u)) pv[u] = 0.f;
     }
+    pb[q >> 1] = pack_bf16(pv[0], pv[1]);
+    pb[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+  }
+}
+
+// Second phase: dS = P (dP - Delta) for the same 32 columns, packed bf16
+// (the A operand of dK += dS^T Q).  P comes back from its bf16 pairs (a bf16
+// widens to fp32 by a 16-bit shift), the values dV was computed with.
+__device__ __forceinline__ void ds_chunk32(const uint32_t* du, const uint32_t* pb,
+                                           const float4* del_c, uint32_t* pd) {
+#pragma unroll
+  for (int q = 0; q < 32; q += 4) {
+    const float4 d4 = del_c[q >> 2];
+    const uint32_t w0 = pb[q >> 1], w1 = pb[(q >> 1) + 1];
     float d0, d1, d2, d3;
-    f2_split(f2_mul(f2(pv[0], pv[1]), f2_sub(f2(__uint_as_float(du[q]), __uint_as_float(du[q + 1])),
-                                             f2(d4.x, d4.y))),
+    f2_split(f2_mul(f2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u)),
+                    f2_sub(f2(__uint_as_float(du[q]), __uint_as_float(du[q + 1])), f2(d4.x, d4.y))),
              d0, d1);
-    f2_split(f2_mul(f2(pv[2], pv[3]),
-                    f2_sub(f2(__uint_as_float(du[q + 2]), __uint_as_float(du[q + 3])), f2(d4.z, d4.w))),
+    f2_split(f2_mul(f2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)),
+                    f2_sub(f2(__uint_as_float(du[q + 2]), __uint_as_float(du[q + 3])),
+                           f2(d4.z, d4.w))),
              d2, d3);
-    pk[q >> 1] = pack_bf16(pv[0], pv[1]);
-    pk[(q >> 1) + 1] = pack_bf16(pv[2], pv[3]);
     pd[q >> 1] = pack_bf16(d0, d1);
     pd[(q >> 1) + 1] = pack_bf16(d2, d3);
   }
 }
 
 //
-// dK/dV work is done in half steps: half h of query tile i is its rows
-// [64h, 64h + 64) (positions [h P/2, (h+1) P/2) x the g heads), with TMEM
-// buffer h (S^T | dP^T, 64 + 64 columns).  Both element-wise warpgroups take
-// each half step, 32 query columns each, and overwrite the columns they have
-// read with P^T and dS^T (bf16, two per 32-bit column), which the tensor core
-// takes straight from TMEM as the A operand of dV += P^T dO_h and
-// dK += dS^T Q_h.  While they compute one half, the tensor core works on the
-// other buffer.
+// dK/dV works a whole query tile at a time: S^T = K Q^T and dP^T = V dO^T
+// (128 keys x 128 query rows each, N = 128) land in TMEM buffers of their
+// own.  The element-wise warpgroups (thread = key, warpgroup w = query
+// columns [64w, 64w + 64)) first turn S^T into P^T and write it (bf16 pairs)
+// over the S^T columns they read, so that dV += P^T dO can start while
+// dP^T is still being computed; then they turn dP^T into dS^T the same way
+// for dK += dS^T Q.  A buffer is rewritten once the product that reads it
+// is done: S^T after dV, dP^T after dK.
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;
@@ -158,18 +162,17 @@ struct DkdvCfg {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;         // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;    // 2 stages
-  // dK / dV staging of the epilogue warps: per warp two 4 KB buffers of
+  // dK / dV staging of the epilogue warps: per warp one 4 KB block of
   // 32 rows x 32 fp32 in the 128-byte swizzled layout of a TMA store
   static constexpr int kStage = kDO + 2 * kTile;
-  static constexpr int kCOL = kStage + 4 * 2 * 4096;  // [warpgroup][2][32 LSE*log2e, 32 Delta]
-  static constexpr int kBar = kCOL + 2 * 2 * 64 * 4;
-  static constexpr int kNumBars = 22;
+  static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
+  static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
+  static constexpr int kNumBars = 20;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
-  // TMEM: dV [0,128), dK [128,256); buffer h at 256 + 128h: S^T in its
-  // first 64 columns, dP^T in the next 64
-  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemBuf = 256;
+  // TMEM: dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512)
+  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384;
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
 
@@ -192,9 +195,9 @@ __device__ __forceinline__ DkdvItem dkdv_item(const PlanDev& p, int item) {
   return it;
 }
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...  Every role keeps
-// the same counters across non-empty items: query tiles so far (tbase: the
-// Q / dO stage and the parity of every per-tile barrier) and items so far
+// Persistent: CTA c takes work items in snake order.  Every role keeps the
+// same counters across non-empty items: query tiles so far (tbase: the Q /
+// dO stage and the parity of every per-tile barrier) and items so far
 // (ibase: parity of kv_full, kv_empty, acc_done, acc_free).
 template <int D>
 __global__ void __launch_bounds__(512, 1)
@@ -228,14 +231,16 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* q_empty = bars + 3;    // [2]
   uint64_t* do_full = bars + 5;    // [2]
   uint64_t* do_empty = bars + 7;   // [2]
-  uint64_t* sdp_full = bars + 9;   // [2] per buffer: S^T and dP^T computed (two commits)
-  uint64_t* pds_full = bars + 11;  // [2] P^T, dS^T written over them (both warpgroups)
-  uint64_t* buf_free = bars + 13;  // [2] dK of that half step done (dS^T read)
+  uint64_t* s_full = bars + 9;     // S^T of the current tile computed
+  uint64_t* dp_full = bars + 10;   // dP^T computed
+  uint64_t* p_full = bars + 11;    // P^T written over S^T
+  uint64_t* ds_full = bars + 12;   // dS^T written over dP^T
+  uint64_t* dv_done = bars + 13;   // dV += P^T dO done (the S^T buffer is free)
+  uint64_t* dk_done = bars + 14;   // dK += dS^T Q done (the dP^T buffer is free)
   uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
   uint64_t* acc_done = bars + 17;  // an item's dV, dK complete
   uint64_t* kv_empty = bars + 18;  // an item's last S^T and dP^T done (two commits)
   uint64_t* acc_free = bars + 19;  // the epilogue warps have read an item's dV, dK
-  uint64_t* dv_free = bars + 20;   // [2] dV of that half step done (P^T read)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -246,12 +251,14 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
-      mbar_init(&sdp_full[i], 2);
-      mbar_init(&pds_full[i], 8);   // one arrival per element-wise warp
-      mbar_init(&buf_free[i], 1);
-      mbar_init(&dv_free[i], 1);
-      mbar_init(&col_ready[i], 2);  // the two staging warps of the warpgroup
+      mbar_init(&col_ready[i], 4);  // the four warps of the warpgroup
     }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 8);   // one arrival per element-wise warp
+    mbar_init(ds_full, 8);
+    mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
     mbar_init(acc_free, 4);
@@ -278,8 +285,8 @@ __global__ void __launch_bounds__(512, 1)
       int last_t = -1, ibase = 0, tbase = 0;
       bool kv_pending = false, ok = true;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         const int krow0 = it.b * p.seq_len + it.kt * kTileN;
@@ -322,52 +329,124 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------- MMA issuers: S^T (warp 1), dP^T (warp 2)
-      // half step (tile i, h): S^T = K Q_h^T and dP^T = V dO_h^T into buffer
-      // h, once dV / dK of the previous tile's half h have read that buffer.
-      // Each commits once to sdp_full[h], and once to kv_empty per item.
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
-      const bool is_s = warp == 1;
-      const uint32_t a_addr = smem_u32(is_s ? sK : sV);
-      uint8_t* b_tiles = is_s ? sQ : sDO;
-      uint64_t* b_full = is_s ? q_full : do_full;
-      const uint32_t d_off = is_s ? 0u : 64u;
+      // ------------------------------------------ MMA issuer: S^T, then dK
+      // per query tile t: S^T(t) = K Q^T into its buffer once dV(t-1) has read
+      // P^T(t-1) there, then dK(t-1) += dS^T Q: the tensor pipe takes S^T(t),
+      // on which the next element-wise phase waits, before dK(t-1).  (dS^T
+      // A operands from TMEM: warpgroup w's query columns [64w, 64w + 64) sit
+      // in TMEM columns [64w, 64w + 32) of the buffer, 8 per 16-deep step.)
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t k_addr = smem_u32(sK);
+      uint64_t* last_commit = nullptr;
+      uint32_t last_parity = 0;
+      bool ok = true;
+      int tbase = 0, ibase = 0;
+      // the tile whose dK is still to be issued (-1: none), and whether it
+      // is the first / last of its item
+      int pk = -1;
+      bool pk_first = false, pk_last = false;
+      int acc_items = 0;  // acc_done phases committed
+      auto issue_dk = [&]() -> bool {
+        if (!mbar_wait(ds_full, pk & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ + (pk & 1) * Cfg::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                     sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                     (!pk_first || kk > 0) ? 1u : 0u);
+        mma_commit(dk_done);
+        // dV(pk) is known complete (dv_done was awaited): Q, dO of tile pk
+        // are free once dK(pk) is, and so is the item's accumulator pair
+        mma_commit(&do_empty[pk & 1]);
+        mma_commit(&q_empty[pk & 1]);
+        last_commit = dk_done;
+        last_parity = pk & 1;
+        if (pk_last) {
+          mma_commit(acc_done);
+          last_commit = acc_done;
+          last_parity = acc_items & 1;
+          ++acc_items;
+        }
+        return true;
+      };
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
+        const DkdvItem it = dkdv_item(p, item);
+        if (it.n == 0) continue;
+        if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
+        for (int i = 0; i < it.n; ++i) {
+          const int ig = tbase + i, st = ig & 1;
+          if (ig >= 1 && !mbar_wait(dv_done, (ig - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&q_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+            mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
+                        sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(s_full);
+          last_commit = s_full;
+          last_parity = ig & 1;
+          if (pk >= 0) {
+            if (!issue_dk()) { ok = false; break; }
+          }
+          pk = ig;
+          pk_first = i == 0;
+          pk_last = i == it.n - 1;
+        }
+        if (!ok) break;
+        mma_commit(kv_empty);  // this item's K reads are done once these complete
+        tbase += it.n;
+        ++ibase;
+      }
+      if (ok && pk >= 0) {  // the CTA's last tile
+        if (!mbar_wait(dv_done, pk & 1, ctl)) ok = false;
+        else if (!issue_dk()) ok = false;
+      }
+      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ------------------------------------------------- MMA issuer: dP^T
+      // per query tile: dP^T = V dO^T into its buffer once dK of the previous
+      // tile has read dS^T there
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t v_addr = smem_u32(sV);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
       int tbase = 0, ibase = 0;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
-        for (int s = 0; s < 2 * it.n; ++s) {
-          const int ig = tbase + (s >> 1), h = s & 1, st = ig & 1;
-          const uint32_t ph = (ig >> 1) & 1;
-          // S^T overwrites P^T (read by dV), dP^T overwrites dS^T (read by dK)
-          if (ig >= 1 && !mbar_wait(is_s ? &dv_free[h] : &buf_free[h], (ig - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&b_full[st], ph, ctl)) { ok = false; break; }
+        for (int i = 0; i < it.n; ++i) {
+          const int ig = tbase + i, st = ig & 1;
+          if (ig >= 1 && !mbar_wait(dk_done, (ig - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d = tmem + Cfg::kTmemBuf + 128 * h + d_off;
-          const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile) + h * 8192;
+          const uint32_t b_addr = smem_u32(sDO + st * Cfg::kTile);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_bf16_ss(d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024),
-                        idesc_s, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
+                        sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&sdp_full[h]);
-          last_commit = &sdp_full[h];
+          mma_commit(dp_full);
+          last_commit = dp_full;
           last_parity = ig & 1;
         }
         if (!ok) break;
-        mma_commit(kv_empty);  // this item's K / V reads are done once these complete
+        mma_commit(kv_empty);  // this item's V reads are done once these complete
         tbase += it.n;
         ++ibase;
       }
@@ -375,55 +454,39 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 3) {
     if (lane == 0) {
-      // -------------------------------------------------- MMA issuer: dV, dK
-      // once both warpgroups have written P^T, dS^T over buffer h:
-      // dV += P^T dO_h, dK += dS^T Q_h (A operands from TMEM).  A separate
-      // issuing thread keeps these queued behind the S^T / dP^T products.
+      // --------------------------------------------------- MMA issuer: dV
+      // dV += P^T dO once P^T is in TMEM (A operand from TMEM, laid out as
+      // for dK above)
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
       int tbase = 0, ibase = 0;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
-        for (int s = 0; s < 2 * it.n; ++s) {
-          const int ig = tbase + (s >> 1), h = s & 1, st = ig & 1;
-          const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * h;
-          if (!mbar_wait(&pds_full[h], ig & 1, ctl)) { ok = false; break; }
+        for (int i = 0; i < it.n; ++i) {
+          const int ig = tbase + i, st = ig & 1;
+          if (!mbar_wait(p_full, ig & 1, ctl)) { ok = false; break; }
           // the item's first products overwrite dV, dK: the previous item's
           // must have been read out by the epilogue warps
-          if (s == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+          if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+          // P^T follows from Q alone: dO may still be on its way
+          if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile) + h * 8192;
-          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile) + h * 8192;
-          // warpgroup w left its 32 query columns of P^T at buf + 32w (16
-          // packed columns) and of dS^T at buf + 64 + 32w
+          const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h; K = the half's 64 rows
-            mma_f16_ts(tmem + Cfg::kTmemDV, buf + 8 * kk + (kk >= 2 ? 16 : 0),
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + 64 * (kk >> 2) + 8 * (kk & 3),
                        sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                       (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&dv_free[h]);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
-            mma_f16_ts(tmem + Cfg::kTmemDK, buf + 64 + 8 * kk + (kk >= 2 ? 16 : 0),
-                       sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                       (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&buf_free[h]);
-          last_commit = &buf_free[h];
+                       (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(dv_done);
+          last_commit = dv_done;
           last_parity = ig & 1;
-          if (h == 1) {
-            mma_commit(&do_empty[st]);
-            mma_commit(&q_empty[st]);
-          }
         }
         if (!ok) break;
-        mma_commit(acc_done);
-        last_commit = acc_done;
-        last_parity = ibase & 1;
         tbase += it.n;
         ++ibase;
       }
@@ -431,21 +494,22 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp < 12) {
     // ----------------------------------------------------------- key rows
-    // thread r of warpgroup w owns key r and, in every half step, the 32
-    // query columns [32w, 32w + 32) of that half
+    // thread r of warpgroup w owns key r and query columns [64w, 64w + 64)
+    // of every query tile
     const int t = threadIdx.x - 128;
     const int r = t & 127, w = t >> 7;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int lg = 31 - __clz(g);
     const float sl2 = p.scale_log2;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
-    // statistics of this warpgroup's columns: thread r < 32 stages LSE of
-    // column 32w + r, thread 32 <= r < 64 Delta of column 32w + r - 32
-    const int qsub = 32 * w + (r & 31);
-    const bool stager = r < 64;
-    const float* stat_src = (r < 32) ? lse : p.delta;
-    const float stat_mul = (r < 32) ? -kLog2e : 1.f;  // staged: -LSE*log2e, Delta
-    float* col = sCOL + w * 128;  // [2 stages][64] floats per warpgroup
+    // statistics of this warpgroup's columns: thread r < 64 stages
+    // -LSE*log2e of column 64w + r, thread r >= 64 Delta of column 64w + r - 64
+    const int qcol = 64 * w + (r & 63);
+    const float* stat_src = (r < 64) ? lse : p.delta;
+    const float stat_mul = (r < 64) ? -kLog2e : 1.f;
+    float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
+    const uint32_t s_cols = tmem + lane_base + Cfg::kTmemS + 64 * w;
+    const uint32_t dp_cols = tmem + lane_base + Cfg::kTmemDP + 64 * w;
     bool ok = true;
     int tbase = 0;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
@@ -456,72 +520,84 @@ __global__ void __launch_bounds__(512, 1)
       const int key = it.kt * kTileN + r;  // position within the sample
       // queries that may attend this key: positions [key, doc_end)
       const int doc_end = p.doc_hi[static_cast<long long>(it.b) * p.seq_len + key];
-      auto stat_row = [&](int hh) -> long long {
-        const int qrow = 64 * hh + qsub;
-        return (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (qrow & (g - 1))) * Lq +
-               (qrow >> lg);
-      };
-      const long long stat_base0 = stat_row(0), stat_base1 = stat_row(1);
-      const int steps = 2 * it.n;
+      const long long stat_base =
+          (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (qcol & (g - 1))) * Lq +
+          (qcol >> lg);
       // list entries of this tile (e) and the next (e_nx), loaded a tile ahead
       uint32_t e = static_cast<uint32_t>(it.list[0]);
       uint32_t e_nx = it.n > 1 ? static_cast<uint32_t>(it.list[1]) : 0u;
-      float nxt = stager ? stat_src[stat_base0 + static_cast<int>(e & kIndexMask) * P] : 0.f;
-      for (int s = 0; s < steps; ++s) {
-        const int i = s >> 1, h = s & 1, ig = tbase + i;
-        if (s > 0 && h == 0) {
+      float nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
+      for (int i = 0; i < it.n; ++i) {
+        const int ig = tbase + i;
+        if (i > 0) {
           e = e_nx;
           if (i + 1 < it.n) e_nx = static_cast<uint32_t>(it.list[i + 1]);
         }
         {
-          // stage this step's statistics, fetch the next step's
+          // stage this tile's statistics, fetch the next tile's
           const float cur = nxt;
-          if (stager && s + 1 < steps) {
-            const int s1 = s + 1;
-            const uint32_t e1 = (s1 & 1) ? e : e_nx;
-            nxt = stat_src[((s1 & 1) ? stat_base1 : stat_base0) + static_cast<int>(e1 & kIndexMask) * P];
-          }
-          if (stager) {
-            col[(s & 1) * 64 + r] = cur * stat_mul;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&col_ready[w]);
-          }
-          if (!warp_wait(&col_ready[w], s & 1, ctl)) { ok = false; break; }
+          if (i + 1 < it.n) nxt = stat_src[stat_base + static_cast<int>(e_nx & kIndexMask) * P];
+          col[(ig & 1) * 128 + r] = cur * stat_mul;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&col_ready[w]);
+          if (!warp_wait(&col_ready[w], ig & 1, ctl)) { ok = false; break; }
         }
         // allowed query positions of this key in the tile: [key, doc_end);
-        // in this warpgroup's columns of half h: [lo_c, hi_c)
-        int lo_c = 0, hi_c = 32;
+        // in tile columns: [lo_c, hi_c)
+        int lo_c = 0, hi_c = 128;
         if (e & kPartialBit) {
           const int l0 = static_cast<int>(e & kIndexMask) * P;
           const int q0 = (l0 < C) ? (ca * C + l0) : (cb * C + (l0 - C));
-          lo_c = (max(0, key - q0) << lg) - 64 * h - 32 * w;
-          hi_c = (min(P, max(0, doc_end - q0)) << lg) - 64 * h - 32 * w;
+          lo_c = max(0, key - q0) << lg;
+          hi_c = min(P, max(0, doc_end - q0)) << lg;
         }
-        const float4* lse_c = reinterpret_cast<const float4*>(col + (s & 1) * 64);
-        const float4* del_c = reinterpret_cast<const float4*>(col + (s & 1) * 64 + 32);
-        const uint32_t buf = tmem + lane_base + Cfg::kTmemBuf + 128 * h;
-        if (!warp_wait(&sdp_full[h], ig & 1, ctl)) { ok = false; break; }
+        const bool masked = (e & kPartialBit) != 0;
+        const float4* nlse_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128);
+        const float4* del_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128 + 64);
+        // phase 1: P^T over S^T.  All 64 columns come in with one wait: a
+        // TMEM load takes hundreds of cycles while the tensor pipe is busy.
+        if (!warp_wait(s_full, ig & 1, ctl)) { ok = false; break; }
         tc_fence_after();
+        uint32_t pb[32];  // P of the 64 columns as bf16 pairs
         {
-          uint32_t su[32], du[32];
-          tmem_ld32_nowait(buf + 32 * w, su);
-          tmem_ld32_nowait(buf + 64 + 32 * w, du);
+          uint32_t su[64];
+          tmem_ld32_nowait(s_cols, su);
+          tmem_ld32_nowait(s_cols + 32, su + 32);
           tmem_wait_ld();
           reg_fence32(su);
+          reg_fence32(su + 32);
+          if (masked) {
+            p_chunk32<true>(su, nlse_c, range_bits(lo_c - 64 * w, hi_c - 64 * w), sl2, pb);
+            p_chunk32<true>(su + 32, nlse_c + 8, range_bits(lo_c - 64 * w - 32, hi_c - 64 * w - 32),
+                            sl2, pb + 16);
+          } else {
+            p_chunk32<false>(su, nlse_c, 0u, sl2, pb);
+            p_chunk32<false>(su + 32, nlse_c + 8, 0u, sl2, pb + 16);
+          }
+        }
+        // over the first 32 of the S^T columns
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st8_nowait(s_cols + 8 * c, pb + 8 * c);
+        tmem_wait_st();
+        warp_arrive(p_full);
+        // phase 2: dS^T over dP^T
+        if (!warp_wait(dp_full, ig & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t du[64];
+          tmem_ld32_nowait(dp_cols, du);
+          tmem_ld32_nowait(dp_cols + 32, du + 32);
+          tmem_wait_ld();
           reg_fence32(du);
-          uint32_t pk[16], pd[16];
-          if (e & kPartialBit)
-            p_ds_chunk32<true>(su, du, lse_c, del_c, range_bits(lo_c, hi_c), sl2, pk, pd);
-          else
-            p_ds_chunk32<false>(su, du, lse_c, del_c, 0u, sl2, pk, pd);
-          // P^T and dS^T of these 32 columns over the first 16 columns read
-          tmem_st8_nowait(buf + 32 * w, pk);
-          tmem_st8_nowait(buf + 32 * w + 8, pk + 8);
-          tmem_st8_nowait(buf + 64 + 32 * w, pd);
-          tmem_st8_nowait(buf + 64 + 32 * w + 8, pd + 8);
+          reg_fence32(du + 32);
+          uint32_t pd[32];
+          ds_chunk32(du, pb, del_c, pd);
+          ds_chunk32(du + 32, pb + 16, del_c + 8, pd + 16);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_st8_nowait(dp_cols + 8 * c, pd + 8 * c);
         }
         tmem_wait_st();
-        warp_arrive(&pds_full[h]);
+        warp_arrive(ds_full);
       }
       tbase += it.n;
     }
@@ -534,9 +610,9 @@ __global__ void __launch_bounds__(512, 1)
     // last read.  Items without queries get zero rows the same way.
     const int wq = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t stage0 = smem_u32(smem + Cfg::kStage) + wq * 8192;
+    const uint32_t stg = smem_u32(smem + Cfg::kStage) + wq * 4096;
     bool ok = true;
-    int ibase = 0, round = 0;
+    int ibase = 0;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
@@ -562,13 +638,9 @@ __global__ void __launch_bounds__(512, 1)
           for (int c = 0; c < 32; ++c) u[c] = 0u;
         }
         const float sc = is_dk ? p.scale : 1.f;
-        // this buffer was last stored two rounds ago: wait until that store
-        // has read it
-        if (lane == 0 && round >= 2) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        }
+        // the previous block's store must have read the staging buffer
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        const uint32_t stg = stage0 + (round & 1) * 4096;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
@@ -586,7 +658,6 @@ __global__ void __launch_bounds__(512, 1)
               : "memory");
           bulk_commit();
         }
-        ++round;
       }
       if (!empty) ++ibase;
     }
