@@ -11,11 +11,11 @@
 // score matrix", sections "Online softmax" and "Tiling").
 //
 // GB300 mapping (sm_103a), one persistent CTA per SM, 16 warps:
-//   warp 0      TMA producer: per item Q, then K_j and V_j (fp16 copy) for
-//               each key tile, through one ring of tile-sized slots
-//   warp 1      tcgen05 issuer for S = Q K^T into one of two TMEM buffers (Q
-//               copied once per item into TMEM as the A operand); owns the
-//               TMEM allocation
+//   warp 0      TMA producer: per item Q (two buffers), then K_j and V_j
+//               (fp16 copy) for each key tile through two rings of
+//               tile-sized slots, K one tile ahead of V
+//   warp 1      tcgen05 issuer for S = Q K^T into one of three TMEM buffers
+//               (Q and K from shared memory); owns the TMEM allocation
 //   warp 3      tcgen05 issuer for O += P V with P taken from TMEM
 //   warps 4-11  softmax: two warpgroups split each tile's 128 key columns,
 //               thread r of each owns row r (TMEM lane r); they exchange row
@@ -26,8 +26,9 @@
 //               warps start the next one
 // Separate issuing threads keep the tensor pipe fed while the softmax warps
 // keep the warp schedulers busy.
-// Keeping Q and P in TMEM leaves the tensor core only K and V to read from
-// shared memory, which halves the shared-memory traffic per tile.
+// Three S buffers let S_{t+1} and S_{t+2} be computed while tile t's
+// softmax and P V run: S_{t+3} waits only for P_t V_t, which reads P_t from
+// S_t's buffer, so the softmax warps rarely wait for a score tile.
 // P V runs in fp16 against an fp16 copy of V made once per call
 // (v_to_f16_kernel): fp16's 11-bit significand keeps the rounding of the
 // probabilities 8x below bf16's, so O meets a 1e-2 absolute bound even on
@@ -47,14 +48,17 @@ struct FwdCfg {
   static constexpr int kRegion = 128 * 128;       // one 64-column SW128 region of a 128-row tile
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile (16-bit)
-  // a ring of tile-sized slots carries K_j, V_j for each key tile j of each
-  // work item's row list; Q has a buffer of its own (the next item's Q is
-  // loaded as soon as the current one has been copied into TMEM)
-  static constexpr int kSlots = (D == 128) ? 5 : 10;
-  static constexpr int kQbuf = kSlots * kTileBytes;
+  // K_j and V_j of each work item's row list go through two rings of
+  // tile-sized slots, K loaded a tile ahead of V; Q has two buffers of its
+  // own (item i uses buffer i % 2, so the next item's Q loads while the
+  // current one is still in use)
+  static constexpr int kKVSlots = (D == 128) ? 2 : 4;  // per ring
+  static constexpr int kKring = 0;
+  static constexpr int kVring = kKring + kKVSlots * kTileBytes;
+  static constexpr int kQbuf = kVring + kKVSlots * kTileBytes;  // 2 buffers
   // O epilogue staging: per epilogue warp one 4 KB block of 32 rows x 32
   // fp32 in the 128-byte swizzled layout of a TMA store
-  static constexpr int kStage = kQbuf + kTileBytes;
+  static constexpr int kStage = kQbuf + 2 * kTileBytes;
   // row maxima [2 tiles][2 warpgroups][128], then per item parity: row sums
   // [2][2 warpgroups][128] and reference maxima [2][128]
   static constexpr int kXchg = kStage + 4 * 4096;
@@ -64,16 +68,15 @@ struct FwdCfg {
   static constexpr int kMeta = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
   static constexpr int kMetaInts = 4 + 2 * 128;
   static constexpr int kBar = kMeta + 2 * kMetaInts * 4;
-  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 1 + 2;
+  static constexpr int kNumBars = 4 * kKVSlots + 3 * 3 + 2 + 1 + 2 + 1 + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM: S buffers (128 columns each; P overwrites part of them as fp16
-  // pairs), the O accumulator, and two Q buffers as bf16 pairs (the A
-  // operand of Q K^T; item i uses buffer i % 2)
-  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
-  static_assert(kTmemQ + D <= 512, "forward TMEM layout exceeds 512 columns");
+  // TMEM: three S buffers (128 columns each; P overwrites part of one as
+  // fp16 pairs; tile t uses buffer t % 3) and the O accumulator
+  static constexpr uint32_t kTmemO = 384;
+  static_assert(kTmemO + D <= 512, "forward TMEM layout exceeds 512 columns");
   static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
 };
 
@@ -105,18 +108,18 @@ __device__ __forceinline__ FwdItem fwd_item(const PlanDev& p, int item) {
   return it;
 }
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...  Every role keeps
-// the same counters across items: the stream index of the next slot load
-// (sidx), the key tiles processed so far (tbase: S buffer t & 1 and every
-// per-tile barrier parity follow from the global tile index t) and the
-// items so far (ibase: parity of q_tmem and l_ready).
+// Persistent: CTA c takes work items in snake order.  Every role keeps the
+// same counters across non-empty items: the key tiles processed so far
+// (tbase: K / V slot t % kKVSlots, S buffer t % 3 and every per-tile barrier
+// parity follow from the global tile index t) and the items so far (ibase:
+// Q buffer and metadata buffer ibase % 2, parity of l_ready and o_free).
 template <int D>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                const PlanDev p, float* __restrict__ o, float* __restrict__ lse, int n_items) {
   using Cfg = FwdCfg<D>;
-  constexpr int NS = Cfg::kSlots;
+  constexpr int NS = Cfg::kKVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
@@ -129,42 +132,48 @@ __global__ void __launch_bounds__(512, 1)
   const int g = p.group, Lq = p.local_len;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* slot_full = bars;          // [NS]
-  uint64_t* slot_empty = bars + NS;    // [NS]
-  uint64_t* s_full = bars + 2 * NS;    // [2] S computed in buffer t & 1
-  // per S buffer (tile parity), so that no waiter can fall two phases behind
-  // while the S and P V issuers run independently
-  uint64_t* p_full = s_full + 2;       // [2] P written over S
-  uint64_t* o_done = p_full + 2;       // [2] P V of a tile done (its S buffer is free)
-  uint64_t* mx_ready = o_done + 2;     // [2] both softmax warpgroups posted a tile's row maxima
+  uint64_t* k_full = bars;              // [NS] K ring
+  uint64_t* k_empty = bars + NS;        // [NS]
+  uint64_t* v_full = bars + 2 * NS;     // [NS] V ring
+  uint64_t* v_empty = bars + 3 * NS;    // [NS]
+  // per S buffer (tile t uses buffer t % 3), so that no waiter can fall two
+  // phases behind while the S and P V issuers run independently
+  uint64_t* s_full = bars + 4 * NS;    // [3] S computed
+  uint64_t* p_full = s_full + 3;       // [3] P written over S
+  uint64_t* o_done = p_full + 3;       // [3] P V of a tile done (its S buffer is free)
+  uint64_t* mx_ready = o_done + 3;     // [2] both softmax warpgroups posted a tile's row maxima
   uint64_t* l_ready = mx_ready + 2;    // both posted an item's partial row sums
-  uint64_t* q_tmem = l_ready + 1;      // [2] an item's Q copied into TMEM Q buffer item % 2
-  uint64_t* o_free = q_tmem + 2;       // the epilogue warps have read an item's O
-  uint64_t* q_full = o_free + 1;       // an item's Q in the Q buffer
-  uint64_t* q_empty = q_full + 1;      // ... copied into TMEM (buffer free)
+  uint64_t* meta_ready = l_ready + 1;  // [2] an item's metadata staged in buffer item % 2
+  uint64_t* o_free = meta_ready + 2;   // the epilogue warps have read an item's O
+  uint64_t* q_full = o_free + 1;       // [2] an item's Q in Q buffer item % 2
+  uint64_t* q_empty = q_full + 2;      // [2] ... and all its S products done
   uint8_t* sQ = smem + Cfg::kQbuf;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
-  auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTileBytes; };
+  auto k_slot = [&](int t) { return smem + Cfg::kKring + (t % NS) * Cfg::kTileBytes; };
+  auto v_slot = [&](int t) { return smem + Cfg::kVring + (t % NS) * Cfg::kTileBytes; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&slot_full[i], 1);
-      mbar_init(&slot_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     // the softmax and epilogue warps arrive once per warp
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
       mbar_init(&o_done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&mx_ready[i], 8);
+      mbar_init(&meta_ready[i], 4);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
     }
     mbar_init(l_ready, 8);
-    mbar_init(&q_tmem[0], 4);
-    mbar_init(&q_tmem[1], 4);
     mbar_init(o_free, 4);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -181,136 +190,143 @@ __global__ void __launch_bounds__(512, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ producer: the stream
-      // K_j, V_j of every item through the slot ring; each item's Q into the
-      // Q buffer, the next one as soon as the current one is in TMEM
+      // Two cursors walk this CTA's key tiles in order: the K cursor (which
+      // also loads an item's Q when it enters the item) runs one tile ahead
+      // of the V cursor, so that the S products never wait for a V slot to
+      // free.  Tile t's K goes to K slot t % NS once S_{t-NS} is done, its V
+      // to V slot t % NS once P_{t-NS} V_{t-NS} is done.
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int sidx = 0, qn = 0;  // slot loads issued, Q loads issued
+      struct Cursor {
+        int k;     // snake step of the current item
+        int j;     // tile within it
+        int t;     // global tile index
+        int item;  // non-empty items entered so far - 1
+        FwdItem it;
+        bool done;
+      };
+      // move a cursor to the first tile of the next non-empty item
+      auto next_item = [&](Cursor& c) {
+        for (++c.k; c.k * static_cast<int>(gridDim.x) < n_items; ++c.k) {
+          const int item = snake_item(c.k);
+          if (item >= n_items) continue;
+          c.it = fwd_item(p, item);
+          if (c.it.n == 0) continue;
+          c.j = 0;
+          ++c.item;
+          return;
+        }
+        c.done = true;
+      };
+      Cursor kc{-1, 0, 0, -1, FwdItem{}, false}, vc = kc;
+      next_item(kc);
+      next_item(vc);
       bool ok = true;
-      auto acquire = [&](int idx) -> bool {
-        if (!mbar_wait(&slot_empty[idx % NS], ((idx / NS) & 1) ^ 1u, ctl)) return false;
-        mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTileBytes);
-        return true;
-      };
-      auto load_q = [&](const FwdItem& qi) -> bool {
-        if (qn > 0 && !mbar_wait(q_empty, (qn - 1) & 1, ctl)) return false;
-        mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
+      int q_issued = 0;  // Q loads issued (item index of the next one)
+      while (ok && !vc.done) {
+        const bool do_k = !kc.done && kc.t <= vc.t + 1;
+        Cursor& c = do_k ? kc : vc;
+        if (do_k && c.j == 0 && q_issued == c.item) {
+          // entering an item: its Q into buffer item % 2 once the S products
+          // of the item two back are done
+          const int qb = c.item & 1;
+          if (!mbar_wait(&q_empty[qb], ((c.item >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&q_full[qb], Cfg::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(sQ + c * Cfg::kRegion, &tq, q_full, c * 64, qi.kvh * g, qi.b * Lq + qi.l0);
-        ++qn;
-        return true;
-      };
-      bool first = true;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
-        const FwdItem it = fwd_item(p, item);
-        if (it.n == 0) continue;
-        if (first) {
-          if (!load_q(it)) { ok = false; break; }
-          first = false;
+          for (int ch = 0; ch < Cfg::kChunks; ++ch)
+            tma_load_3d(sQ + qb * Cfg::kTileBytes + ch * Cfg::kRegion, &tq, &q_full[qb], ch * 64,
+                        c.it.kvh * g, c.it.b * Lq + c.it.l0);
+          ++q_issued;
         }
-        // the next item's Q: the buffer frees once this item's Q is in TMEM;
-        // issued between K / V loads as soon as that has happened
-        FwdItem nx{};
-        bool q_next = false;
-        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
-          const int cand = snake_item(kx);
-          if (cand >= n_items) continue;
-          nx = fwd_item(p, cand);
-          if (nx.n == 0) continue;
-          q_next = true;
-          break;
-        }
-        for (int j = 0; j < it.n; ++j) {
-          if (q_next && mbar_try_wait(q_empty, (qn - 1) & 1)) {
-            if (!load_q(nx)) { ok = false; break; }
-            q_next = false;
-          }
-          const int kt = static_cast<int>(static_cast<uint32_t>(it.list[j]) & kIndexMask);
-          const int krow = it.b * p.seq_len + kt * kTileN;
-          if (!acquire(sidx)) { ok = false; break; }
+        const int kt = static_cast<int>(static_cast<uint32_t>(c.it.list[c.j]) & kIndexMask);
+        const int krow = c.it.b * p.seq_len + kt * kTileN;
+        const int sl = c.t % NS;
+        const uint32_t ph = ((c.t / NS) & 1) ^ 1u;
+        uint64_t* full = do_k ? &k_full[sl] : &v_full[sl];
+        if (!mbar_wait(do_k ? &k_empty[sl] : &v_empty[sl], ph, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+        uint8_t* dst = do_k ? k_slot(c.t) : v_slot(c.t);
 #pragma unroll
-          for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tk, &slot_full[sidx % NS],
-                        it.kvh * D + c * 64, krow);
-          ++sidx;
-          if (!acquire(sidx)) { ok = false; break; }
-#pragma unroll
-          for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_2d(slot_ptr(sidx) + c * Cfg::kRegion, &tv, &slot_full[sidx % NS],
-                        it.kvh * D + c * 64, krow);
-          ++sidx;
-        }
-        if (ok && q_next && !load_q(nx)) ok = false;
+        for (int ch = 0; ch < Cfg::kChunks; ++ch)
+          tma_load_2d(dst + ch * Cfg::kRegion, do_k ? &tk : &tv, full, c.it.kvh * D + ch * 64, krow);
+        ++c.t;
+        if (++c.j == c.it.n) next_item(c);
       }
       if (!ok) {  // drain this CTA's copies still in flight
-        for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
-          drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
-        if (qn > 0) drain_wait(q_full, (qn - 1) & 1, 100000000ull);
+        for (int t = max(0, kc.t - NS); t < kc.t; ++t)
+          drain_wait(&k_full[t % NS], (t / NS) & 1, 100000000ull);
+        for (int t = max(0, vc.t - NS); t < vc.t; ++t)
+          drain_wait(&v_full[t % NS], (t / NS) & 1, 100000000ull);
+        for (int i = max(0, q_issued - 2); i < q_issued; ++i)
+          drain_wait(&q_full[i & 1], (i >> 1) & 1, 100000000ull);
       }
     }
   } else if (warp == 1 || warp == 3) {
     if (lane == 0) {
       // ------------------------------------------------------ MMA issuers
-      // warp 1: S_t = Q K_t^T into TMEM buffer t & 1 (A = Q from TMEM); the
-      // buffer is reused for S_{t+2} once P_t V_t (which reads P_t from it)
-      // has completed.  warp 3: once the softmax has written P_t over S_t:
-      // O += P_t V_t with A = P_t from TMEM.  Two issuing threads keep the
-      // tensor pipe fed while the softmax warps keep the schedulers busy.
+      // warp 1: S_t = Q K_t^T into TMEM buffer t % 3 (Q and K from shared
+      // memory); the buffer is reused for S_{t+3} once P_t V_t (which reads
+      // P_t from it) has completed.  warp 3: once the softmax has written P_t
+      // over S_t: O += P_t V_t with A = P_t from TMEM.  Two issuing threads
+      // keep the tensor pipe fed while the softmax warps keep the schedulers
+      // busy.
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
-      int sidx = 0, tbase = 0, ibase = 0;
+      int tbase = 0, ibase = 0;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
         const FwdItem it = fwd_item(p, item);
         if (it.n == 0) continue;
-        if (warp == 1 && !mbar_wait(&q_tmem[ibase & 1], (ibase >> 1) & 1, ctl)) { ok = false; break; }
+        const int qb = ibase & 1;
+        if (warp == 1 && !mbar_wait(&q_full[qb], (ibase >> 1) & 1, ctl)) { ok = false; break; }
+        const uint32_t q_addr = smem_u32(sQ + qb * Cfg::kTileBytes);
         for (int j = 0; j < it.n; ++j) {
-          const int t = tbase + j, sb = t & 1;
-          const int kidx = sidx + 2 * j, vidx = kidx + 1;
+          const int t = tbase + j, sb = t % 3;
+          const uint32_t use = (t / 3) & 1;  // parity of this use of buffer sb
+          const uint32_t kv_ph = (t / NS) & 1;
           if (warp == 1) {
-            if (!mbar_wait(&slot_full[kidx % NS], (kidx / NS) & 1, ctl)) { ok = false; break; }
-            if (t >= 2 && !mbar_wait(&o_done[sb], ((t - 2) >> 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&k_full[t % NS], kv_ph, ctl)) { ok = false; break; }
+            if (t >= 3 && !mbar_wait(&o_done[sb], use ^ 1u, ctl)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t k_addr = smem_u32(slot_ptr(kidx));
-            const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+            const uint32_t k_addr = smem_u32(k_slot(t));
+            const uint32_t d_s = tmem + 128 * sb;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_f16_ts(d_s, tmem + Cfg::kTmemQ + (ibase & 1) * (D / 2) + 8 * kk,
-                         sdesc_sw128(k_addr + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024),
-                         idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+              mma_bf16_ss(d_s, sdesc_sw128(q_addr + off, 16, 1024),
+                          sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&s_full[sb]);
-            mma_commit(&slot_empty[kidx % NS]);
+            mma_commit(&k_empty[t % NS]);
             last_commit = &s_full[sb];
-            last_parity = (t >> 1) & 1;
+            last_parity = use;
           } else {
             // the item's first P V overwrites O: the previous item's O must
             // have been read out by the epilogue warps
             if (j == 0 && ibase > 0 && !mbar_wait(o_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(&p_full[sb], (t >> 1) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(&slot_full[vidx % NS], (vidx / NS) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&p_full[sb], use, ctl)) { ok = false; break; }
+            if (!mbar_wait(&v_full[t % NS], kv_ph, ctl)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t v_addr = smem_u32(slot_ptr(vidx));
-            const uint32_t pb = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+            const uint32_t v_addr = smem_u32(v_slot(t));
+            const uint32_t pb = tmem + 128 * sb;
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
               mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
                          sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
                          (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&o_done[sb]);
-            mma_commit(&slot_empty[vidx % NS]);
+            mma_commit(&v_empty[t % NS]);
             last_commit = &o_done[sb];
-            last_parity = (t >> 1) & 1;
+            last_parity = use;
           }
         }
-        sidx += 2 * it.n;
+        if (!ok) break;
+        if (warp == 1) mma_commit(&q_empty[qb]);  // the item's Q reads are done once these complete
         tbase += it.n;
         ++ibase;
       }
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(512, 1)
     int tbase = 0, ibase = 0;
     // items in order, as staged by the epilogue warps (n == 0 ends the list)
     for (;;) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_tmem[ibase & 1], (ibase >> 1) & 1, ctl))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&meta_ready[ibase & 1], (ibase >> 1) & 1, ctl))) {
         ok = false;
         break;
       }
@@ -351,13 +367,13 @@ __global__ void __launch_bounds__(512, 1)
       float m_run = -INFINITY, l_run = 0.f;
       uint32_t e_next = static_cast<uint32_t>(meta[2]);
       for (int j = 0; j < it.n; ++j) {
-        const int t = tbase + j, sb = t & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (t >> 1) & 1, ctl))) {
+        const int t = tbase + j, sb = t % 3, xb = t & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (t / 3) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sc = tmem + lane_base + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0) + cw;
+        const uint32_t sc = tmem + lane_base + 128 * sb + cw;
         float s[64];
         {
           uint32_t u[64];
@@ -387,14 +403,14 @@ __global__ void __launch_bounds__(512, 1)
           mx3 = fmaxf(mx3, s[c + 3]);
         }
         float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-        xmax[(sb * 2 + w) * 128 + r] = mx;
+        xmax[(xb * 2 + w) * 128 + r] = mx;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&mx_ready[sb]);
-        if (!__all_sync(0xffffffffu, mbar_wait(&mx_ready[sb], (t >> 1) & 1, ctl))) {
+        if (lane == 0) mbar_arrive(&mx_ready[xb]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&mx_ready[xb], (t >> 1) & 1, ctl))) {
           ok = false;
           break;
         }
-        mx = fmaxf(mx, xmax[(sb * 2 + (w ^ 1)) * 128 + r]);
+        mx = fmaxf(mx, xmax[(xb * 2 + (w ^ 1)) * 128 + r]);
         const float mxl2 = mx * sl2;
         const float m_new = (mxl2 > m_run + 8.f) ? mxl2 : m_run;
         const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(512, 1)
           // the reference max moved: rescale this warpgroup's half of O
           // once P_{t-1} V_{t-1} is in
           if (!__all_sync(0xffffffffu,
-                          mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, ctl))) {
+                          mbar_wait(&o_done[(t - 1) % 3], ((t - 1) / 3) & 1, ctl))) {
             ok = false;
             break;
           }
@@ -466,8 +482,8 @@ __global__ void __launch_bounds__(512, 1)
     // the row statistics, read O out of TMEM (row r = lane of warp w - 12),
     // hand the accumulator back, then write O / l (per warp, TMA stores of
     // 32 x 32 fp32 blocks) and the LSE; this overlaps the next item's tiles.
-    // Ahead of that, the warps copy the next item's Q into the other TMEM Q
-    // buffer and stage its metadata for the softmax warps.
+    // Ahead of that, the warps stage the next item's metadata for the
+    // softmax warps.
     const int wq = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int lg = 31 - __clz(g);
@@ -477,10 +493,6 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t stage = smem_u32(smem + Cfg::kStage) + wq * 4096;
     bool ok = true;
     int tbase = 0, ibase = 0;
-    // row r of an item's Q (slot q_idx) into TMEM Q buffer qb.  Buffer qb was
-    // last used by the item two back, whose products completed before its
-    // epilogue, which these warps have done.
-    int qn = 0;  // Q tiles copied so far (the q_full / q_empty phase)
     // stage item `mi`'s metadata for the softmax warps into buffer qb (the
     // softmax warps read buffer qb at the top of the item two back, which
     // they have finished); n = 0 marks the end of this CTA's items
@@ -499,15 +511,9 @@ __global__ void __launch_bounds__(512, 1)
         meta[2] = mi->list[0];
       }
     };
-    auto copy_q = [&](int qb, const FwdItem& mi) -> bool {
-      stage_meta(qb, &mi);
-      if (!__all_sync(0xffffffffu, mbar_wait(q_full, qn & 1, ctl))) return false;
-      sw128_row_to_tmem<D>(smem_u32(sQ), r, tmem + lane_base + Cfg::kTmemQ + qb * (D / 2));
-      tmem_wait_st();
-      warp_arrive(&q_tmem[qb]);
-      warp_arrive(q_empty);
-      ++qn;
-      return true;
+    auto post_meta = [&](int qb, const FwdItem* mi) {
+      stage_meta(qb, mi);
+      warp_arrive(&meta_ready[qb]);
     };
     bool first = true;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
@@ -516,11 +522,11 @@ __global__ void __launch_bounds__(512, 1)
       const FwdItem it = fwd_item(p, item);
       if (it.n == 0) continue;
       if (first) {
-        if (!copy_q(ibase & 1, it)) { ok = false; break; }
+        post_meta(ibase & 1, &it);
         first = false;
       }
-      // the next item's Q into the other buffer as soon as it has landed, so
-      // that the S products run on into the next item without a gap
+      // the next item's metadata into the other buffer, so that the softmax
+      // warps run on into the next item without a gap
       {
         bool more = false;
         for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
@@ -528,20 +534,16 @@ __global__ void __launch_bounds__(512, 1)
           if (cand >= n_items) continue;
           const FwdItem nx = fwd_item(p, cand);
           if (nx.n == 0) continue;
-          if (!copy_q((ibase + 1) & 1, nx)) ok = false;
+          post_meta((ibase + 1) & 1, &nx);
           more = true;
           break;
         }
-        if (!ok) break;
-        if (!more) {  // end of this CTA's items
-          stage_meta((ibase + 1) & 1, nullptr);
-          warp_arrive(&q_tmem[(ibase + 1) & 1]);
-        }
+        if (!more) post_meta((ibase + 1) & 1, nullptr);  // end of this CTA's items
       }
       const int t_last = tbase + it.n - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
           !__all_sync(0xffffffffu,
-                      mbar_wait(&o_done[t_last & 1], (t_last >> 1) & 1, ctl))) {
+                      mbar_wait(&o_done[t_last % 3], (t_last / 3) & 1, ctl))) {
         ok = false;
         break;
       }
@@ -584,10 +586,7 @@ __global__ void __launch_bounds__(512, 1)
       tbase += it.n;
       ++ibase;
     }
-    if (ok && first) {  // no items at all: release the softmax warps
-      stage_meta(0, nullptr);
-      warp_arrive(&q_tmem[0]);
-    }
+    if (ok && first) post_meta(0, nullptr);  // no items at all: release the softmax warps
     if (lane == 0) bulk_wait_all();
   }
 
