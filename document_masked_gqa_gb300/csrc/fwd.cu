@@ -394,15 +394,18 @@ __global__ void __launch_bounds__(512, 1)
           for (int c = 0; c < 64; ++c)
             if (c < lo_c || c > hi_c) s[c] = -INFINITY;
         }
+        // row max of this half: three-input maxima, four chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < 64; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < 60; c += 8) {
+          mx0 = max3f(mx0, s[c], s[c + 1]);
+          mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+          mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+          mx3 = max3f(mx3, s[c + 6], s[c + 7]);
         }
-        float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        mx0 = max3f(mx0, s[60], s[61]);
+        mx1 = max3f(mx1, s[62], s[63]);
+        float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
         xmax[(xb * 2 + w) * 128 + r] = mx;
         __syncwarp();
         if (lane == 0) mbar_arrive(&mx_ready[xb]);
