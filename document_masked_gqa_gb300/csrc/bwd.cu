@@ -16,10 +16,10 @@
 //                 memory; the item walks the column list of query tiles (all
 //                 g heads of the group packed in each 128-row tile, so the
 //                 GQA reduction over the group happens inside the
-//                 accumulation), each done in two 64-row half steps shared by
-//                 two element-wise warpgroups; dV, dK accumulate in TMEM.
+//                 accumulation), a whole 128-row query tile per step shared
+//                 by two element-wise warpgroups; dV, dK accumulate in TMEM.
 //   dq_kernel     work item = (query tile, K/V head): Q and dO are copied into
-//                 TMEM; the item walks the row list of key tiles; S, dP and
+//                 TMEM (tcgen05.cp by the S and dP issuers); the item walks the row list of key tiles; S, dP and
 //                 the dQ accumulator in TMEM; four row warpgroups split each
 //                 tile's key columns.
 // Both attention kernels are persistent (one CTA per SM) with one TMA
@@ -684,7 +684,7 @@ struct DqCfg {
   static constexpr int kSlots = (D == 128) ? 6 : 8;
   static constexpr int kDS = kSlots * kTile;     // dS (128 x 128 bf16)
   static constexpr int kBar = kDS + 128 * 128 * 2;
-  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kNumBars = 2 * kSlots + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -718,7 +718,7 @@ __device__ __forceinline__ DqItem dq_item(const PlanDev& p, int item) {
 // every role keeps identically across items: the stream index of the next
 // slot load (sidx), the number of key tiles processed so far (tbase, which
 // fixes the parity of every per-tile barrier) and the number of non-empty
-// items so far (ibase, the parity of qd_tmem).
+// items so far (ibase, the parity of epi_full and epi_free).
 template <int D>
 __global__ void __launch_bounds__(640, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -751,9 +751,8 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* dp_free = s_full + 3;       // the row warps have read dP
   uint64_t* ds_full = s_full + 4;       // dS written to shared memory
   uint64_t* ds_done = s_full + 5;       // dQ += dS K done reading dS
-  uint64_t* qd_tmem = s_full + 6;       // Q and dO of an item copied into TMEM
-  uint64_t* epi_full = s_full + 7;      // an item's dQ tile staged in the dS buffer
-  uint64_t* epi_free = s_full + 8;      // its store has read the dS buffer
+  uint64_t* epi_full = s_full + 6;      // an item's dQ tile staged in the dS buffer
+  uint64_t* epi_free = s_full + 7;      // its store has read the dS buffer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTile; };
@@ -763,14 +762,13 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&slot_full[i], 1);
       mbar_init(&slot_empty[i], 1);
     }
-    // the row warps arrive once per warp: 16 warps, of which the first 8 copy Q / dO
+    // the row warps arrive once per warp
     mbar_init(s_full, 1);
     mbar_init(s_free, 16);
     mbar_init(dp_full, 1);
     mbar_init(dp_free, 16);
     mbar_init(ds_full, 16);
     mbar_init(ds_done, 1);
-    mbar_init(qd_tmem, 8);
     mbar_init(epi_full, 16);
     mbar_init(epi_free, 1);
     *abort_flag = 0;
@@ -861,12 +859,24 @@ __global__ void __launch_bounds__(640, 1)
         const DqItem it = dq_item(p, item);
         if (it.n == 0) continue;
         if (warp == 1 || warp == 2) {
-          if (!mbar_wait(qd_tmem, ibase & 1, ctl)) { ok = false; break; }
-          // Q and dO are in TMEM: their slots go back to the producer
-          if (warp == 1) {
-            mbar_arrive(&slot_empty[sidx % NS]);
-            mbar_arrive(&slot_empty[(sidx + 1) % NS]);
+          // the item's Q (warp 1) or dO (warp 2) into TMEM by tcgen05.cp,
+          // once the previous item's last S (or dP) has read the old one; the
+          // copy is ordered before this thread's next MMAs, and the slot goes
+          // back to the producer when it completes
+          const int cidx = sidx + (warp == 1 ? 0 : 1);
+          if (tbase > 0 && !mbar_wait(warp == 1 ? s_full : dp_full, (tbase - 1) & 1, ctl)) {
+            ok = false;
+            break;
           }
+          if (!mbar_wait(&slot_full[cidx % NS], (cidx / NS) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t src = smem_u32(slot_ptr(cidx));
+          const uint32_t dst_t = tmem + (warp == 1 ? Cfg::kTmemQ : Cfg::kTmemDO);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tmem_cp_128x256b(dst_t + 8 * kk,
+                             sdesc_sw128(src + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024));
+          mma_commit(&slot_empty[cidx % NS]);
         }
         for (int j = 0; j < it.n; ++j) {
           const int t = tbase + j;
@@ -956,8 +966,15 @@ __global__ void __launch_bounds__(640, 1)
     const int ch0 = (q & 1) * 4;
     constexpr int DQ = D / 4;  // head_dim columns of dQ this warpgroup writes
     bool ok = true;
-    int sidx = 0, tbase = 0, ibase = 0;
-    int copied = -1;  // item whose Q / dO are already in TMEM
+    int tbase = 0, ibase = 0;
+    // this row's data of the next item, loaded at the end of the previous
+    // one so that the loads overlap its epilogue
+    int pf_item = -1, pf_lo = 0;
+    float pf_lse = 0.f, pf_del = 0.f;
+    uint32_t pf_e0 = 0;
+    auto row_stat = [&](const DqItem& di) -> long long {
+      return (static_cast<long long>(di.b) * p.n_heads + di.kvh * g + h) * Lq + di.l0 + pos;
+    };
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
@@ -973,24 +990,12 @@ __global__ void __launch_bounds__(640, 1)
       }
       const int qabs =
           (l < C) ? (p.cp_rank * C + l) : ((2 * p.cp_size - 1 - p.cp_rank) * C + l - C);
-      const int lo_r = p.doc_lo[static_cast<long long>(it.b) * Lq + l];
-      const long long stat = (static_cast<long long>(it.b) * p.n_heads + hq) * Lq + l;
-      const float lse2 = lse[stat] * kLog2e;
-      const float del = p.delta[stat];
-      // warpgroup 0 copies the Q tile into TMEM, warpgroup 1 the dO tile
-      // (the previous item's S and dP products have all completed); after
-      // the first item this happened already, ahead of the previous epilogue
-      auto copy_qdo = [&](int slot_idx) -> bool {
-        const int idx = slot_idx + q;
-        if (!warp_wait(&slot_full[idx % NS], (idx / NS) & 1, ctl)) return false;
-        sw128_row_to_tmem<D>(smem_u32(slot_ptr(idx)), r,
-                             tmem + lane_base + (q ? Cfg::kTmemDO : Cfg::kTmemQ));
-        tmem_wait_st();
-        warp_arrive(qd_tmem);
-        return true;
-      };
-      if (q < 2 && copied != item && !copy_qdo(sidx)) { ok = false; break; }
-      uint32_t e_next = static_cast<uint32_t>(it.list[0]);
+      const bool pf = pf_item == item;
+      const long long stat = row_stat(it);
+      const int lo_r = pf ? pf_lo : p.doc_lo[static_cast<long long>(it.b) * Lq + l];
+      const float lse2 = (pf ? pf_lse : lse[stat]) * kLog2e;
+      const float del = pf ? pf_del : p.delta[stat];
+      uint32_t e_next = pf ? pf_e0 : static_cast<uint32_t>(it.list[0]);
       for (int j = 0; j < it.n; ++j) {
         const int t = tbase + j;
         const uint32_t e = e_next;  // list entries run one tile ahead
@@ -1059,21 +1064,27 @@ __global__ void __launch_bounds__(640, 1)
         if (lane == 0) mbar_arrive(ds_full);
       }
       if (!ok) break;
-      // the last S and dP of this item have been read: bring in the next
-      // non-empty item's Q and dO now, so that its first products overlap
-      // this epilogue
+      // the next non-empty item's row data: loaded now, used after this
+      // epilogue
       {
         int nx = n_items;
+        DqItem nit{};
         for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
           const int cand = snake_item(kx);
-          if (cand < n_items && dq_item(p, cand).n != 0) {
+          if (cand >= n_items) continue;
+          nit = dq_item(p, cand);
+          if (nit.n != 0) {
             nx = cand;
             break;
           }
         }
         if (nx < n_items) {
-          if (q < 2 && !copy_qdo(sidx + 2 + 2 * it.n)) { ok = false; break; }
-          copied = nx;
+          const long long nstat = row_stat(nit);
+          pf_lo = p.doc_lo[static_cast<long long>(nit.b) * Lq + nit.l0 + pos];
+          pf_lse = lse[nstat];
+          pf_del = p.delta[nstat];
+          pf_e0 = static_cast<uint32_t>(nit.list[0]);
+          pf_item = nx;
         }
       }
       // epilogue: dQ (scaled, bf16) staged in the dS buffer in the layout of
@@ -1108,7 +1119,6 @@ __global__ void __launch_bounds__(640, 1)
       // the next item's first dQ product overwrites the accumulator only
       // after every warp has arrived on ds_full for it, i.e. after this read
       warp_arrive(epi_full);
-      sidx += 2 + 2 * it.n;
       tbase += it.n;
       ++ibase;
     }

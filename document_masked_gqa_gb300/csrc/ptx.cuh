@@ -337,6 +337,16 @@ __device__ __forceinline__ void sw128_row_to_tmem(uint32_t tile, int r, uint32_t
   }
 }
 
+// Asynchronous copy of 128 rows x 32 bytes from shared memory (described
+// like an MMA operand: `desc`) into 8 TMEM columns at `taddr`, lane = row.
+// With a 128-byte-swizzled K-major descriptor of a 16-deep step it yields the
+// TMEM A-operand layout of that step (16-bit pairs, even element low).
+// Ordered before later tcgen05.mma of the same thread; tracked by
+// tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
 // Half `half` (0 or 1) of the same copy: 16-byte chunk pairs
 // [half * D/32, (half + 1) * D/32) of the row, so that two warpgroups can
 // share it.
