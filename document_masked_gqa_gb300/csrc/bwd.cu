@@ -972,13 +972,14 @@ __global__ void __launch_bounds__(640, 1)
     int pf_item = -1, pf_lo = 0;
     float pf_lse = 0.f, pf_del = 0.f;
     uint32_t pf_e0 = 0;
+    DqItem pf_it{};  // the next item's descriptor, from the same lookup
     auto row_stat = [&](const DqItem& di) -> long long {
       return (static_cast<long long>(di.b) * p.n_heads + di.kvh * g + h) * Lq + di.l0 + pos;
     };
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
-      const DqItem it = dq_item(p, item);
+      const DqItem it = (item == pf_item) ? pf_it : dq_item(p, item);
       const int l = it.l0 + pos;
       const int hq = it.kvh * g + h;
       uint4* dst = reinterpret_cast<uint4*>(
@@ -1084,6 +1085,7 @@ __global__ void __launch_bounds__(640, 1)
           pf_lse = lse[nstat];
           pf_del = p.delta[nstat];
           pf_e0 = static_cast<uint32_t>(nit.list[0]);
+          pf_it = nit;
           pf_item = nx;
         }
       }
