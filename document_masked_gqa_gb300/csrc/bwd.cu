@@ -167,7 +167,7 @@ struct DkdvCfg {
   static constexpr int kStage = kDO + 2 * kTile;
   static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
   static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 20;
+  static constexpr int kNumBars = 22;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -233,14 +233,16 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* do_empty = bars + 7;   // [2]
   uint64_t* s_full = bars + 9;     // S^T of the current tile computed
   uint64_t* dp_full = bars + 10;   // dP^T computed
-  uint64_t* p_full = bars + 11;    // P^T written over S^T
-  uint64_t* ds_full = bars + 12;   // dS^T written over dP^T
-  uint64_t* dv_done = bars + 13;   // dV += P^T dO done (the S^T buffer is free)
-  uint64_t* dk_done = bars + 14;   // dK += dS^T Q done (the dP^T buffer is free)
-  uint64_t* col_ready = bars + 15; // [2] per warpgroup: statistics staged
-  uint64_t* acc_done = bars + 17;  // an item's dV, dK complete
-  uint64_t* kv_empty = bars + 18;  // an item's last S^T and dP^T done (two commits)
-  uint64_t* acc_free = bars + 19;  // the epilogue warps have read an item's dV, dK
+  // P^T (dS^T) written over S^T (dP^T), per half: query columns [0, 32) and
+  // [64, 96) of the tile (each warpgroup's first 32), then the rest
+  uint64_t* p_full = bars + 11;    // [2]
+  uint64_t* ds_full = bars + 13;   // [2]
+  uint64_t* dv_done = bars + 15;   // dV += P^T dO done (the S^T buffer is free)
+  uint64_t* dk_done = bars + 16;   // dK += dS^T Q done (the dP^T buffer is free)
+  uint64_t* col_ready = bars + 17; // [2] per warpgroup: statistics staged
+  uint64_t* acc_done = bars + 19;  // an item's dV, dK complete
+  uint64_t* kv_empty = bars + 20;  // an item's last S^T and dP^T done (two commits)
+  uint64_t* acc_free = bars + 21;  // the epilogue warps have read an item's dV, dK
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -252,11 +254,11 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
       mbar_init(&col_ready[i], 4);  // the four warps of the warpgroup
+      mbar_init(&p_full[i], 8);     // one arrival per element-wise warp
+      mbar_init(&ds_full[i], 8);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 8);   // one arrival per element-wise warp
-    mbar_init(ds_full, 8);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
@@ -350,14 +352,20 @@ __global__ void __launch_bounds__(512, 1)
       bool pk_first = false, pk_last = false;
       int acc_items = 0;  // acc_done phases committed
       auto issue_dk = [&]() -> bool {
-        if (!mbar_wait(ds_full, pk & 1, ctl)) return false;
-        tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ + (pk & 1) * Cfg::kTile);
+        // each half as soon as it is written: steps kk = 4w + 2h + {0, 1}
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
-                     sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                     (!pk_first || kk > 0) ? 1u : 0u);
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&ds_full[h], pk & 1, ctl)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
+            mma_f16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                       sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                       (!pk_first || kk > 0) ? 1u : 0u);
+          }
+        }
         mma_commit(dk_done);
         // dV(pk) is known complete (dv_done was awaited): Q, dO of tile pk
         // are free once dK(pk) is, and so is the item's accumulator pair
@@ -469,19 +477,26 @@ __global__ void __launch_bounds__(512, 1)
         if (it.n == 0) continue;
         for (int i = 0; i < it.n; ++i) {
           const int ig = tbase + i, st = ig & 1;
-          if (!mbar_wait(p_full, ig & 1, ctl)) { ok = false; break; }
           // the item's first products overwrite dV, dK: the previous item's
           // must have been read out by the epilogue warps
           if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
           // P^T follows from Q alone: dO may still be on its way
           if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
           const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
+          // each half of P^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + 64 * (kk >> 2) + 8 * (kk & 3),
-                       sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(&p_full[h], ig & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
+              mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + 64 * (kk >> 2) + 8 * (kk & 3),
+                         sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
           mma_commit(dv_done);
           last_commit = dv_done;
           last_parity = ig & 1;
@@ -566,20 +581,22 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld();
           reg_fence32(su);
           reg_fence32(su + 32);
-          if (masked) {
-            p_chunk32<true>(su, nlse_c, range_bits(lo_c - 64 * w, hi_c - 64 * w), sl2, pb);
-            p_chunk32<true>(su + 32, nlse_c + 8, range_bits(lo_c - 64 * w - 32, hi_c - 64 * w - 32),
-                            sl2, pb + 16);
-          } else {
-            p_chunk32<false>(su, nlse_c, 0u, sl2, pb);
-            p_chunk32<false>(su + 32, nlse_c + 8, 0u, sl2, pb + 16);
+          // each half (32 columns) is written over the first 16 of the S^T
+          // columns and handed to dV as soon as it is done
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (masked)
+              p_chunk32<true>(su + 32 * h, nlse_c + 8 * h,
+                              range_bits(lo_c - 64 * w - 32 * h, hi_c - 64 * w - 32 * h), sl2,
+                              pb + 16 * h);
+            else
+              p_chunk32<false>(su + 32 * h, nlse_c + 8 * h, 0u, sl2, pb + 16 * h);
+            tmem_st8_nowait(s_cols + 16 * h, pb + 16 * h);
+            tmem_st8_nowait(s_cols + 16 * h + 8, pb + 16 * h + 8);
+            tmem_wait_st();
+            warp_arrive(&p_full[h]);
           }
         }
-        // over the first 32 of the S^T columns
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_st8_nowait(s_cols + 8 * c, pb + 8 * c);
-        tmem_wait_st();
-        warp_arrive(p_full);
         // phase 2: dS^T over dP^T
         if (!warp_wait(dp_full, ig & 1, ctl)) { ok = false; break; }
         tc_fence_after();
@@ -590,14 +607,16 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld();
           reg_fence32(du);
           reg_fence32(du + 32);
-          uint32_t pd[32];
-          ds_chunk32(du, pb, del_c, pd);
-          ds_chunk32(du + 32, pb + 16, del_c + 8, pd + 16);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st8_nowait(dp_cols + 8 * c, pd + 8 * c);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pd[16];
+            ds_chunk32(du + 32 * h, pb + 16 * h, del_c + 8 * h, pd);
+            tmem_st8_nowait(dp_cols + 16 * h, pd);
+            tmem_st8_nowait(dp_cols + 16 * h + 8, pd + 8);
+            tmem_wait_st();
+            warp_arrive(&ds_full[h]);
+          }
         }
-        tmem_wait_st();
-        warp_arrive(ds_full);
       }
       tbase += it.n;
     }
