@@ -42,7 +42,18 @@ UNIT = "TFLOP/s"
 DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, NVIDIA's figure without sparsity
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_RANK_STEP = 12  # plan: 7, forward: 2 (V to fp16, attention), backward: 3
+PLAN_SORT_MAX = 2048  # launch orders up to this many units are sorted inside the scan kernel
+
+
+def kernels_per_rank_step(w) -> int:
+    """Kernels one rank's step launches: the planner's four (positions,
+    block classes, scans + launch orders, lists) plus one per launch order
+    too long for the in-block sort, the forward's two (V to fp16,
+    attention) and the backward's three (Delta, dK/dV, dQ)."""
+    g = w.n_heads // w.n_kv_heads
+    nq = w.batch * ((w.seq_len // w.cp_size) // (128 // g))
+    nk = w.batch * (w.seq_len // 128)
+    return 4 + int(nq > PLAN_SORT_MAX) + int(nk > PLAN_SORT_MAX) + 2 + 3
 
 
 # ------------------------------------------------------------------ counting
@@ -447,7 +458,7 @@ def run_gpu(args, w: wl.Workload):
             "pct_of_measured_peak": 100.0 * value / world / peak,
             "pct_of_datasheet_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_RANK_STEP * len(w.ranks) * args.steps,
+            "gpu_launches": kernels_per_rank_step(w) * len(w.ranks) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -19,9 +19,9 @@
 //                 accumulation), a whole 128-row query tile per step shared
 //                 by two element-wise warpgroups; dV, dK accumulate in TMEM.
 //   dq_kernel     work item = (query tile, K/V head): Q and dO are copied into
-//                 TMEM (tcgen05.cp by the S and dP issuers); the item walks the row list of key tiles; S, dP and
-//                 the dQ accumulator in TMEM; four row warpgroups split each
-//                 tile's key columns.
+//                 TMEM (tcgen05.cp by the S and dP issuers); the item walks
+//                 the row list of key tiles; S, dP and the dQ accumulator in
+//                 TMEM; four row warpgroups split each tile's key columns.
 // Both attention kernels are persistent (one CTA per SM) with one TMA
 // producer thread, one tcgen05-issuing thread per product on its own warp,
 // element-wise warpgroups and an epilogue that overlaps the next item;

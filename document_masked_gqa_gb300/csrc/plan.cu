@@ -51,6 +51,9 @@ __global__ void plan_positions_kernel(PlanDev p, const int32_t* __restrict__ cu,
     if (cu[lo] != want) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_BAD_DOCS));
   }
 
+  // --- column counts start at zero (the block-mask builder adds to them)
+  for (int i = tid; i < p.batch * p.n_ktiles; i += nthreads) p.col_cnt[i] = 0;
+
   // --- chunk order (rank-major) and position map
   for (int j = tid; j < 2 * p.cp_size; j += nthreads)
     p.chunk_order[j] = (j & 1) ? (2 * p.cp_size - 1 - (j >> 1)) : (j >> 1);
@@ -154,9 +157,16 @@ __device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
   return incl - v;
 }
 
-// one block of 1024: exclusive scans of the row and column counts
-__global__ void scan_kernel(PlanDev p) {
+constexpr int kSortMax = 2048;  // units the one-block sort of the launch orders takes
+
+// one block of 1024: exclusive scans of the row and column counts, then the
+// longest-first launch orders of rows and columns when they have at most
+// kSortMax units (order_kernel takes larger ones).  The order sorts the keys
+// (INT_MAX - count, index) ascending with a bitonic network in shared
+// memory: longer lists first, ties by ascending index.
+__global__ void scan_order_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
+  __shared__ unsigned long long s_key[kSortMax];
   for (int which = 0; which < 2; ++which) {
     const int n = which == 0 ? p.batch * p.n_qtiles : p.batch * p.n_ktiles;
     const int32_t* cnt = which == 0 ? p.row_cnt : p.col_cnt;
@@ -172,13 +182,41 @@ __global__ void scan_kernel(PlanDev p) {
     }
     if (threadIdx.x == 0) ptr[n] = carry;
     __syncthreads();
+    if (n > kSortMax) continue;  // uniform across the block
+    int32_t* order = which == 0 ? p.fwd_order : p.bwd_order;
+    int npow = 1;
+    while (npow < n) npow <<= 1;
+    for (int i = threadIdx.x; i < npow; i += blockDim.x)
+      s_key[i] = (i < n) ? ((static_cast<unsigned long long>(0x7FFFFFFF - cnt[i]) << 32) |
+                            static_cast<unsigned int>(i))
+                         : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= npow; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long a = s_key[i], b = s_key[ixj];
+            if ((a > b) == ((i & k) == 0)) {
+              s_key[i] = b;
+              s_key[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      order[i] = static_cast<int32_t>(s_key[i] & 0xFFFFFFFFull);
+    __syncthreads();
   }
 }
 
-// grid (n_qtiles, batch) for rows or (n_ktiles, batch) for columns; block 1024
-__global__ void fill_lists_kernel(PlanDev p, int columns) {
+// grid (n_qtiles + n_ktiles, batch): row lists, then column lists; block 1024
+__global__ void fill_lists_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
-  const int line = blockIdx.x, b = blockIdx.y;
+  const int columns = blockIdx.x >= p.n_qtiles;
+  const int line = columns ? blockIdx.x - p.n_qtiles : blockIdx.x, b = blockIdx.y;
   const int n = columns ? p.n_qtiles : p.n_ktiles;
   const long long stride = columns ? p.n_ktiles : 1;
   const uint8_t* base =
@@ -255,20 +293,17 @@ cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t) * 4, s);
   if (e != cudaSuccess) return e;
   if (p.batch == 0) return cudaSuccess;
-  e = cudaMemsetAsync(p.col_cnt, 0, sizeof(int32_t) * p.batch * p.n_ktiles, s);
-  if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(p.batch) * p.seq_len;
   int blocks = static_cast<int>((n + 255) / 256);
   if (blocks > 4 * pl.num_sms) blocks = 4 * pl.num_sms;
   if (blocks < 1) blocks = 1;
   plan_positions_kernel<<<blocks, 256, 0, s>>>(p, pl.cu, pl.n_docs);
   mask_classify_kernel<<<dim3(p.n_qtiles, p.batch), 128, 0, s>>>(p);
-  scan_kernel<<<1, 1024, 0, s>>>(p);
-  fill_lists_kernel<<<dim3(p.n_qtiles, p.batch), 1024, 0, s>>>(p, 0);
-  fill_lists_kernel<<<dim3(p.n_ktiles, p.batch), 1024, 0, s>>>(p, 1);
+  scan_order_kernel<<<1, 1024, 0, s>>>(p);
   const int nq = p.batch * p.n_qtiles, nk = p.batch * p.n_ktiles;
-  order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
-  order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
+  if (nq > kSortMax) order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
+  if (nk > kSortMax) order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
+  fill_lists_kernel<<<dim3(p.n_qtiles + p.n_ktiles, p.batch), 1024, 0, s>>>(p);
   return cudaGetLastError();
 }
 
