@@ -159,15 +159,16 @@ __device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
 
 constexpr int kSortMax = 2048;  // units the one-block sort of the launch orders takes
 
-// one block of 1024: exclusive scans of the row and column counts, then the
-// longest-first launch orders of rows and columns when they have at most
-// kSortMax units (order_kernel takes larger ones).  The order sorts the keys
+// two blocks of 1024, block 0 for the rows and block 1 for the columns:
+// exclusive scan of the counts, then the longest-first launch order when
+// there are at most kSortMax units (order_kernel takes larger ones).  The order sorts the keys
 // (INT_MAX - count, index) ascending with a bitonic network in shared
 // memory: longer lists first, ties by ascending index.
 __global__ void scan_order_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
   __shared__ unsigned long long s_key[kSortMax];
-  for (int which = 0; which < 2; ++which) {
+  {
+    const int which = blockIdx.x;
     const int n = which == 0 ? p.batch * p.n_qtiles : p.batch * p.n_ktiles;
     const int32_t* cnt = which == 0 ? p.row_cnt : p.col_cnt;
     int32_t* ptr = which == 0 ? p.row_ptr : p.col_ptr;
@@ -182,7 +183,7 @@ __global__ void scan_order_kernel(PlanDev p) {
     }
     if (threadIdx.x == 0) ptr[n] = carry;
     __syncthreads();
-    if (n > kSortMax) continue;  // uniform across the block
+    if (n > kSortMax) return;  // uniform across the block
     int32_t* order = which == 0 ? p.fwd_order : p.bwd_order;
     int npow = 1;
     while (npow < n) npow <<= 1;
@@ -299,7 +300,7 @@ cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   if (blocks < 1) blocks = 1;
   plan_positions_kernel<<<blocks, 256, 0, s>>>(p, pl.cu, pl.n_docs);
   mask_classify_kernel<<<dim3(p.n_qtiles, p.batch), 128, 0, s>>>(p);
-  scan_order_kernel<<<1, 1024, 0, s>>>(p);
+  scan_order_kernel<<<2, 1024, 0, s>>>(p);
   const int nq = p.batch * p.n_qtiles, nk = p.batch * p.n_ktiles;
   if (nq > kSortMax) order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
   if (nk > kSortMax) order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
