@@ -266,12 +266,6 @@ __device__ __forceinline__ void reg_fence16(uint32_t* r) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
-// Orders the computation of r[0..7] before any later volatile asm (such as
-// the next chunk's tensor-memory loads), bounding the registers in flight.
-__device__ __forceinline__ void reg_fence8(uint32_t* r) {
-  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-               "+r"(r[6]), "+r"(r[7]));
-}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -314,29 +308,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 
 // ---------------------------------------------------------------- descriptors
 
-// Row r of a 128-row tile (K-major, 128-byte swizzled, D/64 regions of 16 KB)
-// into TMEM lane r as packed 16-bit pairs: columns [0, D/2).  The caller
-// waits for the stores (tmem_wait_st).
-template <int D>
-__device__ __forceinline__ void sw128_row_to_tmem(uint32_t tile, int r, uint32_t taddr) {
-#pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-#pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      uint32_t w[8];
-      const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
-      const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                   : "r"(a0));
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                   : "r"(a1));
-      tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
-    }
-  }
-}
-
 // Asynchronous copy of 128 rows x 32 bytes from shared memory (described
 // like an MMA operand: `desc`) into 8 TMEM columns at `taddr`, lane = row.
 // With a 128-byte-swizzled K-major descriptor of a 16-deep step it yields the
@@ -345,30 +316,6 @@ __device__ __forceinline__ void sw128_row_to_tmem(uint32_t tile, int r, uint32_t
 // tcgen05.commit.
 __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
-// Half `half` (0 or 1) of the same copy: 16-byte chunk pairs
-// [half * D/32, (half + 1) * D/32) of the row, so that two warpgroups can
-// share it.
-template <int D>
-__device__ __forceinline__ void sw128_row_to_tmem_half(uint32_t tile, int r, uint32_t taddr,
-                                                       int half) {
-  constexpr int kPairs = (D / 64) * 4;
-#pragma unroll
-  for (int i = 0; i < kPairs / 2; ++i) {
-    const int pi = half * (kPairs / 2) + i;
-    const int c = pi >> 2, k = 2 * (pi & 3);
-    uint32_t w[8];
-    const uint32_t a0 = tile + c * 16384 + r * 128 + (((k ^ (r & 7))) << 4);
-    const uint32_t a1 = tile + c * 16384 + r * 128 + ((((k + 1) ^ (r & 7))) << 4);
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                 : "r"(a0));
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "r"(a1));
-    tmem_st8_nowait(taddr + 32 * c + 4 * k, w);
-  }
 }
 
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
@@ -476,7 +423,5 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d)
                : "memory");
 }
-
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 }  // namespace dma

@@ -23,13 +23,24 @@ EDGE = {
 }
 
 
+# plan-only cases whose launch orders have more than 2048 units (rows: 4096
+# query tiles of 8 positions; rows and columns: 17 samples x 128 tiles), which
+# the planner orders with its separate ranking kernel
+LONG_ORDERS = {
+    "long-row-order": wl.custom("long-row-order", 32768, 1, 1, 16, 1, 64, "uniform", 64, 4096,
+                                seed=14),
+    "long-col-order": wl.custom("long-col-order", 16384, 1, 17, 2, 2, 64, "uniform", 64, 4096,
+                                seed=15),
+}
+
+
 def _cases():
     out = []
     for name in ["tiny", "8b", "70b", "sparse", "405b-logu", "405b-1doc"]:
         w = wl.WORKLOADS[name]
         for r in w.ranks:
             out.append((name, w, r))
-    for name, w in EDGE.items():
+    for name, w in list(EDGE.items()) + list(LONG_ORDERS.items()):
         for r in w.ranks:
             out.append((name, w, r))
     return out
