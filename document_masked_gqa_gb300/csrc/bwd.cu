@@ -151,8 +151,10 @@ __device__ __forceinline__ void ds_chunk32(const uint32_t* du, const uint32_t* p
 // columns [64w, 64w + 64)) first turn S^T into P^T and write it (bf16 pairs)
 // over the S^T columns they read, so that dV += P^T dO can start while
 // dP^T is still being computed; then they turn dP^T into dS^T the same way
-// for dK += dS^T Q.  A buffer is rewritten once the product that reads it
-// is done: S^T after dV, dP^T after dK.
+// for dK += dS^T Q.  Both are handed over in two halves (each warpgroup's
+// first 32 query columns, then the rest), so that dV and dK start on the
+// first half while the second is computed.  A buffer is rewritten once the
+// product that reads it is done: S^T after dV, dP^T after dK.
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;
