@@ -1,0 +1,110 @@
+"""CP load-balance report (document_masked_gqa_gb300.balance) against the
+oracle's per-position pair counts, a hand-worked example, and properties:
+the pages' chunk pairing balances a single document exactly, and the
+document-aware alternative never balances worse."""
+import numpy as np
+import pytest
+
+from document_masked_gqa_gb300 import balance
+from document_masked_gqa_gb300 import workloads as wl
+from oracle import cp as ocp
+from oracle import flops as ofl
+
+NAMES = ["tiny", "8b", "70b", "sparse", "405b-logu", "405b-1doc"]
+
+
+def _explicit_rank_pairs(cu, batch, seq_len, cp_size, bounds):
+    """Oracle-side count for arbitrary chunk bounds: sum over the rank's query
+    positions of (position - start of its document + 1)."""
+    start = ocp.doc_start(cu, batch, seq_len)
+    n = 2 * cp_size
+    out = np.zeros((cp_size, batch), dtype=np.int64)
+    for b in range(batch):
+        e = bounds[b]
+        for r in range(cp_size):
+            pos = np.r_[e[r]:e[r + 1], e[n - 1 - r]:e[n - r]]
+            out[r, b] = int((pos - start[b, pos] + 1).sum())
+    return out
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_rank_work_matches_oracle(name):
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    got = balance.rank_work(cu, w.batch, w.seq_len, w.cp_size)
+    for r in range(w.cp_size):
+        want = ofl.pairs_per_head(cu, w.batch, w.seq_len, w.cp_size, r)
+        assert np.array_equal(got[r], want), (name, r)
+    # the ranks together hold every query once
+    whole = ofl.pairs_per_head(cu, w.batch, w.seq_len, 1, 0)
+    assert np.array_equal(got.sum(axis=0), whole)
+
+
+def test_worked_example():
+    # S = 16, CP = 2 (chunks of 4), documents [0, 6) and [6, 16).  A query at
+    # p sees p - start + 1 keys: 1..6 in the first document, 1..10 in the
+    # second.  Chunks: [0,4) 1+2+3+4 = 10; [4,8) 5+6+1+2 = 14;
+    # [8,12) 3+4+5+6 = 18; [12,16) 7+8+9+10 = 34.  Rank 0 holds chunks 0 and
+    # 3 (44), rank 1 chunks 1 and 2 (32).
+    cu = np.array([0, 6, 16], dtype=np.int32)
+    got = balance.rank_work(cu, 1, 16, 2)
+    assert got[:, 0].tolist() == [44, 32]
+    imb = balance.imbalance(got)
+    assert imb["max_over_mean"] == pytest.approx(44 / 38)
+    assert imb["slowest_over_fastest"] == pytest.approx(44 / 32)
+
+
+@pytest.mark.parametrize("cp_size", [1, 2, 4, 16])
+def test_single_document_is_balanced(cp_size):
+    seq_len = 4096
+    cu = np.array([0, seq_len], dtype=np.int32)
+    got = balance.rank_work(cu, 1, seq_len, cp_size)
+    assert len(set(got[:, 0].tolist())) == 1
+    assert got[0, 0] == ofl.single_doc_pairs_closed_form(seq_len // (2 * cp_size), cp_size)
+    assert balance.imbalance(got)["max_over_mean"] == 1.0
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_explicit_bounds_match_oracle(name):
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    rng = np.random.default_rng(7)
+    n = 2 * w.cp_size
+    bounds = np.zeros((w.batch, n + 1), dtype=np.int64)
+    for b in range(w.batch):
+        inner = np.sort(rng.choice(np.arange(1, w.seq_len), size=n - 1, replace=False))
+        bounds[b] = np.r_[0, inner, w.seq_len]
+    got = balance.rank_work(cu, w.batch, w.seq_len, w.cp_size, bounds)
+    assert np.array_equal(got, _explicit_rank_pairs(cu, w.batch, w.seq_len, w.cp_size, bounds))
+
+
+@pytest.mark.parametrize("name,cp_size", [(n, None) for n in NAMES] + [("8b", 4), ("8b", 8),
+                                                                     ("405b-logu", 4)])
+def test_doc_aware_alternative(name, cp_size):
+    w = wl.WORKLOADS[name]
+    cp = cp_size or w.cp_size
+    cu = wl.cu_doc_lens(w)
+    rep = balance.report(cu, w.batch, w.seq_len, cp)
+    bounds = np.asarray(rep["doc_aware"]["bounds"])
+    n = 2 * cp
+    assert bounds.shape == (w.batch, n + 1)
+    assert (bounds[:, 0] == 0).all() and (bounds[:, -1] == w.seq_len).all()
+    assert (np.diff(bounds, axis=1) > 0).all()
+    assert rep["doc_aware"]["imbalance"]["max_over_mean"] <= rep["imbalance"]["max_over_mean"]
+    # the alternative's work is counted the same way as the oracle counts it
+    alt = np.asarray(rep["doc_aware"]["pairs_per_rank"])
+    want = _explicit_rank_pairs(cu, w.batch, w.seq_len, cp, bounds).sum(axis=1)
+    assert np.array_equal(alt, want)
+    # and it moves no work between ranks that is not there
+    assert alt.sum() == sum(rep["pairs_per_rank"])
+
+
+def test_equal_work_bounds_on_the_grid():
+    w = wl.WORKLOADS["405b-logu"]
+    cu = wl.cu_doc_lens(w)
+    b = balance.balanced_bounds(cu, w.batch, w.seq_len, 4, granule=256)
+    assert (b % 256 == 0).all() and (np.diff(b, axis=1) > 0).all()
+    chunks = [balance._segment_work(balance._docs_of_sample(cu, 0, w.seq_len), b[0, c], b[0, c + 1])
+              for c in range(8)]
+    # every chunk within a few granules' work of the ideal share
+    assert max(chunks) / (sum(chunks) / 8) < 1.1
