@@ -9,6 +9,7 @@ unmasked (query, key) pairs: FLOPs = sum over ranks and samples of
 Hq * pairs * (4*D forward + 10*D backward).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b]
+    python bench.py --sweep-causal [--steps K]   # throughput vs sequence length
     python bench.py --impl reference ...   # the float64 oracle on host cores
 
 Under torchrun (N > 1) every rank runs its own copy of the workload with its
@@ -575,6 +576,86 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+SWEEP_LENGTHS = (8192, 16384, 32768, 65536, 131072)
+
+
+def run_sweep(args) -> int:
+    """Throughput against sequence length on one GPU: CP = 1, batch 1, the
+    405B shard's heads (Hq = 16, Hkv = 1, D = 128), plain causal (one
+    document) and document-masked (log-uniform lengths in [1024,
+    min(65536, S/2)]) at 8K ... 128K.  One JSON line per configuration; `rel` = its TFLOP/s over
+    the 128K causal value, the kind of curve the pages' Figure 11 draws as
+    relative HFU.  Inputs resident, L2 flushed between steps, CUDA events
+    around each step (plan, forward, backward)."""
+    import torch
+    import document_masked_gqa_gb300 as dma
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak = measured_peaks().get("bf16_tflops") or FALLBACK_BF16_TFLOPS
+    lines = []
+    for mask in ("causal", "docs"):
+        for n, s_len in enumerate(SWEEP_LENGTHS):
+            if mask == "causal":
+                w = wl.custom(f"sweep-causal-{s_len}", s_len, 1, 1, 16, 1, 128, "single",
+                              seed=2000 + n)
+            else:
+                w = wl.custom(f"sweep-docs-{s_len}", s_len, 1, 1, 16, 1, 128, "loguniform",
+                              1024, min(65536, s_len // 2), seed=2100 + n)
+            cu_np = wl.cu_doc_lens(w)
+            inp = {k: v.to(dev) for k, v in wl.tensors(w).items()}
+            cu = torch.from_numpy(cu_np).to(dev)
+            need = dma.dma_plan_workspace_bytes(w.batch, w.seq_len, 1, w.n_heads, w.n_kv_heads,
+                                                w.head_dim)
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            out = {}
+
+            def step():
+                plan = dma.dma_plan(cu, w.batch, w.seq_len, 1, 0, w.n_heads, w.n_kv_heads,
+                                    w.head_dim, workspace=ws)
+                if not out:
+                    o, lse = dma.dma_attn_fwd(plan, inp["q"], inp["k"], inp["v"])
+                    dq, dk, dv = dma.dma_attn_bwd(plan, inp["q"], inp["k"], inp["v"], o, lse,
+                                                  inp["do"])
+                    out.update(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+                else:
+                    dma.dma_attn_fwd(plan, inp["q"], inp["k"], inp["v"], out["o"], out["lse"])
+                    dma.dma_attn_bwd(plan, inp["q"], inp["k"], inp["v"], out["o"], out["lse"],
+                                     inp["do"], out["dq"], out["dk"], out["dv"])
+                return plan
+
+            for _ in range(args.warmup):
+                step()
+                flush.zero_()
+            torch.cuda.synchronize(dev)
+            times = []
+            for _ in range(args.steps):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                plan = step()
+                b.record(stream)
+                flush.zero_()
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            st = dma.dma_plan_check(plan)
+            if st != 0:
+                raise RuntimeError(f"plan status {st}: {dma.status_str(st)}")
+            ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+            tf = flops_of(w, cu_np, (0,)) / (ms * 1e-3) / 1e12
+            lines.append({"sweep": "causal-vs-docs", "mask": mask, "seq_len": s_len,
+                          "docs": len(cu_np) - 1, "ms_per_step": ms, "tflops": tf,
+                          "pct_of_measured_peak": 100.0 * tf / peak})
+            del inp, out, ws
+            torch.cuda.empty_cache()
+    ref = [x["tflops"] for x in lines if x["mask"] == "causal" and x["seq_len"] == SWEEP_LENGTHS[-1]]
+    for x in lines:
+        x["rel"] = x["tflops"] / ref[0] if ref else None
+        print(json.dumps(x), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,9 +664,13 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="8b", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep-causal", action="store_true",
+                    help="throughput against sequence length, causal vs document-masked")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep_causal:
+        return run_sweep(args)
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -81,6 +81,10 @@ WORKLOADS = {
                           1, 16, 1, 128, "loguniform", 1024, 65536, 1.0, 1014),
     "sparse": Workload("sparse-stress", 32768, 4, (0, 1, 2, 3), 1, 16, 1, 128,
                        "uniform", 32, 512, 1.0, 1005),
+    # plain causal attention (one document) at 128K on a single rank: the
+    # long-sequence case of the pages' Figure 11 without CP
+    "causal-128k": Workload("causal-128k-cp1", 131072, 1, (0,), 1, 16, 1, 128,
+                            "single", 0, 0, 1.0, 1006),
 }
 
 

@@ -86,7 +86,7 @@ def test_bwd_parity_405b_logu_rank15_full():
         assert rel_fro(g[key].numpy(), ref[key]) <= TOL_GRAD, key
 
 
-@pytest.mark.parametrize("name", ["405b-logu", "405b-1doc"])
+@pytest.mark.parametrize("name", ["405b-logu", "405b-1doc", "causal-128k"])
 def test_bwd_405b_sampled_rows_and_tail_keys(name):
     """Every emulated rank at full size: sampled query rows (O, LSE, dQ), the
     exact dK/dV of the last key tile the rank reaches (only its last 128

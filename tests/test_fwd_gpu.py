@@ -42,7 +42,7 @@ def test_fwd_parity_edge(name):
         _fwd_case(w, r)
 
 
-@pytest.mark.parametrize("name", ["405b-logu", "405b-1doc"])
+@pytest.mark.parametrize("name", ["405b-logu", "405b-1doc", "causal-128k"])
 def test_fwd_parity_405b_sampled_rows(name):
     w = wl.WORKLOADS[name]
     rng = np.random.default_rng(99)
