@@ -67,3 +67,22 @@ def test_two_gloo_ranks_take_the_max_step_time():
         p.join(timeout=120)
         assert p.exitcode == 0
     assert out[0] == out[1] == 3.5
+
+
+def test_kernels_per_step_follow_the_planner():
+    # four planner kernels, V to fp16 + forward, Delta + dK/dV + dQ
+    for name in ["tiny", "8b", "70b", "sparse", "405b-1doc", "causal-128k"]:
+        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 9
+    # launch orders over 2048 units take one extra ranking kernel each
+    rows = wl.custom("rows", 32768, 1, 1, 16, 1, 64, "uniform", 64, 4096, seed=14)
+    both = wl.custom("both", 16384, 1, 17, 2, 2, 64, "uniform", 64, 4096, seed=15)
+    assert bench.kernels_per_rank_step(rows) == 10
+    assert bench.kernels_per_rank_step(both) == 11
+
+
+def test_source_hash_ignores_comments():
+    a = "int f(int x) {  // one\n  return x + 1; /* two\n three */ }\n"
+    b = "int f(int x) {\n\n  return x + 1;   }"
+    c = "int f(int x) { return x + 2; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
