@@ -97,6 +97,28 @@ def dist_info():
     return rank, world, local
 
 
+def delta_bytes(w: wl.Workload) -> int:
+    """Algorithmic bytes of one rank's Delta preprocess: reads O (fp32) and dO
+    (bf16), writes Delta (fp32), per query row and head."""
+    return w.batch * w.local_len * w.n_heads * (6 * w.head_dim + 4)
+
+
+def plan_bytes(w: wl.Workload, n_docs: int, listed_pairs: int) -> int:
+    """Algorithmic bytes of one rank's planner: reads cu_doc_lens; writes the
+    position map, document starts (queries) and ends (keys), chunk order,
+    tile classes (1 byte per tile pair), row / column counts and pointers,
+    the row and column lists (`listed_pairs` non-skipped tile pairs each) and
+    the two launch orders."""
+    g = w.n_heads // w.n_kv_heads
+    nqt = w.local_len // (128 // g)
+    nkt = w.seq_len // 128
+    b = w.batch
+    return (4 * (n_docs + 1) + 4 * w.local_len + 4 * b * w.local_len + 4 * b * w.seq_len
+            + 4 * 2 * w.cp_size + b * nqt * nkt
+            + 4 * (2 * b * nqt + 1) + 4 * (2 * b * nkt + 1)
+            + 4 * 2 * listed_pairs + 4 * (b * nqt + b * nkt))
+
+
 def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
     """Weak scaling: every process gets the same shape with its own seed."""
     return dataclasses.replace(w, seed=w.seed + 7919 * rank) if rank else w
@@ -444,6 +466,27 @@ def run_gpu(args, w: wl.Workload):
             "algorithmic_flops_per_launch": algo_flops,
             "kernel_ms": {n: round(kms[n], 5) for n in names}}
 
+    # the HBM-bound parts against the measured copy bandwidth: Delta, and the
+    # planner (latency-bound: a handful of small launches)
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm = {"peak_gbs": hbm_peak, "peak_source": "measured copy (MEASURED_PEAKS.json hbm_gbs)"}
+    db = delta_bytes(w)
+    hbm["delta"] = {"bytes": db, "ms": kms["delta"], "gbs": db / (kms["delta"] * 1e-3) / 1e9}
+    try:
+        listed = [int(dma.plan_arrays(R["plan"])["row_ptr"][-1]) for R in ranks]
+        pb = sum(plan_bytes(w, len(cu_np) - 1, n) for n in listed) / len(listed)
+        hbm["plan"] = {"bytes": pb, "ms": kms["plan"], "gbs": pb / (kms["plan"] * 1e-3) / 1e9,
+                       "note": "latency-bound: one memset and four small launches"}
+    except Exception as exc:  # the line is printed regardless
+        hbm["plan"] = {"error": str(exc)[:120]}
+    for part in ("delta", "plan"):
+        if hbm_peak and "gbs" in hbm[part]:
+            hbm[part]["frac"] = hbm[part]["gbs"] / hbm_peak
+    # the same step counted without the backward's recompute (4D + 8D per pair)
+    mfu_value = world * flops_of(w, cu_np, w.ranks, fwd=4, bwd=8) / (ms * 1e-3) / 1e12
+    mfu = {"value": mfu_value, "unit": UNIT, "count": "4D fwd + 8D bwd per pair and head",
+           "pct_of_measured_peak": 100.0 * mfu_value / world / peak}
+
     # end to end through the public API: pinned host inputs -> device -> step ->
     # results back to pinned host memory, every step
     e2e = run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world)
@@ -467,7 +510,7 @@ def run_gpu(args, w: wl.Workload):
             "dtype": "bf16", "data": "synthetic", "config": config_of(w),
             "pct_of_measured_peak": 100.0 * value / world / peak,
             "pct_of_datasheet_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "mfu_style": mfu, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels_per_rank_step(w) * len(w.ranks) * args.steps,
             "clocks": clocks,
         }

@@ -88,3 +88,15 @@ def test_source_hash_ignores_comments():
     c = "int f(int x) { return x + 2; }"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_hbm_byte_counts():
+    w = wl.WORKLOADS["8b"]
+    # O fp32 + dO bf16 in, Delta fp32 out: 2 x 8192 rows x 32 heads x (6*128 + 4)
+    assert bench.delta_bytes(w) == 2 * 8192 * 32 * 772
+    # a one-sample toy by hand: S = 256, CP = 1, Hq = Hkv = 1 (P = 128): 2 query
+    # tiles, 2 key tiles; 3 non-skipped pairs; 2 documents
+    t = wl.custom("toy", 256, 1, 1, 1, 1, 64, "fixed", fixed_docs=[[100, 156]])
+    want = (4 * 3 + 4 * 256 + 4 * 256 + 4 * 256 + 4 * 2 + 4
+            + 4 * 5 + 4 * 5 + 4 * 2 * 3 + 4 * 4)
+    assert bench.plan_bytes(t, 2, 3) == want
