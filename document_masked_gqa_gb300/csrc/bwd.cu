@@ -735,7 +735,7 @@ __device__ __forceinline__ DqItem dq_item(const PlanDev& p, int item) {
   return it;
 }
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...  Counters that
+// Persistent: CTA c takes work items in snake order.  Counters that
 // every role keeps identically across items: the stream index of the next
 // slot load (sidx), the number of key tiles processed so far (tbase, which
 // fixes the parity of every per-tile barrier) and the number of non-empty
