@@ -9,6 +9,7 @@ import fails loudly; there is no fallback.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -158,14 +159,18 @@ def dma_plan(cu_doc_lens, batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads,
             workspace = torch.empty(256, dtype=torch.uint8, device="cuda")
         else:
             workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
-    if cu_doc_lens is not None:
-        assert cu_doc_lens.dtype == torch.int32 and cu_doc_lens.is_cuda
-        assert cu_doc_lens.is_contiguous()
+    if cu_doc_lens is not None and (cu_doc_lens.dtype != torch.int32 or not cu_doc_lens.is_cuda
+                                    or not cu_doc_lens.is_contiguous()
+                                    or cu_doc_lens.dim() != 1):
+        raise ValueError("cu_doc_lens: want a contiguous 1-D int32 cuda tensor")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace: want a contiguous cuda tensor")
     n_docs = 0 if cu_doc_lens is None else cu_doc_lens.numel() - 1
     h = ctypes.c_void_p()
     st = lib().dma_plan(_ptr(cu_doc_lens), n_docs, batch, seq_len, cp_size, cp_rank, n_heads,
                         n_kv_heads, head_dim, float(softmax_scale), _ptr(workspace),
-                        workspace.numel(), _stream(stream), ctypes.byref(h))
+                        workspace.numel() * workspace.element_size(), _stream(stream),
+                        ctypes.byref(h))
     _check(st, "dma_plan")
     return Plan(h, workspace, (batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim),
                 cu_doc_lens)
@@ -224,17 +229,41 @@ def dma_attn_bwd(plan: Plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, s
 
 
 def dma_attn_bwd_delta(plan: Plan, o, dout, stream=None):
+    import torch
+    B, S, cp, _, Hq, Hkv, D = plan.shape
+    Lq = S // cp
+    _expect(o, torch.float32, (B, Lq, Hq, D), "o")
+    _expect(dout, torch.bfloat16, (B, Lq, Hq, D), "dout")
     _check(lib().dma_attn_bwd_delta(plan.handle, _ptr(o), _ptr(dout), _stream(stream)),
            "dma_attn_bwd_delta")
 
 
 def dma_attn_bwd_dkdv(plan: Plan, q, k, v, lse, dout, dk, dv, stream=None):
+    import torch
+    B, S, cp, _, Hq, Hkv, D = plan.shape
+    Lq = S // cp
+    _expect(q, torch.bfloat16, (B, Lq, Hq, D), "q")
+    _expect(k, torch.bfloat16, (B, S, Hkv, D), "k")
+    _expect(v, torch.bfloat16, (B, S, Hkv, D), "v")
+    _expect(lse, torch.float32, (B, Hq, Lq), "lse")
+    _expect(dout, torch.bfloat16, (B, Lq, Hq, D), "dout")
+    _expect(dk, torch.float32, (B, S, Hkv, D), "dk")
+    _expect(dv, torch.float32, (B, S, Hkv, D), "dv")
     _check(lib().dma_attn_bwd_dkdv(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
                                    _ptr(dout), _ptr(dk), _ptr(dv), _stream(stream)),
            "dma_attn_bwd_dkdv")
 
 
 def dma_attn_bwd_dq(plan: Plan, q, k, v, lse, dout, dq, stream=None):
+    import torch
+    B, S, cp, _, Hq, Hkv, D = plan.shape
+    Lq = S // cp
+    _expect(q, torch.bfloat16, (B, Lq, Hq, D), "q")
+    _expect(k, torch.bfloat16, (B, S, Hkv, D), "k")
+    _expect(v, torch.bfloat16, (B, S, Hkv, D), "v")
+    _expect(lse, torch.float32, (B, Hq, Lq), "lse")
+    _expect(dout, torch.bfloat16, (B, Lq, Hq, D), "dout")
+    _expect(dq, torch.bfloat16, (B, Lq, Hq, D), "dq")
     _check(lib().dma_attn_bwd_dq(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
                                  _ptr(dout), _ptr(dq), _stream(stream)), "dma_attn_bwd_dq")
 
@@ -252,18 +281,22 @@ def dma_cp_gather(plan: Plan, full, local=None, stream=None):
     import torch
     B, S, cp, _, _, _, _ = plan.shape
     Lq = S // cp
-    assert full.is_cuda and full.is_contiguous() and full.shape[:2] == (B, S)
+    _expect(full, full.dtype, (B, S) + tuple(full.shape[2:]), "full")
     if local is None:
         local = torch.empty((B, Lq) + tuple(full.shape[2:]), dtype=full.dtype, device=full.device)
-    row_bytes = full[0, 0].numel() * full.element_size()
+    _expect(local, full.dtype, (B, Lq) + tuple(full.shape[2:]), "local")
+    row_bytes = math.prod(full.shape[2:]) * full.element_size()
     _check(lib().dma_cp_gather(plan.handle, _ptr(full), _ptr(local), row_bytes,
                                _stream(stream)), "dma_cp_gather")
     return local
 
 
 def dma_cp_scatter(plan: Plan, local, full, stream=None):
-    assert local.is_cuda and full.is_cuda and local.is_contiguous() and full.is_contiguous()
-    row_bytes = local[0, 0].numel() * local.element_size()
+    B, S, cp, _, _, _, _ = plan.shape
+    Lq = S // cp
+    _expect(full, full.dtype, (B, S) + tuple(full.shape[2:]), "full")
+    _expect(local, full.dtype, (B, Lq) + tuple(full.shape[2:]), "local")
+    row_bytes = math.prod(full.shape[2:]) * full.element_size()
     _check(lib().dma_cp_scatter(plan.handle, _ptr(local), _ptr(full), row_bytes,
                                 _stream(stream)), "dma_cp_scatter")
     return full

@@ -81,3 +81,48 @@ def test_plan_rejects_bad_arguments_on_the_host(lib):
     assert lib.dma_attn_fwd(None, None, None, None, None, None, None) == 1
     assert lib.dma_attn_bwd(None, *([None] * 10)) == 1
     assert lib.dma_plan_destroy(None) == 0
+
+
+class _ShapeOnlyPlan:
+    """Stands in for a plan: the binding checks tensors against plan.shape
+    before it makes any library call."""
+    handle = None
+    shape = (1, 256, 2, 0, 4, 1, 64)  # batch, seq_len, cp_size, cp_rank, Hq, Hkv, D
+
+
+def test_binding_checks_tensors_before_any_call():
+    import torch
+    import document_masked_gqa_gb300 as dma
+    plan = _ShapeOnlyPlan()
+    q = torch.zeros(1, 128, 4, 64, dtype=torch.bfloat16)        # right shape, but on the host
+    kv = torch.zeros(1, 256, 1, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 128, 4, 64)
+    lse = torch.zeros(1, 4, 128)
+    dkv = torch.zeros(1, 256, 1, 64)
+    calls = [
+        lambda: dma.dma_attn_fwd(plan, q, kv, kv, o, lse),
+        lambda: dma.dma_attn_bwd(plan, q, kv, kv, o, lse, q, q, dkv, dkv),
+        lambda: dma.dma_attn_bwd_delta(plan, o, q),
+        lambda: dma.dma_attn_bwd_dkdv(plan, q, kv, kv, lse, q, dkv, dkv),
+        lambda: dma.dma_attn_bwd_dq(plan, q, kv, kv, lse, q, q),
+        lambda: dma.dma_cp_gather(plan, kv, q),
+        lambda: dma.dma_cp_scatter(plan, q, kv),
+        lambda: dma.dma_plan(torch.zeros(2, dtype=torch.int32), 1, 256, 2, 0, 4, 1, 64,
+                             workspace=torch.zeros(1 << 16, dtype=torch.uint8)),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError):
+            call()
+
+
+def test_binding_rejects_wrong_shapes_and_dtypes():
+    import torch
+    from document_masked_gqa_gb300 import _lib
+    with pytest.raises(ValueError):
+        _lib._expect(torch.zeros(1, 128, 4, 64), torch.bfloat16, (1, 128, 4, 64), "q")
+    with pytest.raises(ValueError):
+        _lib._expect(torch.zeros(1, 128, 4, 32, dtype=torch.bfloat16), torch.bfloat16,
+                     (1, 128, 4, 64), "q")
+    with pytest.raises(ValueError):
+        _lib._expect(torch.zeros(1, 64, 128, 4, dtype=torch.bfloat16).transpose(1, 2),
+                     torch.bfloat16, (1, 128, 64, 4), "q")
