@@ -119,6 +119,27 @@ def plan_bytes(w: wl.Workload, n_docs: int, listed_pairs: int) -> int:
             + 4 * 2 * listed_pairs + 4 * (b * nqt + b * nkt))
 
 
+def host_description() -> dict:
+    """CPU model and numpy's BLAS backend of the host the oracle runs on."""
+    out = {"cpu_model": None, "blas": None}
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            m = re.search(rf"^{key}\s*:\s*(.+)$", info, flags=re.M)
+            if m:
+                out["cpu_model"] = m.group(1).strip() if key != "CPU part" else f"arm part {m.group(1).strip()}"
+                break
+    except OSError:
+        pass
+    try:
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]
+        out["blas"] = f"{blas.get('name')} {blas.get('version')}"
+    except Exception:  # older numpy: no dict form
+        pass
+    return out
+
+
 def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
     """Weak scaling: every process gets the same shape with its own seed."""
     return dataclasses.replace(w, seed=w.seed + 7919 * rank) if rank else w
@@ -310,7 +331,7 @@ def run_reference(args, w: wl.Workload):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": sample, "threads": threads},
+                         "sample": sample, "threads": threads, **host_description()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -497,7 +518,7 @@ def run_gpu(args, w: wl.Workload):
         fl, threads = oracle_sample_step(w, inputs, cu_np)
         dt = time.perf_counter() - t0
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-               "kind": "oracle", "threads": threads,
+               "kind": "oracle", "threads": threads, **host_description(),
                "sample": (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank "
                           f"{w.ranks[0]}, all {w.local_len} local rows, fwd+bwd, "
                           f"{dt:.1f} s, float64 numpy")}

@@ -100,3 +100,9 @@ def test_hbm_byte_counts():
     want = (4 * 3 + 4 * 256 + 4 * 256 + 4 * 256 + 4 * 2 + 4
             + 4 * 5 + 4 * 5 + 4 * 2 * 3 + 4 * 4)
     assert bench.plan_bytes(t, 2, 3) == want
+
+
+def test_host_description_names_cpu_and_blas():
+    d = bench.host_description()
+    assert set(d) == {"cpu_model", "blas"}
+    assert d["cpu_model"] is None or isinstance(d["cpu_model"], str)
