@@ -22,6 +22,7 @@ DMA_ERR_UNSUPPORTED = 3
 DMA_ERR_CUDA = 4
 DMA_ERR_TIMEOUT = 5
 DMA_ERR_WORKSPACE = 6
+DMA_WARN_V_SATURATED = 7
 
 TILE_SKIP, TILE_FULL, TILE_PARTIAL = 0, 1, 2
 

@@ -145,6 +145,59 @@ dma_status map_o_f32(CUtensorMap* m, void* base, const dma::PlanDev& p, int rows
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Fills a plan's shape, scale, wait limit and device pointers into the
+// scratch at `ws` (laid out as `w`), and its device and SM count.  Shared by
+// dma_plan (caller's workspace) and dma_attn_fwd_noalloc (the library's
+// static scratch), so that the two cannot drift apart.
+dma_status init_plan(dma_plan_s& pl, const int32_t* cu_doc_lens, int n_docs, int batch,
+                     int seq_len, int cp_size, int cp_rank, int n_heads, int n_kv_heads,
+                     int head_dim, float softmax_scale, uint8_t* ws, const WorkspaceLayout& w) {
+  dma::PlanDev& p = pl.d;
+  p.batch = batch;
+  p.seq_len = seq_len;
+  p.cp_size = cp_size;
+  p.cp_rank = cp_rank;
+  p.n_heads = n_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.head_dim = head_dim;
+  p.chunk = seq_len / (2 * cp_size);
+  p.local_len = 2 * p.chunk;
+  p.group = n_heads / n_kv_heads;
+  p.tile_pos = dma::kTileM / p.group;
+  p.n_qtiles = p.local_len / p.tile_pos;
+  p.n_ktiles = seq_len / dma::kTileN;
+  p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.timeout_ns = 2000000000ull;
+  if (const char* env = std::getenv("DMA_WAIT_TIMEOUT_NS")) {
+    const unsigned long long t = std::strtoull(env, nullptr, 10);
+    if (t > 0) p.timeout_ns = t;
+  }
+  p.status = reinterpret_cast<uint32_t*>(ws + w.status);
+  p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
+  p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
+  p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);
+  p.chunk_order = reinterpret_cast<int32_t*>(ws + w.chunk_order);
+  p.tile_class = ws + w.tile_class;
+  p.row_cnt = reinterpret_cast<int32_t*>(ws + w.row_cnt);
+  p.row_ptr = reinterpret_cast<int32_t*>(ws + w.row_ptr);
+  p.row_idx = reinterpret_cast<int32_t*>(ws + w.row_idx);
+  p.col_cnt = reinterpret_cast<int32_t*>(ws + w.col_cnt);
+  p.col_ptr = reinterpret_cast<int32_t*>(ws + w.col_ptr);
+  p.col_idx = reinterpret_cast<int32_t*>(ws + w.col_idx);
+  p.fwd_order = reinterpret_cast<int32_t*>(ws + w.fwd_order);
+  p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
+  p.delta = reinterpret_cast<float*>(ws + w.delta);
+  p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+  pl.cu = cu_doc_lens;
+  pl.n_docs = n_docs;
+  if (cudaGetDevice(&pl.device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device) !=
+          cudaSuccess)
+    return DMA_ERR_CUDA;
+  return DMA_OK;
+}
+
 dma_status check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
@@ -184,49 +237,8 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch, int seq_l
 
   dma_plan_s* pl = new (std::nothrow) dma_plan_s();
   if (!pl) return DMA_ERR_CUDA;
-  dma::PlanDev& p = pl->d;
-  p.batch = batch;
-  p.seq_len = seq_len;
-  p.cp_size = cp_size;
-  p.cp_rank = cp_rank;
-  p.n_heads = n_heads;
-  p.n_kv_heads = n_kv_heads;
-  p.head_dim = head_dim;
-  p.chunk = seq_len / (2 * cp_size);
-  p.local_len = 2 * p.chunk;
-  p.group = n_heads / n_kv_heads;
-  p.tile_pos = dma::kTileM / p.group;
-  p.n_qtiles = p.local_len / p.tile_pos;
-  p.n_ktiles = seq_len / dma::kTileN;
-  p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
-  p.scale_log2 = p.scale * 1.4426950408889634f;
-  p.timeout_ns = 2000000000ull;
-  if (const char* env = std::getenv("DMA_WAIT_TIMEOUT_NS")) {
-    const unsigned long long t = std::strtoull(env, nullptr, 10);
-    if (t > 0) p.timeout_ns = t;
-  }
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.status = reinterpret_cast<uint32_t*>(ws + w.status);
-  p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
-  p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
-  p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);
-  p.chunk_order = reinterpret_cast<int32_t*>(ws + w.chunk_order);
-  p.tile_class = ws + w.tile_class;
-  p.row_cnt = reinterpret_cast<int32_t*>(ws + w.row_cnt);
-  p.row_ptr = reinterpret_cast<int32_t*>(ws + w.row_ptr);
-  p.row_idx = reinterpret_cast<int32_t*>(ws + w.row_idx);
-  p.col_cnt = reinterpret_cast<int32_t*>(ws + w.col_cnt);
-  p.col_ptr = reinterpret_cast<int32_t*>(ws + w.col_ptr);
-  p.col_idx = reinterpret_cast<int32_t*>(ws + w.col_idx);
-  p.fwd_order = reinterpret_cast<int32_t*>(ws + w.fwd_order);
-  p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
-  p.delta = reinterpret_cast<float*>(ws + w.delta);
-  p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-  pl->cu = cu_doc_lens;
-  pl->n_docs = n_docs;
-  if (cudaGetDevice(&pl->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device) !=
-          cudaSuccess) {
+  if (init_plan(*pl, cu_doc_lens, n_docs, batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads,
+                head_dim, softmax_scale, static_cast<uint8_t*>(workspace), w) != DMA_OK) {
     delete pl;
     return DMA_ERR_CUDA;
   }
@@ -332,12 +344,14 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
 
 dma_status dma_plan_check(dma_plan_t plan, void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
-  uint32_t st = 0;
+  uint32_t st[2] = {0u, 0u};  // error word, warning word
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&st, plan->d.status, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (cudaMemcpyAsync(st, plan->d.status, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DMA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DMA_ERR_CUDA;
-  return static_cast<dma_status>(st);
+  if (st[0] != 0u) return static_cast<dma_status>(st[0]);
+  if (st[1] & 1u) return DMA_WARN_V_SATURATED;
+  return DMA_OK;
 }
 
 dma_status dma_plan_destroy(dma_plan_t plan) {
@@ -354,6 +368,8 @@ const char* dma_status_str(dma_status s) {
     case DMA_ERR_CUDA: return "CUDA call failed";
     case DMA_ERR_TIMEOUT: return "bounded device wait expired";
     case DMA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case DMA_WARN_V_SATURATED:
+      return "finite v values beyond +-65504 were saturated in the fp16 copy";
   }
   return "unknown status";
 }
@@ -443,19 +459,34 @@ dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev, void*
 namespace {
 
 // 64 MiB of scratch per device, held by every GPU that loads the library
-// until the process exits.  Fits the plan plus the fp16 V copy of, e.g., an
-// 8K-token batch of 2 with 8 K/V heads of 128, or one 128K-token sample with
-// one K/V head of 128.
+// until the process exits.  It fits the plan plus the fp16 V copy of, e.g.,
+// an 8K-token batch of 2 with 8 K/V heads of 128 (about 34 MiB), or one
+// 128K-token sample with one K/V head of 128 at CP = 16 (about 42 MiB); at
+// CP = 1 the same sample needs about 186 MiB, mostly its tile lists.
+// dma_plan_workspace_bytes gives the exact need of a shape.
 constexpr size_t kNoAllocScratchBytes = 64ull << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // In host code `g_noalloc_scratch` is only a stand-in for the symbol, not a
-// device address: its device address is looked up once per device, with
-// that device current.
+// device address: its device address is looked up per device, with that
+// device current.  Only a successful lookup is kept; a failed one (made under
+// stream capture, say) is retried by the next call.
 constexpr int kNoAllocMaxDevices = 64;
 void* g_noalloc_ptr[kNoAllocMaxDevices];
-cudaError_t g_noalloc_err[kNoAllocMaxDevices];
-std::once_flag g_noalloc_once[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+void* noalloc_scratch(int dev) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();  // clear the (non-sticky) error for the caller
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = a;
+  }
+  return g_noalloc_ptr[dev];
+}
 
 }  // namespace
 
@@ -479,56 +510,15 @@ extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_doc
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return DMA_ERR_UNSUPPORTED;
-  std::call_once(g_noalloc_once[dev], [dev] {
-    g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
-  });
-  if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return DMA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
+  if (!ws) return DMA_ERR_CUDA;
 
   // the plan lives on this stack frame and in the scratch array
   dma_plan_s pl{};
-  dma::PlanDev& p = pl.d;
-  p.batch = batch;
-  p.seq_len = seq_len;
-  p.cp_size = cp_size;
-  p.cp_rank = cp_rank;
-  p.n_heads = n_heads;
-  p.n_kv_heads = n_kv_heads;
-  p.head_dim = head_dim;
-  p.chunk = seq_len / (2 * cp_size);
-  p.local_len = 2 * p.chunk;
-  p.group = n_heads / n_kv_heads;
-  p.tile_pos = dma::kTileM / p.group;
-  p.n_qtiles = p.local_len / p.tile_pos;
-  p.n_ktiles = seq_len / dma::kTileN;
-  p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
-  p.scale_log2 = p.scale * 1.4426950408889634f;
-  p.timeout_ns = 2000000000ull;
-  if (const char* env = std::getenv("DMA_WAIT_TIMEOUT_NS")) {
-    const unsigned long long t = std::strtoull(env, nullptr, 10);
-    if (t > 0) p.timeout_ns = t;
-  }
-  uint8_t* ws = static_cast<uint8_t*>(g_noalloc_ptr[dev]);
-  p.status = reinterpret_cast<uint32_t*>(ws + w.status);
-  p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
-  p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
-  p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);
-  p.chunk_order = reinterpret_cast<int32_t*>(ws + w.chunk_order);
-  p.tile_class = ws + w.tile_class;
-  p.row_cnt = reinterpret_cast<int32_t*>(ws + w.row_cnt);
-  p.row_ptr = reinterpret_cast<int32_t*>(ws + w.row_ptr);
-  p.row_idx = reinterpret_cast<int32_t*>(ws + w.row_idx);
-  p.col_cnt = reinterpret_cast<int32_t*>(ws + w.col_cnt);
-  p.col_ptr = reinterpret_cast<int32_t*>(ws + w.col_ptr);
-  p.col_idx = reinterpret_cast<int32_t*>(ws + w.col_idx);
-  p.fwd_order = reinterpret_cast<int32_t*>(ws + w.fwd_order);
-  p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
-  p.delta = reinterpret_cast<float*>(ws + w.delta);
-  p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-  pl.cu = cu_doc_lens;
-  pl.n_docs = n_docs;
-  pl.device = dev;
-  if (cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  if (init_plan(pl, cu_doc_lens, n_docs, batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads,
+                head_dim, softmax_scale, ws, w) != DMA_OK)
     return DMA_ERR_CUDA;
+  const dma::PlanDev& p = pl.d;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the plan kernels clear what must start at zero (status word, column
@@ -542,9 +532,7 @@ extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_doc
   if ((st = map_kv(&tv16, p.v16, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != DMA_OK) return st;
   if (dma::launch_v_to_f16(pl, v, s) != cudaSuccess) return DMA_ERR_CUDA;
   if (dma::launch_fwd(pl, tq, tk, tv16, to, o, lse, s) != cudaSuccess) return DMA_ERR_CUDA;
-  if (status_dev &&
-      cudaMemcpyAsync(status_dev, p.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
-          cudaSuccess)
+  if (status_dev && dma::launch_status_out(p.status, status_dev, s) != cudaSuccess)
     return DMA_ERR_CUDA;
   return DMA_OK;
 }

@@ -22,7 +22,7 @@ struct PlanDev {
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   uint64_t timeout_ns;
-  uint32_t* status;
+  uint32_t* status;   // [0] error word (kernels do nothing once set), [1] warning bits
   int32_t* qpos;      // [Lq]
   int32_t* doc_lo;    // [B][Lq]
   int32_t* doc_hi;    // [B][S] end (exclusive) of each key position's document
@@ -83,4 +83,5 @@ cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& 
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
+cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s);
 }  // namespace dma

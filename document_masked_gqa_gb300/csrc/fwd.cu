@@ -601,10 +601,19 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-// V (bf16) -> fp16 copy for the P V product; values beyond the fp16 range
-// saturate at +-65504.  8 elements per thread.
+// V (bf16) -> fp16 copy for the P V product, 8 elements per thread.  NaN and
+// +-Inf pass through unchanged (a NaN in V reaches O as it would in bf16
+// arithmetic).  Finite values beyond the fp16 range (|v| > 65504) saturate at
+// +-65504, and the kernel then sets bit 0 of warn (the plan's warning word),
+// which dma_plan_check reports as DMA_WARN_V_SATURATED.
+__device__ __forceinline__ float sat_f16_range(float x, bool& clamped) {
+  const bool over = fabsf(x) > 65504.f && fabsf(x) <= 3.402823466e38f;  // finite only
+  clamped |= over;
+  return over ? copysignf(65504.f, x) : x;
+}
 __global__ void v_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                long long n8) {
+                                long long n8, uint32_t* __restrict__ warn) {
+  bool clamped = false;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const uint4 a = src[i];
@@ -612,12 +621,13 @@ __global__ void v_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict
     uint32_t o4[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float lo = fminf(fmaxf(__uint_as_float(w[e] << 16), -65504.f), 65504.f);
-      const float hi = fminf(fmaxf(__uint_as_float(w[e] & 0xFFFF0000u), -65504.f), 65504.f);
+      const float lo = sat_f16_range(__uint_as_float(w[e] << 16), clamped);
+      const float hi = sat_f16_range(__uint_as_float(w[e] & 0xFFFF0000u), clamped);
       o4[e] = pack_f16(lo, hi);
     }
     dst[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
   }
+  if (__any_sync(0xffffffffu, clamped) && (threadIdx.x & 31) == 0) atomicOr(warn, 1u);
 }
 
 template <int D>
@@ -644,8 +654,8 @@ cudaError_t launch_v_to_f16(const dma_plan_s& pl, const dma_bf16* v, cudaStream_
   if (n8 == 0) return cudaSuccess;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 8LL * pl.num_sms) blocks = 8LL * pl.num_sms;
-  v_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(v),
-                                                        reinterpret_cast<uint4*>(p.v16), n8);
+  v_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(p.v16), n8, p.status + 1);
   return cudaGetLastError();
 }
 

@@ -271,6 +271,13 @@ __global__ void cp_copy_kernel(PlanDev p, const uint8_t* __restrict__ src, uint8
   }
 }
 
+// The status a caller sees for a plan: the error word if set, else
+// DMA_WARN_V_SATURATED if the warning word says V was saturated, else OK.
+__global__ void status_out_kernel(const uint32_t* __restrict__ st, uint32_t* __restrict__ out) {
+  const uint32_t e = st[0];
+  *out = e != 0u ? e : ((st[1] & 1u) ? static_cast<uint32_t>(DMA_WARN_V_SATURATED) : 0u);
+}
+
 __global__ void wait_probe_kernel(uint64_t timeout_ns, uint32_t* status) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -315,6 +322,11 @@ cudaError_t launch_cp_copy(const dma_plan_s& pl, const void* src, void* dst, siz
   if (rows == 0) return cudaSuccess;
   cp_copy_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
       p, static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), row_bytes, gather ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s) {
+  status_out_kernel<<<1, 1, 0, s>>>(status, out);
   return cudaGetLastError();
 }
 

@@ -75,7 +75,13 @@ typedef enum {
   DMA_ERR_UNSUPPORTED = 3, /* shape outside the supported set, or not sm_103 */
   DMA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
   DMA_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired */
-  DMA_ERR_WORKSPACE = 6    /* workspace too small or misaligned */
+  DMA_ERR_WORKSPACE = 6,   /* workspace too small or misaligned */
+  /* Not an error: the results were computed, but finite v values beyond the
+   * fp16 range (|v| > 65504) were saturated at +-65504 in the forward's fp16
+   * copy of v, so o and lse of the rows that attend them are inexact.
+   * Reported by dma_plan_check (and the no-alloc forward's status_dev) only
+   * when no error occurred. */
+  DMA_WARN_V_SATURATED = 7
 } dma_status;
 
 /* bf16 values are passed as raw 16-bit patterns. */
@@ -121,12 +127,15 @@ dma_status dma_plan(const int32_t* cu_doc_lens, int n_docs, int batch,
 
 /*
  * Forward: o = softmax(scale * q k^T + mask) v and the row log-sum-exp.
- * Two launches: an fp16 copy of v into the plan workspace (values beyond
- * +-65504 saturate), then the attention kernel, in which pairs of tiles
+ * Two launches: an fp16 copy of v into the plan workspace, then the attention
+ * kernel, in which pairs of tiles
  * classified skip issue no work.  The probabilities enter the P V product in
  * fp16 and o is written in fp32: a bf16 o could not hold a 1e-2 absolute
  * error bound once |o| >= 4 (half a bf16 ulp there is 0.0156), which rows that
  * see only a few keys of a short document reach.
+ * The fp16 copy keeps NaN and +-Inf as they are (they reach o as they would
+ * in bf16 arithmetic); finite values beyond +-65504 saturate there, which the
+ * plan's status then reports as DMA_WARN_V_SATURATED.
  */
 dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
                         const dma_bf16* v, float* o, float* lse,
@@ -162,8 +171,10 @@ dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k
                            const dma_bf16* v, const float* lse, const dma_bf16* dout,
                            dma_bf16* dq, void* stream);
 
-/* Synchronize `stream` and return the plan's device status word
- * (DMA_OK, DMA_ERR_BAD_DOCS or DMA_ERR_TIMEOUT) or DMA_ERR_CUDA. */
+/* Synchronize `stream` and return the plan's device status: DMA_ERR_BAD_DOCS
+ * or DMA_ERR_TIMEOUT if the device recorded an error, else
+ * DMA_WARN_V_SATURATED if a forward saturated v values, else DMA_OK; or
+ * DMA_ERR_CUDA if the read-back itself failed. */
 dma_status dma_plan_check(dma_plan_t plan, void* stream);
 
 /* Free the host handle (the caller's workspace is untouched). NULL is ok. */
@@ -251,11 +262,14 @@ dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev,
  *     (dma_plan_workspace_bytes gives the size a shape needs).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call outside any stream capture.
+ *     Only a successful lookup is kept (a failed one returns DMA_ERR_CUDA and
+ *     is tried again by the next call).
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (different streams, or different host threads) race and corrupt each
  *     other; serialize them (one stream is enough).
- *   - status_dev (optional, device uint32) receives the plan's status word
- *     (DMA_OK, DMA_ERR_BAD_DOCS, DMA_ERR_TIMEOUT) in stream order; on a
+ *   - status_dev (optional, device uint32) receives the plan's status
+ *     (DMA_OK, DMA_ERR_BAD_DOCS, DMA_ERR_TIMEOUT or DMA_WARN_V_SATURATED, as
+ *     dma_plan_check would return it) in stream order; on a
  *     malformed cu_doc_lens, o and lse are left unwritten.
  *   - It calls no allocator: no cudaMalloc, no cudaFree, no host heap.
  */

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     import document_masked_gqa_gb300 as dma
-    for s in range(7):
+    for s in range(8):
         assert dma.status_str(s) and dma.status_str(s) != "unknown status"
     assert dma.status_str(99) == "unknown status"
 
