@@ -12,9 +12,12 @@ Hq * pairs * (4*D forward + 10*D backward).
     python bench.py --sweep-causal [--steps K]   # throughput vs sequence length
     python bench.py --impl reference ...   # the float64 oracle on host cores
 
-Under torchrun (N > 1) every rank runs its own copy of the workload with its
-own seed (independent problems, weak scaling, no data-path collective); the
-step time is the max over ranks.  Rank 0 prints one JSON line.
+Under torchrun (N > 1) the emulated CP ranks of the workload are dealt to the
+processes (rank r of the workload to process r mod N, each process holding
+the full K/V), the natural partition of the path: no data-path collective.
+When there are more processes than emulated ranks, further copies of the
+workload (inputs re-drawn from a shifted seed) fill them.  The step time is
+the max over processes.  Rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -41,9 +44,12 @@ from document_masked_gqa_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "doc-masked GQA attn fwd+bwd TFLOP/s (unmasked FLOPs), % of GB300 bf16 peak"
 UNIT = "TFLOP/s"
-DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, NVIDIA's figure without sparsity
+# GB300 dense bf16: NVIDIA's HGX B300 figure of 36 PFLOP/s bf16 for 8 GPUs is
+# quoted with 2:4 sparsity, i.e. 4.5 PFLOP/s sparse and 2.25 dense per GPU
+DATASHEET_BF16_TFLOPS = 2250.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+CPU_BASELINE_TARGET_S = 15.0  # seconds of host work the bounded oracle sample aims at
 PLAN_SORT_MAX = 2048  # launch orders up to this many units are sorted inside the scan kernel
 
 
@@ -140,9 +146,48 @@ def host_description() -> dict:
     return out
 
 
-def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
-    """Weak scaling: every process gets the same shape with its own seed."""
-    return dataclasses.replace(w, seed=w.seed + 7919 * rank) if rank else w
+def copy_workload(w: wl.Workload, copy: int) -> wl.Workload:
+    """Copy `copy` of a workload: the same shape, inputs drawn from the seed
+    shifted by 7919 per copy (copy 0 is the workload itself)."""
+    return dataclasses.replace(w, seed=w.seed + 7919 * copy) if copy else w
+
+
+def assign_units(world: int, ranks) -> tuple:
+    """Work units of an N-process run and the share of each process.  The
+    job is ceil(N / R) copies of the workload (R emulated CP ranks); its
+    (copy, rank) units are dealt round-robin to the processes, so with
+    N <= R the emulated ranks of one workload are split across processes
+    (each holds the full K/V: the partition the path has), and with N > R
+    whole further copies fill the extra processes.  Returns (shares, copies)
+    with shares[p] the (copy, rank) list of process p."""
+    ranks = list(ranks)
+    copies = -(-world // len(ranks))
+    units = [(c, r) for c in range(copies) for r in ranks]
+    return [units[p::world] for p in range(world)], copies
+
+
+def scaling_kind(world: int, copies: int) -> str:
+    """'strong' when one copy of the workload is split over several
+    processes, else 'weak' (fixed work per process as N grows)."""
+    return "strong" if (world > 1 and copies == 1) else "weak"
+
+
+def algorithmic_bytes(w: wl.Workload, kernel: str) -> int:
+    """Bytes one launch of an attention kernel must move at least: every
+    input read once and every output written once (q, dO, dQ bf16; O fp32;
+    K, V bf16 (the forward reads V's fp16 copy, same size); dK, dV fp32;
+    LSE, Delta fp32), whole tensors."""
+    rows = w.batch * w.local_len * w.n_heads
+    qsz = rows * w.head_dim * 2                                   # bf16 [B, Lq, Hq, D]
+    kvsz = w.batch * w.seq_len * w.n_kv_heads * w.head_dim * 2    # bf16 [B, S, Hkv, D]
+    stat = rows * 4                                               # fp32 [B, Hq, Lq]
+    if kernel == "fwd":
+        return qsz + 2 * kvsz + 2 * qsz + stat                    # q, k, v; o fp32, lse
+    if kernel == "dkdv":
+        return 2 * qsz + 2 * kvsz + 2 * stat + 2 * 2 * kvsz       # q, dO, k, v, lse, Delta; dk, dv fp32
+    if kernel == "dq":
+        return 2 * qsz + 2 * kvsz + 2 * stat + qsz                # q, dO, k, v, lse, Delta; dq
+    raise ValueError(kernel)
 
 
 def reduce_max(x: float, world: int, device=None) -> float:
@@ -274,8 +319,10 @@ def profiled_traffic(kernel: str, workload: str) -> float | None:
 
 def oracle_sample_step(w: wl.Workload, inputs: dict, cu, rows=None, threads=None):
     """One bounded sample of the workload on the float64 oracle: sample 0,
-    the query heads of K/V head 0, rank ranks[0]; fwd + bwd.  Returns the
-    counted FLOPs of the sample."""
+    the query heads of K/V head 0, rank ranks[0], the given local rows (all
+    when None; dK/dV then from those rows alone); fwd + bwd on `threads`
+    host threads (default: every core).  Returns (counted FLOPs of the
+    sample, threads)."""
     from oracle import attention as oa
     from oracle import cp as ocp
     r = w.ranks[0]
@@ -285,14 +332,44 @@ def oracle_sample_step(w: wl.Workload, inputs: dict, cu, rows=None, threads=None
     k = inputs["k"][:1, :, :1]
     v = inputs["v"][:1, :, :1]
     cu0 = np.asarray([x for x in cu if x <= w.seq_len], dtype=np.int64)
-    threads = threads or min(g, os.cpu_count() or 1)
+    threads = threads or (os.cpu_count() or 1)
     oa.attention(q, k, v, cu0, w.cp_size, r, do_local=do, rows=rows, threads=threads,
                  kv_grads_from_rows=True)
-    qpos = local_positions(w.seq_len, w.cp_size, r)
+    return float(g) * sample_pairs(w, cu0, rows) * 14 * w.head_dim, threads
+
+
+def sample_pairs(w: wl.Workload, cu0, rows=None) -> int:
+    """Allowed pairs of the sample's rows (sample 0, rank ranks[0]), per head."""
+    qpos = local_positions(w.seq_len, w.cp_size, w.ranks[0])
     sel = qpos if rows is None else qpos[np.asarray(rows)]
     d = np.searchsorted(cu0, sel, side="right") - 1
-    pairs = int((sel - cu0[d] + 1).sum())
-    return float(g) * pairs * 14 * w.head_dim, threads
+    return int((sel - cu0[d] + 1).sum())
+
+
+def oracle_sample_rows(w: wl.Workload, inputs: dict, cu, target_s: float):
+    """Rows of the bounded oracle sample: the last local rows (the rank's
+    heaviest, at the end of its second chunk), as many as take about
+    `target_s` seconds, from a calibration run of 64 rows.  None = all."""
+    cu0 = np.asarray([x for x in cu if x <= w.seq_len], dtype=np.int64)
+    cal = np.arange(w.local_len - min(64, w.local_len), w.local_len)
+    t0 = time.perf_counter()
+    oracle_sample_step(w, inputs, cu, rows=cal)
+    per_pair = (time.perf_counter() - t0) / max(1, sample_pairs(w, cu0, cal))
+    budget_pairs = target_s / per_pair
+    if sample_pairs(w, cu0) <= budget_pairs:
+        return None
+    n = len(cal)
+    while n < w.local_len and sample_pairs(w, cu0, np.arange(w.local_len - 2 * n, w.local_len)) \
+            <= budget_pairs:
+        n *= 2
+    return np.arange(w.local_len - n, w.local_len)
+
+
+def sample_text(w: wl.Workload, rows) -> str:
+    what = (f"all {w.local_len} local rows" if rows is None else
+            f"local rows {rows[0]}-{rows[-1]} (dK/dV from those rows)")
+    return (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank {w.ranks[0]}, "
+            f"{what}, fwd+bwd, float64 numpy")
 
 
 def run_reference(args, w: wl.Workload):
@@ -303,19 +380,9 @@ def run_reference(args, w: wl.Workload):
     inputs = wl.tensors(w)
     budget = float(os.environ.get("DMA_REF_BUDGET_S", "150"))
     steps_total = args.steps + args.warmup
-    # size the sample: all rows of one K/V group of sample 0, cut to fit budget
-    t0 = time.perf_counter()
-    flops, threads = oracle_sample_step(w, inputs, cu)
-    t_full = time.perf_counter() - t0
-    rows = None
-    sample = (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank {w.ranks[0]}, "
-              f"all {w.local_len} local rows, fwd+bwd")
-    if t_full * steps_total > budget:
-        frac = max(budget / (t_full * steps_total), 1.0 / w.local_len)
-        n = max(1, int(w.local_len * frac))
-        rows = np.arange(w.local_len - n, w.local_len)  # the heaviest rows: last chunk tail
-        sample = (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank {w.ranks[0]}, "
-                  f"local rows {rows[0]}-{rows[-1]}, fwd+bwd (dK/dV from those rows)")
+    # size the sample so that the whole run stays within the budget
+    rows = oracle_sample_rows(w, inputs, cu, budget / steps_total)
+    sample = sample_text(w, rows)
     times = []
     for i in range(steps_total):
         t0 = time.perf_counter()
@@ -330,8 +397,9 @@ def run_reference(args, w: wl.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": sample, "threads": threads, **host_description()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample, "threads": threads,
+                         "cores_available": os.cpu_count(), **host_description()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -364,53 +432,61 @@ def run_gpu(args, w: wl.Workload):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    w = rank_workload(w, rank)
-    cu_np = wl.cu_doc_lens(w)
-    cu = torch.from_numpy(cu_np).to(dev)
-    inputs = wl.tensors(w)
+    shares, copies = assign_units(world, w.ranks)
     stream = torch.cuda.current_stream(dev)
 
-    k = inputs["k"].to(dev)
-    v = inputs["v"].to(dev)
-    ranks = []
-    for r in w.ranks:
+    # every unit of the whole job, for the FLOP count; this process's own
+    copy_of = {c: copy_workload(w, c) for c in range(copies)}
+    cu_of = {c: wl.cu_doc_lens(copy_of[c]) for c in range(copies)}
+    flops_job = sum(flops_of(copy_of[c], cu_of[c], (r,)) for sh in shares for c, r in sh)
+    mine = shares[rank]
+    inputs_of = {c: wl.tensors(copy_of[c]) for c in sorted({c for c, _ in mine})}
+    dev_of = {}
+    for c, inp in inputs_of.items():
+        dev_of[c] = {"cu": torch.from_numpy(cu_of[c]).to(dev), "k": inp["k"].to(dev),
+                     "v": inp["v"].to(dev)}
+    units = []
+    for c, r in mine:
+        D = dev_of[c]
         need = dma.dma_plan_workspace_bytes(w.batch, w.seq_len, w.cp_size, w.n_heads,
                                             w.n_kv_heads, w.head_dim)
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
-        plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
+        plan = dma.dma_plan(D["cu"], w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
                             w.head_dim, workspace=ws)
-        q = dma.dma_cp_gather(plan, inputs["q"].to(dev))
-        do = dma.dma_cp_gather(plan, inputs["do"].to(dev))
-        o, lse = dma.dma_attn_fwd(plan, q, k, v)
-        dq, dk, dv = dma.dma_attn_bwd(plan, q, k, v, o, lse, do)
-        ranks.append(dict(r=r, ws=ws, q=q, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+        q = dma.dma_cp_gather(plan, inputs_of[c]["q"].to(dev))
+        do = dma.dma_cp_gather(plan, inputs_of[c]["do"].to(dev))
+        o, lse = dma.dma_attn_fwd(plan, q, D["k"], D["v"])
+        dq, dk, dv = dma.dma_attn_bwd(plan, q, D["k"], D["v"], o, lse, do)
+        pairs = int(pairs_per_sample(cu_of[c], w.batch, w.seq_len, w.cp_size, r).sum())
+        units.append(dict(c=c, r=r, ws=ws, q=q, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv,
+                          k=D["k"], v=D["v"], cu=D["cu"], pairs=pairs))
     torch.cuda.synchronize(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     names = ("plan", "fwd", "delta", "dkdv", "dq")
-    ktime = {n: 0.0 for n in names}
 
     def step(record: bool):
         evs = []
-        for R in ranks:
+        for U in units:
             e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
             if record:
                 e[0].record(stream)
-            plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, R["r"], w.n_heads,
-                                w.n_kv_heads, w.head_dim, workspace=R["ws"])
-            R["plan"] = plan
+            plan = dma.dma_plan(U["cu"], w.batch, w.seq_len, w.cp_size, U["r"], w.n_heads,
+                                w.n_kv_heads, w.head_dim, workspace=U["ws"])
+            U["plan"] = plan
             if record:
                 e[1].record(stream)
-            dma.dma_attn_fwd(plan, R["q"], k, v, R["o"], R["lse"])
+            dma.dma_attn_fwd(plan, U["q"], U["k"], U["v"], U["o"], U["lse"])
             if record:
                 e[2].record(stream)
-            dma.dma_attn_bwd_delta(plan, R["o"], R["do"])
+            dma.dma_attn_bwd_delta(plan, U["o"], U["do"])
             if record:
                 e[3].record(stream)
-            dma.dma_attn_bwd_dkdv(plan, R["q"], k, v, R["lse"], R["do"], R["dk"], R["dv"])
+            dma.dma_attn_bwd_dkdv(plan, U["q"], U["k"], U["v"], U["lse"], U["do"], U["dk"],
+                                  U["dv"])
             if record:
                 e[4].record(stream)
-            dma.dma_attn_bwd_dq(plan, R["q"], k, v, R["lse"], R["do"], R["dq"])
+            dma.dma_attn_bwd_dq(plan, U["q"], U["k"], U["v"], U["lse"], U["do"], U["dq"])
             if record:
                 e[5].record(stream)
             evs.append(e)
@@ -420,8 +496,8 @@ def run_gpu(args, w: wl.Workload):
         step(False)
         flush.zero_()
     torch.cuda.synchronize(dev)
-    for R in ranks:
-        st = dma.dma_plan_check(R["plan"])
+    for U in units:
+        st = dma.dma_plan_check(U["plan"])
         if st != 0:
             raise RuntimeError(f"plan status {st}: {dma.status_str(st)}")
 
@@ -454,48 +530,69 @@ def run_gpu(args, w: wl.Workload):
 
     ms_steps = [a.elapsed_time(b) for a, b in step_pairs]
     ms_local = sum(ms_steps) / len(ms_steps)
-    for evs in all_evs:
-        for e in evs:
+    # per unit and kernel: mean ms per launch
+    per_unit = []
+    for ui, U in enumerate(units):
+        km = {n: 0.0 for n in names}
+        for evs in all_evs:
+            e = evs[ui]
             for i, n in enumerate(names):
-                ktime[n] += e[i].elapsed_time(e[i + 1])
-    n_launch = args.steps * len(ranks)
-    kms = {n: ktime[n] / n_launch for n in names}
-    for R in ranks:
-        st = dma.dma_plan_check(R["plan"])
+                km[n] += e[i].elapsed_time(e[i + 1])
+        km = {n: km[n] / args.steps for n in names}
+        per_unit.append({"copy": U["c"], "rank": U["r"], "pairs_per_head": U["pairs"],
+                         "process": rank, "ms": {n: round(km[n], 5) for n in names},
+                         "ms_total": round(sum(km.values()), 5)})
+    kms = {n: sum(u["ms"][n] for u in per_unit) / len(per_unit) for n in names}
+    for U in units:
+        st = dma.dma_plan_check(U["plan"])
         if st != 0:
             raise RuntimeError(f"plan status {st}: {dma.status_str(st)}")
+    if world > 1:
+        import torch.distributed as dist
+        gathered = [None] * world
+        dist.all_gather_object(gathered, per_unit)
+        per_unit_all = [u for part in gathered for u in part]
+    else:
+        per_unit_all = per_unit
 
     ms = reduce_max(ms_local, world, dev)
-    flops_step = flops_of(w, cu_np, w.ranks)
-    value = world * flops_step / (ms * 1e-3) / 1e12
+    value = flops_job / (ms * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (largest share of the step)
-    per_rank_pairs = [int(pairs_per_sample(cu_np, w.batch, w.seq_len, w.cp_size, r).sum())
-                      for r in w.ranks]
+    # roofline of the dominant kernel (largest share of the step), on this
+    # process's launches
     algo = {"fwd": 4, "dkdv": 8, "dq": 6}  # contractions over D per pair and head, x D
     dom = max(("fwd", "dkdv", "dq"), key=lambda n: kms[n])
-    algo_flops = w.n_heads * (sum(per_rank_pairs) / len(w.ranks)) * algo[dom] * w.head_dim
+    mean_pairs = sum(U["pairs"] for U in units) / len(units)
+    algo_flops = w.n_heads * mean_pairs * algo[dom] * w.head_dim
     achieved = algo_flops / (kms[dom] * 1e-3) / 1e12
     peaks = measured_peaks()
     peak = peaks.get("bf16_tflops")
     peak_src = "measured burst (MEASURED_PEAKS.json bf16_tflops)"
     if not peak:
         peak, peak_src = FALLBACK_BF16_TFLOPS, "fallback"
+    hbm_peak = peaks.get("hbm_gbs")
+    abytes = algorithmic_bytes(w, dom)
+    traffic = profiled_traffic(dom, w.name)
     roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-            "traffic": profiled_traffic(dom, w.name),
-            "algorithmic_flops_per_launch": algo_flops,
+            "traffic": traffic, "algorithmic_flops_per_launch": algo_flops,
+            "algorithmic_bytes": abytes,
+            "traffic_over_algorithmic": (traffic / abytes) if traffic else None,
+            # the same launch against the HBM roofline (the second bound that
+            # matters where masks leave little work per byte)
+            "hbm_achieved_gbs": abytes / (kms[dom] * 1e-3) / 1e9,
+            "hbm_frac": (abytes / (kms[dom] * 1e-3) / 1e9 / hbm_peak) if hbm_peak else None,
             "kernel_ms": {n: round(kms[n], 5) for n in names}}
 
     # the HBM-bound parts against the measured copy bandwidth: Delta, and the
     # planner (latency-bound: a handful of small launches)
-    hbm_peak = peaks.get("hbm_gbs")
     hbm = {"peak_gbs": hbm_peak, "peak_source": "measured copy (MEASURED_PEAKS.json hbm_gbs)"}
     db = delta_bytes(w)
     hbm["delta"] = {"bytes": db, "ms": kms["delta"], "gbs": db / (kms["delta"] * 1e-3) / 1e9}
     try:
-        listed = [int(dma.plan_arrays(R["plan"])["row_ptr"][-1]) for R in ranks]
-        pb = sum(plan_bytes(w, len(cu_np) - 1, n) for n in listed) / len(listed)
+        listed = [int(dma.plan_arrays(U["plan"])["row_ptr"][-1]) for U in units]
+        n_docs = len(cu_of[units[0]["c"]]) - 1
+        pb = sum(plan_bytes(w, n_docs, n) for n in listed) / len(listed)
         hbm["plan"] = {"bytes": pb, "ms": kms["plan"], "gbs": pb / (kms["plan"] * 1e-3) / 1e9,
                        "note": "latency-bound: one memset and four small launches"}
     except Exception as exc:  # the line is printed regardless
@@ -504,35 +601,45 @@ def run_gpu(args, w: wl.Workload):
         if hbm_peak and "gbs" in hbm[part]:
             hbm[part]["frac"] = hbm[part]["gbs"] / hbm_peak
     # the same step counted without the backward's recompute (4D + 8D per pair)
-    mfu_value = world * flops_of(w, cu_np, w.ranks, fwd=4, bwd=8) / (ms * 1e-3) / 1e12
+    flops_mfu = sum(flops_of(copy_of[c], cu_of[c], (r,), fwd=4, bwd=8)
+                    for sh in shares for c, r in sh)
+    mfu_value = flops_mfu / (ms * 1e-3) / 1e12
     mfu = {"value": mfu_value, "unit": UNIT, "count": "4D fwd + 8D bwd per pair and head",
            "pct_of_measured_peak": 100.0 * mfu_value / world / peak}
 
     # end to end through the public API: pinned host inputs -> device -> step ->
     # results back to pinned host memory, every step
-    e2e = run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world)
+    e2e = run_e2e(args, w, dma, dev, mine, copy_of, cu_of, inputs_of, flops_job, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inputs = inputs_of[0]
+        rows = oracle_sample_rows(w, inputs, cu_of[0], CPU_BASELINE_TARGET_S)
         t0 = time.perf_counter()
-        fl, threads = oracle_sample_step(w, inputs, cu_np)
+        fl, threads = oracle_sample_step(w, inputs, cu_of[0], rows=rows)
         dt = time.perf_counter() - t0
-        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-               "kind": "oracle", "threads": threads, **host_description(),
-               "sample": (f"sample 0, query heads 0-{w.group - 1} (K/V head 0), rank "
-                          f"{w.ranks[0]}, all {w.local_len} local rows, fwd+bwd, "
-                          f"{dt:.1f} s, float64 numpy")}
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "threads": threads, "cores_available": os.cpu_count(), **host_description(),
+               "sample": f"{sample_text(w, rows)}, {dt:.1f} s"}
 
     if rank == 0:
+        slowest = max(per_unit_all, key=lambda u: u["ms_total"])
+        fastest = min(per_unit_all, key=lambda u: u["ms_total"])
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+            "higher_is_better": True, "scaling": scaling_kind(world, copies),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_of(w), copies=copies,
+                           units_per_process=[[list(u) for u in sh] for sh in shares]),
             "pct_of_measured_peak": 100.0 * value / world / peak,
             "pct_of_datasheet_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
             "roofline": roof, "mfu_style": mfu, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": kernels_per_rank_step(w) * len(w.ranks) * args.steps,
+            "per_rank": per_unit_all,
+            "rank_imbalance": {"slowest_over_fastest": slowest["ms_total"] / fastest["ms_total"],
+                               "slowest": [slowest["copy"], slowest["rank"]],
+                               "fastest": [fastest["copy"], fastest["rank"]]},
+            "gpu_launches": kernels_per_rank_step(w) * len(units) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -542,25 +649,28 @@ def run_gpu(args, w: wl.Workload):
     return 0
 
 
-def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
+def run_e2e(args, w, dma, dev, mine, copy_of, cu_of, inputs_of, flops_job, world):
     import torch
     steps = max(3, min(args.steps, 20))
-    h_k = inputs["k"].pin_memory()
-    h_v = inputs["v"].pin_memory()
-    h_cu = torch.from_numpy(cu_np).pin_memory()
     per = []
-    for r in w.ranks:
+    host_kv = {}
+    for c in sorted(inputs_of):
+        host_kv[c] = {"k": inputs_of[c]["k"].pin_memory(), "v": inputs_of[c]["v"].pin_memory(),
+                      "cu": torch.from_numpy(cu_of[c]).pin_memory()}
+    for c, r in mine:
         pos = torch.from_numpy(local_positions(w.seq_len, w.cp_size, r))
-        h_q = inputs["q"][:, pos].contiguous().pin_memory()
-        h_do = inputs["do"][:, pos].contiguous().pin_memory()
+        h_q = inputs_of[c]["q"][:, pos].contiguous().pin_memory()
+        h_do = inputs_of[c]["do"][:, pos].contiguous().pin_memory()
+        h_k = host_kv[c]["k"]
         outs = {"o": torch.empty(h_q.shape, dtype=torch.float32).pin_memory(),
                 "lse": torch.empty(w.batch, w.n_heads, w.local_len).pin_memory(),
                 "dq": torch.empty_like(h_q).pin_memory(),
                 "dk": torch.empty(h_k.shape, dtype=torch.float32).pin_memory(),
                 "dv": torch.empty(h_k.shape, dtype=torch.float32).pin_memory()}
-        per.append((r, h_q, h_do, outs))
-    h2d = h_k.nbytes + h_v.nbytes + h_cu.nbytes + sum(p[1].nbytes + p[2].nbytes for p in per)
-    d2h = sum(sum(t.nbytes for t in p[3].values()) for p in per)
+        per.append((c, r, h_q, h_do, outs))
+    h2d = sum(t.nbytes for kv in host_kv.values() for t in kv.values()) + \
+        sum(p[2].nbytes + p[3].nbytes for p in per)
+    d2h = sum(sum(t.nbytes for t in p[4].values()) for p in per)
 
     # Within a step the copies overlap the compute: inputs come in on one
     # stream (dO after q, k, v, so that the forward starts first), the
@@ -574,23 +684,22 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
     def one():
         s_in.wait_stream(stream)
         with torch.cuda.stream(s_in):
-            cu = h_cu.to(dev, non_blocking=True)
-            k = h_k.to(dev, non_blocking=True)
-            v = h_v.to(dev, non_blocking=True)
-            qs = [h_q.to(dev, non_blocking=True) for _, h_q, _, _ in per]
+            kv = {c: {n: t.to(dev, non_blocking=True) for n, t in hk.items()}
+                  for c, hk in host_kv.items()}
+            qs = [h_q.to(dev, non_blocking=True) for _, _, h_q, _, _ in per]
             ev_qkv = torch.cuda.Event()
             ev_qkv.record(s_in)
-            dos = [h_do.to(dev, non_blocking=True) for _, _, h_do, _ in per]
+            dos = [h_do.to(dev, non_blocking=True) for _, _, _, h_do, _ in per]
             ev_do = torch.cuda.Event()
             ev_do.record(s_in)
-        for t in [cu, k, v] + qs + dos:
+        for t in [t for d in kv.values() for t in d.values()] + qs + dos:
             t.record_stream(stream)
         stream.wait_event(ev_qkv)
         fwd_out = []
-        for (r, h_q, h_do, outs), q in zip(per, qs):
-            plan = dma.dma_plan(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
-                                w.head_dim)
-            o, lse = dma.dma_attn_fwd(plan, q, k, v)
+        for (c, r, h_q, h_do, outs), q in zip(per, qs):
+            plan = dma.dma_plan(kv[c]["cu"], w.batch, w.seq_len, w.cp_size, r, w.n_heads,
+                                w.n_kv_heads, w.head_dim)
+            o, lse = dma.dma_attn_fwd(plan, q, kv[c]["k"], kv[c]["v"])
             ev = torch.cuda.Event()
             ev.record(stream)
             s_out.wait_event(ev)
@@ -601,8 +710,8 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
             lse.record_stream(s_out)
             fwd_out.append((plan, o, lse))
         stream.wait_event(ev_do)
-        for (r, h_q, h_do, outs), q, do, (plan, o, lse) in zip(per, qs, dos, fwd_out):
-            dq, dk, dv = dma.dma_attn_bwd(plan, q, k, v, o, lse, do)
+        for (c, r, h_q, h_do, outs), q, do, (plan, o, lse) in zip(per, qs, dos, fwd_out):
+            dq, dk, dv = dma.dma_attn_bwd(plan, q, kv[c]["k"], kv[c]["v"], o, lse, do)
             ev = torch.cuda.Event()
             ev.record(stream)
             s_out.wait_event(ev)
@@ -635,7 +744,7 @@ def run_e2e(args, w, dma, dev, stream, cu_np, inputs, flops_step, world):
         torch.cuda.synchronize(dev)
         runs.append(a.elapsed_time(b) / steps)
     ms = reduce_max(sorted(runs)[1], world, dev)
-    return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": UNIT,
+    return {"value": flops_job / (ms * 1e-3) / 1e12, "unit": UNIT,
             "ms_per_step": ms, "steps": steps, "runs_ms_per_step": [round(x, 4) for x in runs],
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 

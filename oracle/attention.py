@@ -87,6 +87,7 @@ def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
     q_local, do_local : [B, Lq, Hq, D], this rank's query rows in local order
                         (chunk i, then chunk 2*CP-1-i).
     k, v              : [B, S, Hkv, D], full sequence, natural order.
+    threads           : worker threads, each taking (head, row block) units
     rows              : optional local row indices; then only o / lse / dq
                         of those rows are computed (others are NaN) and no
                         dk / dv is returned (they need every row), unless
@@ -125,33 +126,37 @@ def attention(q_local, k, v, cu_doc_lens, cp_size: int, cp_rank: int,
             c0, c1 = int(cols[0]), int(cols[-1]) + 1
             blocks.append((b, lr, c0, c1, mask_all[:, c0:c1]))
 
-    def run_heads(heads):
+    # work units (head, row block), dealt round-robin to the threads; each
+    # thread keeps its own dK / dV partial sums, added at the end
+    units = [(h, i) for h in range(Hq) for i in range(len(blocks))]
+
+    def run_units(mine):
         dk_part = np.zeros((B, S, Hkv, D)) if (do is not None and full) else None
         dv_part = np.zeros((B, S, Hkv, D)) if (do is not None and full) else None
-        for h in heads:
+        for h, i in mine:
             kvh = h // g
-            for (b, lr, c0, c1, mask) in blocks:
-                qb = q[b, lr, h]
-                kc = kk[b, c0:c1, kvh]
-                vc = vv[b, c0:c1, kvh]
-                dob = None if do is None else do[b, lr, h]
-                ob, lb, dqb, dkc, dvc = _rows_block(qb, kc, vc, mask, scale, dob)
-                o[b, lr, h] = ob
-                lse[b, h, lr] = lb
-                if dob is not None:
-                    dq[b, lr, h] = dqb
-                    if full:
-                        dk_part[b, c0:c1, kvh] += dkc
-                        dv_part[b, c0:c1, kvh] += dvc
+            b, lr, c0, c1, mask = blocks[i]
+            qb = q[b, lr, h]
+            kc = kk[b, c0:c1, kvh]
+            vc = vv[b, c0:c1, kvh]
+            dob = None if do is None else do[b, lr, h]
+            ob, lb, dqb, dkc, dvc = _rows_block(qb, kc, vc, mask, scale, dob)
+            o[b, lr, h] = ob
+            lse[b, h, lr] = lb
+            if dob is not None:
+                dq[b, lr, h] = dqb
+                if full:
+                    dk_part[b, c0:c1, kvh] += dkc
+                    dv_part[b, c0:c1, kvh] += dvc
         return dk_part, dv_part
 
-    nthreads = max(1, min(threads, Hq))
-    groups = [list(range(w, Hq, nthreads)) for w in range(nthreads)]
+    nthreads = max(1, min(threads, len(units)))
+    shares = [units[w::nthreads] for w in range(nthreads)]
     if nthreads == 1:
-        parts = [run_heads(groups[0])]
+        parts = [run_units(shares[0])]
     else:
         with ThreadPoolExecutor(nthreads) as ex:
-            parts = list(ex.map(run_heads, groups))
+            parts = list(ex.map(run_units, shares))
 
     out = {"o": o, "lse": lse}
     if rows is not None and full and do is not None:

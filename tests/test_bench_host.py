@@ -26,13 +26,47 @@ def test_pair_count_matches_oracle(name):
     assert fl == ofl.counted_flops(tot, w.n_heads, w.head_dim)
 
 
-def test_rank_workloads_are_independent_problems():
+def test_copies_are_independent_problems():
     w = wl.WORKLOADS["8b"]
-    seeds = {bench.rank_workload(w, r).seed for r in range(8)}
+    seeds = {bench.copy_workload(w, c).seed for c in range(8)}
     assert len(seeds) == 8
-    assert bench.rank_workload(w, 0) == w
-    a = wl.cu_doc_lens(bench.rank_workload(w, 1))
+    assert bench.copy_workload(w, 0) == w
+    a = wl.cu_doc_lens(bench.copy_workload(w, 1))
     assert not np.array_equal(a, wl.cu_doc_lens(w))
+
+
+def test_units_split_the_emulated_ranks_then_add_copies():
+    # N <= R: the emulated ranks of one workload, rank r to process r mod N
+    shares, copies = bench.assign_units(4, (0, 1, 2, 3))
+    assert copies == 1 and shares == [[(0, 0)], [(0, 1)], [(0, 2)], [(0, 3)]]
+    assert bench.scaling_kind(4, copies) == "strong"
+    shares, copies = bench.assign_units(3, (0, 7, 15))
+    assert copies == 1 and shares == [[(0, 0)], [(0, 7)], [(0, 15)]]
+    shares, copies = bench.assign_units(2, (0, 1, 2, 3))
+    assert copies == 1 and shares == [[(0, 0), (0, 2)], [(0, 1), (0, 3)]]
+    # one emulated rank: every process gets its own copy (weak scaling)
+    shares, copies = bench.assign_units(8, (0,))
+    assert copies == 8 and shares == [[(c, 0)] for c in range(8)]
+    assert bench.scaling_kind(8, copies) == "weak"
+    assert bench.scaling_kind(1, 1) == "weak"
+    # every unit of the job is run exactly once
+    for world, ranks in [(3, (0, 1)), (5, (0, 7, 15)), (8, (0, 1, 2, 3))]:
+        shares, copies = bench.assign_units(world, ranks)
+        units = sorted(u for sh in shares for u in sh)
+        assert units == sorted((c, r) for c in range(copies) for r in ranks)
+        assert max(map(len, shares)) - min(map(len, shares)) <= 1
+
+
+def test_algorithmic_bytes_per_launch():
+    w = wl.WORKLOADS["8b"]
+    q = 2 * 8192 * 32 * 128 * 2          # bf16 q (or dO, dQ)
+    kv = 2 * 8192 * 8 * 128 * 2          # bf16 k (or v)
+    st = 2 * 32 * 8192 * 4               # fp32 LSE (or Delta)
+    # dK/dV: q, dO, k, v, LSE, Delta in; dK, dV fp32 out: about 473 MB
+    assert bench.algorithmic_bytes(w, "dkdv") == 2 * q + 2 * kv + 2 * st + 4 * kv
+    assert 472e6 < bench.algorithmic_bytes(w, "dkdv") < 474e6
+    assert bench.algorithmic_bytes(w, "dq") == 3 * q + 2 * kv + 2 * st
+    assert bench.algorithmic_bytes(w, "fwd") == q + 2 * kv + 2 * q + st
 
 
 def _free_port():
@@ -67,6 +101,66 @@ def test_two_gloo_ranks_take_the_max_step_time():
         p.join(timeout=120)
         assert p.exitcode == 0
     assert out[0] == out[1] == 3.5
+
+
+def _split_worker(rank, world, port, out):
+    """One process of a two-process run of the tiny workload: it takes the
+    emulated CP ranks bench.assign_units gives it, computes their outputs
+    (the oracle stands in for the kernels on CPU), and all processes gather
+    every rank's outputs."""
+    import torch.distributed as dist
+    from oracle import attention as oa
+    from oracle import cp as ocp
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = wl.WORKLOADS["tiny"]
+    shares, copies = bench.assign_units(world, w.ranks)
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    mine = {}
+    for c, r in shares[rank]:
+        assert c == 0
+        res = oa.attention(ocp.gather_local(inp["q"], w.seq_len, w.cp_size, r), inp["k"],
+                           inp["v"], cu, w.cp_size, r,
+                           do_local=ocp.gather_local(inp["do"], w.seq_len, w.cp_size, r))
+        mine[r] = res
+    gathered = [None] * world
+    dist.all_gather_object(gathered, mine)
+    if rank == 0:
+        out["ranks"] = [sorted(part) for part in gathered]
+        allr = {r: v for part in gathered for r, v in part.items()}
+        out["o"] = ocp.assemble_full({r: allr[r]["o"] for r in allr}, w.seq_len, w.cp_size)
+        out["dq"] = ocp.assemble_full({r: allr[r]["dq"] for r in allr}, w.seq_len, w.cp_size)
+        out["dk"] = sum(allr[r]["dk"] for r in allr)
+        out["dv"] = sum(allr[r]["dv"] for r in allr)
+    dist.destroy_process_group()
+
+
+def test_two_processes_split_the_emulated_ranks_and_reassemble():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    procs = [ctx.Process(target=_split_worker, args=(r, world, port, out))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+        assert p.exitcode == 0
+    # rank r of the workload ran on process r
+    assert out["ranks"] == [[0], [1]]
+    # the processes' outputs, put back in sequence order, are the whole
+    # sequence's attention (CP = 1), and the partial dK / dV sum to the full
+    from oracle import attention as oa
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.tensors(w)
+    full = oa.attention(inp["q"], inp["k"], inp["v"], wl.cu_doc_lens(w), 1, 0,
+                        do_local=inp["do"])
+    for key in ("o", "dq", "dk", "dv"):
+        assert np.allclose(out[key], full[key], rtol=1e-12, atol=1e-12), key
 
 
 def test_kernels_per_step_follow_the_planner():
