@@ -348,21 +348,18 @@ def sample_pairs(w: wl.Workload, cu0, rows=None) -> int:
 
 def oracle_sample_rows(w: wl.Workload, inputs: dict, cu, target_s: float):
     """Rows of the bounded oracle sample: the last local rows (the rank's
-    heaviest, at the end of its second chunk), as many as take about
-    `target_s` seconds, from a calibration run of 64 rows.  None = all."""
-    cu0 = np.asarray([x for x in cu if x <= w.seq_len], dtype=np.int64)
-    cal = np.arange(w.local_len - min(64, w.local_len), w.local_len)
-    t0 = time.perf_counter()
-    oracle_sample_step(w, inputs, cu, rows=cal)
-    per_pair = (time.perf_counter() - t0) / max(1, sample_pairs(w, cu0, cal))
-    budget_pairs = target_s / per_pair
-    if sample_pairs(w, cu0) <= budget_pairs:
-        return None
-    n = len(cal)
-    while n < w.local_len and sample_pairs(w, cu0, np.arange(w.local_len - 2 * n, w.local_len)) \
-            <= budget_pairs:
-        n *= 2
-    return np.arange(w.local_len - n, w.local_len)
+    heaviest, at the end of its second chunk), grown from 64 by trial runs
+    until one takes about `target_s` / 2 seconds or more.  None = all."""
+    n = min(64, w.local_len)
+    while n < w.local_len:
+        rows = np.arange(w.local_len - n, w.local_len)
+        t0 = time.perf_counter()
+        oracle_sample_step(w, inputs, cu, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 2:
+            return rows
+        n = min(w.local_len, n * max(2, min(8, int(target_s / max(dt, 1e-3)))))
+    return None
 
 
 def sample_text(w: wl.Workload, rows) -> str:

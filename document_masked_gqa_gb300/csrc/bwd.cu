@@ -148,13 +148,14 @@ __device__ __forceinline__ void ds_chunk32(const uint32_t* du, const uint32_t* p
 // dK/dV works a whole query tile at a time: S^T = K Q^T and dP^T = V dO^T
 // (128 keys x 128 query rows each, N = 128) land in TMEM buffers of their
 // own.  The element-wise warpgroups (thread = key, warpgroup w = query
-// columns [64w, 64w + 64)) first turn S^T into P^T and write it (bf16 pairs)
-// over the S^T columns they read, so that dV += P^T dO can start while
-// dP^T is still being computed; then they turn dP^T into dS^T the same way
-// for dK += dS^T Q.  Both are handed over in two halves (each warpgroup's
-// first 32 query columns, then the rest), so that dV and dK start on the
-// first half while the second is computed.  A buffer is rewritten once the
-// product that reads it is done: S^T after dV, dP^T after dK.
+// columns [64w, 64w + 64)) load S^T into registers, which frees its buffer
+// for the next tile's S^T at once, and turn it into P^T (bf16 pairs, kept in
+// registers).  Once dP^T is in, they load it, write P^T over the first half
+// of the dP^T columns they read (dV += P^T dO starts), then turn dP^T into
+// dS^T and write it over the second half (dK += dS^T Q starts, in two
+// halves).  The dP^T buffer is rewritten by the next tile's dP^T once dK,
+// and with it dV, is done.  So the next score tile never waits for dV: the
+// chain per tile is dP^T -> dS^T -> dV, dK -> next dP^T.
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;
@@ -173,7 +174,9 @@ struct DkdvCfg {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
-  // TMEM: dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512)
+  // TMEM: dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512); after
+  // dP^T has been read, warpgroup w's P^T sits in columns [384 + 64w,
+  // 384 + 64w + 32) and its dS^T in the next 32
   static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384;
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
@@ -235,12 +238,11 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* do_empty = bars + 7;   // [2]
   uint64_t* s_full = bars + 9;     // S^T of the current tile computed
   uint64_t* dp_full = bars + 10;   // dP^T computed
-  // P^T (dS^T) written over S^T (dP^T), per half: query columns [0, 32) and
-  // [64, 96) of the tile (each warpgroup's first 32), then the rest
-  uint64_t* p_full = bars + 11;    // [2]
-  uint64_t* ds_full = bars + 13;   // [2]
-  uint64_t* dv_done = bars + 15;   // dV += P^T dO done (the S^T buffer is free)
-  uint64_t* dk_done = bars + 16;   // dK += dS^T Q done (the dP^T buffer is free)
+  uint64_t* s_free = bars + 11;    // the element-wise warps hold S^T in registers
+  uint64_t* p_full = bars + 12;    // P^T written over the dP^T buffer
+  uint64_t* ds_full = bars + 13;   // [2] dS^T written, per half: query columns [0, 32)
+                                   // and [64, 96) of the tile, then the rest
+  uint64_t* dk_done = bars + 15;   // dV and dK of a tile done (the dP^T buffer is free)
   uint64_t* col_ready = bars + 17; // [2] per warpgroup: statistics staged
   uint64_t* acc_done = bars + 19;  // an item's dV, dK complete
   uint64_t* kv_empty = bars + 20;  // an item's last S^T and dP^T done (two commits)
@@ -256,12 +258,12 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
       mbar_init(&col_ready[i], 4);  // the four warps of the warpgroup
-      mbar_init(&p_full[i], 8);     // one arrival per element-wise warp
-      mbar_init(&ds_full[i], 8);
+      mbar_init(&ds_full[i], 8);    // one arrival per element-wise warp
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(dv_done, 1);
+    mbar_init(s_free, 8);
+    mbar_init(p_full, 8);
     mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
@@ -333,102 +335,20 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      // ------------------------------------------ MMA issuer: S^T, then dK
-      // per query tile t: S^T(t) = K Q^T into its buffer once dV(t-1) has read
-      // P^T(t-1) there, then dK(t-1) += dS^T Q: the tensor pipe takes S^T(t),
-      // on which the next element-wise phase waits, before dK(t-1).  (dS^T
-      // A operands from TMEM: warpgroup w's query columns [64w, 64w + 64) sit
-      // in TMEM columns [64w, 64w + 32) of the buffer, 8 per 16-deep step.)
+      // --------------------------------------- MMA issuers: S^T and dP^T
+      // warp 1: S^T(t) = K Q^T once the element-wise warps hold S^T(t-1) in
+      // registers.  warp 2: dP^T(t) = V dO^T once dV(t-1) and dK(t-1),
+      // which read P^T and dS^T from the dP^T buffer, are done.
+      const bool is_s = warp == 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t k_addr = smem_u32(sK);
-      uint64_t* last_commit = nullptr;
-      uint32_t last_parity = 0;
-      bool ok = true;
-      int tbase = 0, ibase = 0;
-      // the tile whose dK is still to be issued (-1: none), and whether it
-      // is the first / last of its item
-      int pk = -1;
-      bool pk_first = false, pk_last = false;
-      int acc_items = 0;  // acc_done phases committed
-      auto issue_dk = [&]() -> bool {
-        const uint32_t q_addr = smem_u32(sQ + (pk & 1) * Cfg::kTile);
-        // each half as soon as it is written: steps kk = 4w + 2h + {0, 1}
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(&ds_full[h], pk & 1, ctl)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
-            mma_f16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
-                       sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                       (!pk_first || kk > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(dk_done);
-        // dV(pk) is known complete (dv_done was awaited): Q, dO of tile pk
-        // are free once dK(pk) is, and so is the item's accumulator pair
-        mma_commit(&do_empty[pk & 1]);
-        mma_commit(&q_empty[pk & 1]);
-        last_commit = dk_done;
-        last_parity = pk & 1;
-        if (pk_last) {
-          mma_commit(acc_done);
-          last_commit = acc_done;
-          last_parity = acc_items & 1;
-          ++acc_items;
-        }
-        return true;
-      };
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
-        const DkdvItem it = dkdv_item(p, item);
-        if (it.n == 0) continue;
-        if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
-        for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, st = ig & 1;
-          if (ig >= 1 && !mbar_wait(dv_done, (ig - 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&q_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_bf16_ss(tmem + Cfg::kTmemS, sdesc_sw128(k_addr + off, 16, 1024),
-                        sdesc_sw128(q_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(s_full);
-          last_commit = s_full;
-          last_parity = ig & 1;
-          if (pk >= 0) {
-            if (!issue_dk()) { ok = false; break; }
-          }
-          pk = ig;
-          pk_first = i == 0;
-          pk_last = i == it.n - 1;
-        }
-        if (!ok) break;
-        mma_commit(kv_empty);  // this item's K reads are done once these complete
-        tbase += it.n;
-        ++ibase;
-      }
-      if (ok && pk >= 0) {  // the CTA's last tile
-        if (!mbar_wait(dv_done, pk & 1, ctl)) ok = false;
-        else if (!issue_dk()) ok = false;
-      }
-      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
-    }
-  } else if (warp == 2) {
-    if (lane == 0) {
-      // ------------------------------------------------- MMA issuer: dP^T
-      // per query tile: dP^T = V dO^T into its buffer once dK of the previous
-      // tile has read dS^T there
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t v_addr = smem_u32(sV);
+      const uint32_t a_addr = smem_u32(is_s ? sK : sV);
+      uint8_t* const b_tiles = is_s ? sQ : sDO;
+      uint64_t* const b_full = is_s ? q_full : do_full;
+      uint64_t* const free_bar = is_s ? s_free : dk_done;
+      uint64_t* const done_bar = is_s ? s_full : dp_full;
+      const uint32_t d_tmem = tmem + (is_s ? Cfg::kTmemS : Cfg::kTmemDP);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
@@ -441,22 +361,22 @@ __global__ void __launch_bounds__(512, 1)
         if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
         for (int i = 0; i < it.n; ++i) {
           const int ig = tbase + i, st = ig & 1;
-          if (ig >= 1 && !mbar_wait(dk_done, (ig - 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
+          if (ig >= 1 && !mbar_wait(free_bar, (ig - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&b_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(sDO + st * Cfg::kTile);
+          const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_bf16_ss(tmem + Cfg::kTmemDP, sdesc_sw128(v_addr + off, 16, 1024),
+            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + off, 16, 1024),
                         sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(dp_full);
-          last_commit = dp_full;
+          mma_commit(done_bar);
+          last_commit = done_bar;
           last_parity = ig & 1;
         }
         if (!ok) break;
-        mma_commit(kv_empty);  // this item's V reads are done once these complete
+        mma_commit(kv_empty);  // this item's K (V) reads are done once these complete
         tbase += it.n;
         ++ibase;
       }
@@ -464,9 +384,11 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 3) {
     if (lane == 0) {
-      // --------------------------------------------------- MMA issuer: dV
-      // dV += P^T dO once P^T is in TMEM (A operand from TMEM, laid out as
-      // for dK above)
+      // ------------------------------------------- MMA issuer: dV, then dK
+      // once P^T is in the dP^T buffer: dV += P^T dO; then dK += dS^T Q, each
+      // half of dS^T as soon as it is written (A operands from TMEM:
+      // warpgroup w's query columns [64w, 64w + 64) sit in 32 columns of the
+      // buffer, 8 per 16-deep step).  The commit after dK covers dV too.
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
@@ -482,26 +404,44 @@ __global__ void __launch_bounds__(512, 1)
           // the item's first products overwrite dV, dK: the previous item's
           // must have been read out by the epilogue warps
           if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-          // P^T follows from Q alone: dO may still be on its way
           if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&q_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(p_full, ig & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
           const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
-          // each half of P^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
+          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                       sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+          // each half of dS^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(&p_full[h], ig & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&ds_full[h], ig & 1, ctl)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
-              mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + 64 * (kk >> 2) + 8 * (kk & 3),
-                         sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+              mma_f16_ts(tmem + Cfg::kTmemDK,
+                         tmem + Cfg::kTmemDP + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
+                         sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                          (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
           if (!ok) break;
-          mma_commit(dv_done);
-          last_commit = dv_done;
+          mma_commit(dk_done);
+          // S^T and dP^T of this tile completed before P^T / dS^T existed:
+          // its Q and dO are free once dV and dK are
+          mma_commit(&do_empty[st]);
+          mma_commit(&q_empty[st]);
+          last_commit = dk_done;
           last_parity = ig & 1;
+          if (i == it.n - 1) {
+            mma_commit(acc_done);
+            last_commit = acc_done;
+            last_parity = ibase & 1;
+          }
         }
         if (!ok) break;
         tbase += it.n;
@@ -571,8 +511,9 @@ __global__ void __launch_bounds__(512, 1)
         const bool masked = (e & kPartialBit) != 0;
         const float4* nlse_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128);
         const float4* del_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128 + 64);
-        // phase 1: P^T over S^T.  All 64 columns come in with one wait: a
-        // TMEM load takes hundreds of cycles while the tensor pipe is busy.
+        // phase 1: P^T from S^T.  All 64 columns come in with one wait (a
+        // TMEM load takes hundreds of cycles while the tensor pipe is busy);
+        // once they are in registers the S^T buffer can take the next tile.
         if (!warp_wait(s_full, ig & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         uint32_t pb[32];  // P of the 64 columns as bf16 pairs
@@ -583,8 +524,7 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld();
           reg_fence32(su);
           reg_fence32(su + 32);
-          // each half (32 columns) is written over the first 16 of the S^T
-          // columns and handed to dV as soon as it is done
+          warp_arrive(s_free);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (masked)
@@ -593,13 +533,10 @@ __global__ void __launch_bounds__(512, 1)
                               pb + 16 * h);
             else
               p_chunk32<false>(su + 32 * h, nlse_c + 8 * h, 0u, sl2, pb + 16 * h);
-            tmem_st8_nowait(s_cols + 16 * h, pb + 16 * h);
-            tmem_st8_nowait(s_cols + 16 * h + 8, pb + 16 * h + 8);
-            tmem_wait_st();
-            warp_arrive(&p_full[h]);
           }
         }
-        // phase 2: dS^T over dP^T
+        // phase 2: load dP^T, write P^T over its first 32 columns (dV starts),
+        // then dS^T over the other 32, in two halves (dK starts on each)
         if (!warp_wait(dp_full, ig & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         {
@@ -610,11 +547,15 @@ __global__ void __launch_bounds__(512, 1)
           reg_fence32(du);
           reg_fence32(du + 32);
 #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_st8_nowait(dp_cols + 8 * q4, pb + 8 * q4);
+          tmem_wait_st();
+          warp_arrive(p_full);
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t pd[16];
             ds_chunk32(du + 32 * h, pb + 16 * h, del_c + 8 * h, pd);
-            tmem_st8_nowait(dp_cols + 16 * h, pd);
-            tmem_st8_nowait(dp_cols + 16 * h + 8, pd + 8);
+            tmem_st8_nowait(dp_cols + 32 + 16 * h, pd);
+            tmem_st8_nowait(dp_cols + 32 + 16 * h + 8, pd + 8);
             tmem_wait_st();
             warp_arrive(&ds_full[h]);
           }

@@ -121,9 +121,15 @@ def test_v_saturation_and_nan_propagation():
         sees = lambda key: (ids[qpos] == ids[key]) & (qpos >= key)  # noqa: E731
         # LSE does not depend on V
         assert np.isfinite(lse).all() and max_abs(lse, ref["lse"]) <= TOL_LSE
-        # every column but the NaN's matches the oracle on the saturated V
-        cols = [c for c in range(w.head_dim) if c != 5]
+        # every column without the NaN or a saturated value matches the
+        # oracle on the saturated V
+        cols = [c for c in range(w.head_dim) if c not in (5, 7, 9)]
         assert max_abs(o[..., cols], ref["o"][..., cols]) <= TOL_O, r
+        # the saturated columns too, within the fp16 rounding of P times
+        # 65504 (relative 2^-11 of the term that value contributes)
+        for c in (7, 9):
+            err = np.abs(o[..., c].astype(np.float64) - ref["o"][..., c])
+            assert (err <= TOL_O + 2.0 ** -10 * np.abs(ref["o"][..., c])).all(), (r, c)
         # the NaN reaches column 5 of every row that attends its key ...
         rows_b = np.nonzero(sees(kb))[0]
         assert len(rows_b) > 0 or r == 1
@@ -137,4 +143,4 @@ def test_v_saturation_and_nan_propagation():
         # rows that attend the saturated key see +-65504 there
         rows_a = np.nonzero(sees(ka))[0]
         assert len(rows_a) > 0 or r == 0
-        assert np.isfinite(o[0, rows_a][..., cols]).all()
+        assert np.isfinite(o[0, rows_a][..., [c for c in range(w.head_dim) if c != 5]]).all()
