@@ -80,6 +80,10 @@ WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int
   w.bwd_order = take(4 * B * nkt);
   w.delta = take(4 * B * static_cast<size_t>(n_heads) * Lq);
   w.v16 = take(2 * B * static_cast<size_t>(seq_len) * n_kv_heads * head_dim);
+  const int segs = dma::kv_segments(batch, seq_len, n_kv_heads);
+  w.kv_part = take(segs > 1 ? 2 * static_cast<size_t>(segs) * 4 * B * static_cast<size_t>(seq_len) *
+                                  n_kv_heads * head_dim
+                            : 0);
   w.total = off;
   return w;
 }
@@ -121,11 +125,12 @@ dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p,
   return encode(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// dK / dV (fp32 [B*S][Hkv*D]) as TMA store targets: box = 32 columns x 32
-// key rows, 128-byte swizzled (one warp's block of the epilogue).
-dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p) {
+// dK / dV (fp32 [B*S][Hkv*D], or `segs` such partials one after another) as
+// TMA store targets: box = 32 columns x 32 key rows, 128-byte swizzled (one
+// warp's block of the epilogue).
+dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p, int segs = 1) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim,
-                              static_cast<cuuint64_t>(p.batch) * p.seq_len};
+                              static_cast<cuuint64_t>(segs) * p.batch * p.seq_len};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim * 4};
   const cuuint32_t box[2] = {32, 32};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
@@ -189,6 +194,8 @@ dma_status init_plan(dma_plan_s& pl, const int32_t* cu_doc_lens, int n_docs, int
   p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
   p.delta = reinterpret_cast<float*>(ws + w.delta);
   p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+  p.kv_segs = dma::kv_segments(batch, seq_len, n_kv_heads);
+  p.kv_part = p.kv_segs > 1 ? reinterpret_cast<float*>(ws + w.kv_part) : nullptr;
   pl.cu = cu_doc_lens;
   pl.n_docs = n_docs;
   if (cudaGetDevice(&pl.device) != cudaSuccess ||
@@ -297,10 +304,20 @@ dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16*
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
   CUtensorMap tdk, tdv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.kv_segs > 1) {
+    // per-segment partials into the workspace, then their ordered sum
+    const size_t n = static_cast<size_t>(p.batch) * p.seq_len * p.n_kv_heads * p.head_dim;
+    if ((st = map_kv_out_f32(&tdk, p.kv_part, p, p.kv_segs)) != DMA_OK) return st;
+    if ((st = map_kv_out_f32(&tdv, p.kv_part + p.kv_segs * n, p, p.kv_segs)) != DMA_OK)
+      return st;
+    if (dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv, s) != cudaSuccess)
+      return DMA_ERR_CUDA;
+    return dma::launch_kv_reduce(*plan, dk, dv, s) == cudaSuccess ? DMA_OK : DMA_ERR_CUDA;
+  }
   if ((st = map_kv_out_f32(&tdk, dk, p)) != DMA_OK) return st;
   if ((st = map_kv_out_f32(&tdv, dv, p)) != DMA_OK) return st;
-  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv,
-                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv, s) == cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;
 }

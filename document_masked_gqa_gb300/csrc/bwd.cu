@@ -170,7 +170,7 @@ struct DkdvCfg {
   static constexpr int kStage = kDO + 2 * kTile;
   static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
   static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 22;
+  static constexpr int kNumBars = 24;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -182,21 +182,27 @@ struct DkdvCfg {
 };
 
 // Work item `item` of the dK/dV pass: (sample, key tile) in longest-list-first
-// order times K/V head (the heads of one key tile side by side).
+// order, times the segment of its query-tile list (kv_segs of them, each a
+// contiguous share of the list), times K/V head (the heads of one key tile
+// side by side).  `seg` also selects the partial the item writes.
 struct DkdvItem {
-  int b, kvh, kt, n;
+  int b, kvh, kt, n, seg;
   const int32_t* list;
 };
 __device__ __forceinline__ DkdvItem dkdv_item(const PlanDev& p, int item) {
   DkdvItem it;
-  const int ord = item / p.n_kv_heads;
+  const int ns = p.kv_segs;
+  const int ord = item / (p.n_kv_heads * ns);
+  it.seg = (item / p.n_kv_heads) % ns;
   it.kvh = item % p.n_kv_heads;
   const int bk = p.bwd_order[ord];
   it.b = bk / p.n_ktiles;
   it.kt = bk % p.n_ktiles;
   const int cp0 = p.col_ptr[bk];
-  it.n = p.col_ptr[bk + 1] - cp0;
-  it.list = p.col_idx + cp0;
+  const int n_all = p.col_ptr[bk + 1] - cp0;
+  const int lo = (it.seg * n_all) / ns, hi = ((it.seg + 1) * n_all) / ns;
+  it.n = hi - lo;
+  it.list = p.col_idx + cp0 + lo;
   return it;
 }
 
@@ -247,6 +253,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* acc_done = bars + 19;  // an item's dV, dK complete
   uint64_t* kv_empty = bars + 20;  // an item's last S^T and dP^T done (two commits)
   uint64_t* acc_free = bars + 21;  // the epilogue warps have read an item's dV, dK
+  // [2] dP^T of tile t issued (barrier t % 2: the next S^T is issued behind
+  // it; one barrier per tile parity, so that it can never run two phases
+  // ahead of the S^T issuer's wait)
+  uint64_t* dp_issued = bars + 22;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -265,6 +275,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(s_free, 8);
     mbar_init(p_full, 8);
     mbar_init(dk_done, 1);
+    mbar_init(&dp_issued[0], 1);
+    mbar_init(&dp_issued[1], 1);
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
     mbar_init(acc_free, 4);
@@ -339,8 +351,12 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       // --------------------------------------- MMA issuers: S^T and dP^T
       // warp 1: S^T(t) = K Q^T once the element-wise warps hold S^T(t-1) in
-      // registers.  warp 2: dP^T(t) = V dO^T once dV(t-1) and dK(t-1),
-      // which read P^T and dS^T from the dP^T buffer, are done.
+      // registers and dP^T(t-1) has been issued.  warp 2: dP^T(t) = V dO^T
+      // once dV(t-1) and dK(t-1), which read P^T and dS^T from the dP^T
+      // buffer, are done.  The tensor pipe takes products in issue order,
+      // and dP^T(t-1) is on the critical chain (dP^T -> dS^T -> dV, dK ->
+      // next dP^T) while S^T(t) is not: S^T(t) then runs while the
+      // element-wise warps turn dP^T(t-1) into P^T, instead of delaying it.
       const bool is_s = warp == 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t a_addr = smem_u32(is_s ? sK : sV);
@@ -362,6 +378,8 @@ __global__ void __launch_bounds__(512, 1)
         for (int i = 0; i < it.n; ++i) {
           const int ig = tbase + i, st = ig & 1;
           if (ig >= 1 && !mbar_wait(free_bar, (ig - 1) & 1, ctl)) { ok = false; break; }
+          if (is_s && ig >= 1 &&
+              !mbar_wait(&dp_issued[(ig - 1) & 1], ((ig - 1) >> 1) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(&b_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
           const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile);
@@ -371,6 +389,7 @@ __global__ void __launch_bounds__(512, 1)
             mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + off, 16, 1024),
                         sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
+          if (!is_s) mbar_arrive(&dp_issued[ig & 1]);
           mma_commit(done_bar);
           last_commit = done_bar;
           last_parity = ig & 1;
@@ -579,7 +598,7 @@ __global__ void __launch_bounds__(512, 1)
       const int item = snake_item(k);
       if (item >= n_items) continue;
       const DkdvItem it = dkdv_item(p, item);
-      const int row0 = it.b * p.seq_len + it.kt * kTileN + 32 * wq;
+      const int row0 = (it.seg * p.batch + it.b) * p.seq_len + it.kt * kTileN + 32 * wq;
       const bool empty = it.n == 0;
       if (!empty) {
         if (!warp_wait(acc_done, ibase & 1, ctl)) { ok = false; break; }
@@ -1096,6 +1115,23 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
+// dK, dV = the sum of the kv_segs partials, added in segment order (the
+// same on every run).  4 elements per thread.
+__global__ void kv_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ dk,
+                                 float4* __restrict__ dv, long long n4, int segs) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float4 a = part[i], b = part[segs * n4 + i];
+    for (int s = 1; s < segs; ++s) {
+      const float4 x = part[s * n4 + i], y = part[(segs + s) * n4 + i];
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    }
+    dk[i] = a;
+    dv[i] = b;
+  }
+}
+
 template <int D>
 cudaError_t launch_delta_d(const dma_plan_s& pl, const float* o, const dma_bf16* dout,
                            cudaStream_t s) {
@@ -1114,7 +1150,7 @@ cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensor
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  const int items = p.batch * p.n_ktiles * p.n_kv_heads;
+  const int items = p.batch * p.n_ktiles * p.n_kv_heads * p.kv_segs;
   if (items == 0) return cudaSuccess;
   // persistent: one CTA per SM (TMEM and shared memory allow no more)
   const int grid = items < pl.num_sms ? items : pl.num_sms;
@@ -1155,6 +1191,19 @@ cudaError_t launch_dkdv(const dma_plan_s& pl, const float* lse, const CUtensorMa
                         const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
   return pl.d.head_dim == 128 ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s)
                               : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s);
+}
+
+cudaError_t launch_kv_reduce(const dma_plan_s& pl, float* dk, float* dv, cudaStream_t s) {
+  const PlanDev& p = pl.d;
+  const long long n4 =
+      static_cast<long long>(p.batch) * p.seq_len * p.n_kv_heads * p.head_dim / 4;
+  if (n4 == 0) return cudaSuccess;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 8LL * pl.num_sms) blocks = 8LL * pl.num_sms;
+  kv_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(p.kv_part), reinterpret_cast<float4*>(dk),
+      reinterpret_cast<float4*>(dv), n4, p.kv_segs);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,

@@ -15,6 +15,20 @@ constexpr int kTileN = 128;  // key positions per tile
 constexpr uint32_t kPartialBit = 0x80000000u;
 constexpr uint32_t kIndexMask = 0x7FFFFFFFu;
 
+// dK/dV work items are (key tile, K/V head).  When a shape has fewer than
+// kKvSplitItems of them (a short sequence with one K/V head, say), most SMs
+// would idle, so each key tile's list of query tiles is cut into segments,
+// up to kKvMaxSegs, each its own work item writing an fp32 partial of dK, dV;
+// a reduction sums the partials in segment order.
+constexpr int kKvSplitItems = 256;
+constexpr int kKvMaxSegs = 8;
+__host__ __device__ inline int kv_segments(int batch, int seq_len, int n_kv_heads) {
+  const long long items = static_cast<long long>(batch) * (seq_len / kTileN) * n_kv_heads;
+  if (items <= 0 || items >= kKvSplitItems) return 1;
+  const long long s = (kKvSplitItems + items - 1) / items;
+  return static_cast<int>(s < kKvMaxSegs ? s : kKvMaxSegs);
+}
+
 // Device-visible shape and workspace pointers of one rank's plan.
 struct PlanDev {
   int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
@@ -38,11 +52,13 @@ struct PlanDev {
   int32_t* bwd_order; // [B*nKt]
   float* delta;       // [B][Hq][Lq]
   uint16_t* v16;      // [B][S][Hkv][D] fp16 copy of V for the forward's P V
+  int kv_segs;        // segments per key tile's query list (kv_segments)
+  float* kv_part;     // kv_segs > 1: [2][kv_segs][B][S][Hkv][D] partial dK, then dV
 };
 
 struct WorkspaceLayout {
   size_t status, qpos, doc_lo, doc_hi, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
-      col_ptr, col_idx, fwd_order, bwd_order, delta, v16, total;
+      col_ptr, col_idx, fwd_order, bwd_order, delta, v16, kv_part, total;
 };
 
 }  // namespace dma
@@ -82,6 +98,7 @@ cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap
 cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s);
+cudaError_t launch_kv_reduce(const dma_plan_s& p, float* dk, float* dv, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s);
 }  // namespace dma

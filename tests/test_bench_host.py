@@ -165,8 +165,15 @@ def test_two_processes_split_the_emulated_ranks_and_reassemble():
 
 def test_kernels_per_step_follow_the_planner():
     # four planner kernels, V to fp16 + forward, Delta + dK/dV + dQ
-    for name in ["tiny", "8b", "70b", "sparse", "405b-1doc"]:
+    for name in ["8b", "sparse", "405b-1doc"]:
         assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 9
+    # fewer than 256 (key tile, K/V head) items: the dK/dV lists are split
+    # and a tenth kernel sums the partials (tiny: 2 items, 70b: 64)
+    assert bench.kv_segments(wl.WORKLOADS["tiny"]) == 8
+    assert bench.kv_segments(wl.WORKLOADS["70b"]) == 4
+    assert bench.kv_segments(wl.WORKLOADS["8b"]) == 1
+    for name in ["tiny", "70b"]:
+        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 10
     # launch orders over 2048 units take one extra ranking kernel each: the
     # 128K single-rank workload has 16384 query tiles of 8 positions
     assert bench.kernels_per_rank_step(wl.WORKLOADS["causal-128k"]) == 10
