@@ -145,17 +145,18 @@ __device__ __forceinline__ void ds_chunk32(const uint32_t* du, const uint32_t* p
 }
 
 //
-// dK/dV works a whole query tile at a time: S^T = K Q^T and dP^T = V dO^T
-// (128 keys x 128 query rows each, N = 128) land in TMEM buffers of their
-// own.  The element-wise warpgroups (thread = key, warpgroup w = query
-// columns [64w, 64w + 64)) load S^T into registers, which frees its buffer
-// for the next tile's S^T at once, and turn it into P^T (bf16 pairs, kept in
-// registers).  Once dP^T is in, they load it, write P^T over the first half
-// of the dP^T columns they read (dV += P^T dO starts), then turn dP^T into
-// dS^T and write it over the second half (dK += dS^T Q starts, in two
-// halves).  The dP^T buffer is rewritten by the next tile's dP^T once dK,
-// and with it dV, is done.  So the next score tile never waits for dV: the
-// chain per tile is dP^T -> dS^T -> dV, dK -> next dP^T.
+// dK/dV works a whole query tile at a time.  Query tiles alternate between
+// two 128-column TMEM buffers: tile t uses buffer t % 2 for S^T = K Q^T,
+// then for dP^T = V dO^T, then for P^T and dS^T.  The element-wise
+// warpgroups (thread = key, warpgroup w = query columns [64w, 64w + 64))
+// load S^T into registers, which lets dP^T be computed into the same
+// columns while they turn S^T into P^T (bf16 pairs, kept in registers).
+// Then they load dP^T, write P^T over the first 32 of the columns they read
+// (dV += P^T dO starts) and dS^T = P^T (dP^T - Delta) over the other 32 (dK
+// += dS^T Q starts, in two halves).  The buffer takes tile t + 2's S^T once
+// dV(t) and dK(t) are done.  With two tiles in flight the next tile's S^T is
+// always ready when the element-wise warps finish a tile, and its dP^T is
+// computed while they exponentiate.
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;
@@ -170,14 +171,14 @@ struct DkdvCfg {
   static constexpr int kStage = kDO + 2 * kTile;
   static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
   static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 24;
+  static constexpr int kNumBars = 28;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
-  // TMEM: dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512); after
-  // dP^T has been read, warpgroup w's P^T sits in columns [384 + 64w,
-  // 384 + 64w + 32) and its dS^T in the next 32
-  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384;
+  // TMEM: dV [0,128), dK [128,256), tile buffers [256,384) and [384,512);
+  // once dP^T has been read, warpgroup w's P^T sits in columns
+  // [64w, 64w + 32) of the tile's buffer and its dS^T in the next 32
+  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemBuf = 256;
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
 
@@ -238,25 +239,22 @@ __global__ void __launch_bounds__(512, 1)
   float* sCOL = reinterpret_cast<float*>(smem + Cfg::kCOL);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;     // [2] per query-tile stage
+  uint64_t* q_full = bars + 1;     // [2] per query-tile stage (tile t: stage t % 2)
   uint64_t* q_empty = bars + 3;    // [2]
   uint64_t* do_full = bars + 5;    // [2]
   uint64_t* do_empty = bars + 7;   // [2]
-  uint64_t* s_full = bars + 9;     // S^T of the current tile computed
-  uint64_t* dp_full = bars + 10;   // dP^T computed
-  uint64_t* s_free = bars + 11;    // the element-wise warps hold S^T in registers
-  uint64_t* p_full = bars + 12;    // P^T written over the dP^T buffer
-  uint64_t* ds_full = bars + 13;   // [2] dS^T written, per half: query columns [0, 32)
-                                   // and [64, 96) of the tile, then the rest
-  uint64_t* dk_done = bars + 15;   // dV and dK of a tile done (the dP^T buffer is free)
-  uint64_t* col_ready = bars + 17; // [2] per warpgroup: statistics staged
-  uint64_t* acc_done = bars + 19;  // an item's dV, dK complete
-  uint64_t* kv_empty = bars + 20;  // an item's last S^T and dP^T done (two commits)
-  uint64_t* acc_free = bars + 21;  // the epilogue warps have read an item's dV, dK
-  // [2] dP^T of tile t issued (barrier t % 2: the next S^T is issued behind
-  // it; one barrier per tile parity, so that it can never run two phases
-  // ahead of the S^T issuer's wait)
-  uint64_t* dp_issued = bars + 22;
+  // per TMEM tile buffer (tile t: buffer t % 2, phase t / 2)
+  uint64_t* s_full = bars + 9;     // [2] S^T computed
+  uint64_t* s_read = bars + 11;    // [2] the element-wise warps hold S^T in registers
+  uint64_t* dp_full = bars + 13;   // [2] dP^T computed
+  uint64_t* p_full = bars + 15;    // [2] P^T written into the buffer
+  uint64_t* ds_full = bars + 17;   // [2 buffers][2 halves] dS^T written: query columns
+                                   // [0, 32) and [64, 96) of the tile, then the rest
+  uint64_t* buf_free = bars + 21;  // [2] dV and dK of the buffer's tile done
+  uint64_t* col_ready = bars + 23; // [2] per warpgroup: statistics staged
+  uint64_t* acc_done = bars + 25;  // an item's dV, dK complete
+  uint64_t* kv_empty = bars + 26;  // an item's last S^T and dP^T done (two commits)
+  uint64_t* acc_free = bars + 27;  // the epilogue warps have read an item's dV, dK
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -268,15 +266,14 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
       mbar_init(&col_ready[i], 4);  // the four warps of the warpgroup
-      mbar_init(&ds_full[i], 8);    // one arrival per element-wise warp
+      mbar_init(&s_full[i], 1);
+      mbar_init(&dp_full[i], 1);
+      mbar_init(&buf_free[i], 1);
+      mbar_init(&s_read[i], 8);     // one arrival per element-wise warp
+      mbar_init(&p_full[i], 8);
+      mbar_init(&ds_full[2 * i], 8);
+      mbar_init(&ds_full[2 * i + 1], 8);
     }
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(s_free, 8);
-    mbar_init(p_full, 8);
-    mbar_init(dk_done, 1);
-    mbar_init(&dp_issued[0], 1);
-    mbar_init(&dp_issued[1], 1);
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
     mbar_init(acc_free, 4);
@@ -350,21 +347,16 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       // --------------------------------------- MMA issuers: S^T and dP^T
-      // warp 1: S^T(t) = K Q^T once the element-wise warps hold S^T(t-1) in
-      // registers and dP^T(t-1) has been issued.  warp 2: dP^T(t) = V dO^T
-      // once dV(t-1) and dK(t-1), which read P^T and dS^T from the dP^T
-      // buffer, are done.  The tensor pipe takes products in issue order,
-      // and dP^T(t-1) is on the critical chain (dP^T -> dS^T -> dV, dK ->
-      // next dP^T) while S^T(t) is not: S^T(t) then runs while the
-      // element-wise warps turn dP^T(t-1) into P^T, instead of delaying it.
+      // warp 1: S^T(t) = K Q^T into buffer t % 2 once dV(t-2) and dK(t-2),
+      // which read P^T and dS^T there, are done.  warp 2: dP^T(t) = V dO^T
+      // into the same buffer once the element-wise warps hold S^T(t) in
+      // registers.
       const bool is_s = warp == 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t a_addr = smem_u32(is_s ? sK : sV);
       uint8_t* const b_tiles = is_s ? sQ : sDO;
       uint64_t* const b_full = is_s ? q_full : do_full;
-      uint64_t* const free_bar = is_s ? s_free : dk_done;
       uint64_t* const done_bar = is_s ? s_full : dp_full;
-      const uint32_t d_tmem = tmem + (is_s ? Cfg::kTmemS : Cfg::kTmemDP);
       uint64_t* last_commit = nullptr;
       uint32_t last_parity = 0;
       bool ok = true;
@@ -376,23 +368,26 @@ __global__ void __launch_bounds__(512, 1)
         if (it.n == 0) continue;
         if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
         for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, st = ig & 1;
-          if (ig >= 1 && !mbar_wait(free_bar, (ig - 1) & 1, ctl)) { ok = false; break; }
-          if (is_s && ig >= 1 &&
-              !mbar_wait(&dp_issued[(ig - 1) & 1], ((ig - 1) >> 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&b_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
+          const int ig = tbase + i, x = ig & 1;
+          const uint32_t use = (ig >> 1) & 1;  // parity of this use of buffer x
+          if (is_s) {
+            if (ig >= 2 && !mbar_wait(&buf_free[x], use ^ 1u, ctl)) { ok = false; break; }
+          } else {
+            if (!mbar_wait(&s_read[x], use, ctl)) { ok = false; break; }
+          }
+          if (!mbar_wait(&b_full[x], use, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(b_tiles + st * Cfg::kTile);
+          const uint32_t b_addr = smem_u32(b_tiles + x * Cfg::kTile);
+          const uint32_t d_tmem = tmem + Cfg::kTmemBuf + 128 * x;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
             mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + off, 16, 1024),
                         sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          if (!is_s) mbar_arrive(&dp_issued[ig & 1]);
-          mma_commit(done_bar);
-          last_commit = done_bar;
-          last_parity = ig & 1;
+          mma_commit(&done_bar[x]);
+          last_commit = &done_bar[x];
+          last_parity = use;
         }
         if (!ok) break;
         mma_commit(kv_empty);  // this item's K (V) reads are done once these complete
@@ -404,8 +399,8 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 3) {
     if (lane == 0) {
       // ------------------------------------------- MMA issuer: dV, then dK
-      // once P^T is in the dP^T buffer: dV += P^T dO; then dK += dS^T Q, each
-      // half of dS^T as soon as it is written (A operands from TMEM:
+      // once P^T is in the tile's buffer: dV += P^T dO; then dK += dS^T Q,
+      // each half of dS^T as soon as it is written (A operands from TMEM:
       // warpgroup w's query columns [64w, 64w + 64) sit in 32 columns of the
       // buffer, 8 per 16-deep step).  The commit after dK covers dV too.
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
@@ -419,43 +414,44 @@ __global__ void __launch_bounds__(512, 1)
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, st = ig & 1;
+          const int ig = tbase + i, x = ig & 1;
+          const uint32_t use = (ig >> 1) & 1;
+          const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * x;
           // the item's first products overwrite dV, dK: the previous item's
           // must have been read out by the epilogue warps
           if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&do_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&q_full[st], (ig >> 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(p_full, ig & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&do_full[x], use, ctl)) { ok = false; break; }
+          if (!mbar_wait(&q_full[x], use, ctl)) { ok = false; break; }
+          if (!mbar_wait(&p_full[x], use, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t do_addr = smem_u32(sDO + st * Cfg::kTile);
-          const uint32_t q_addr = smem_u32(sQ + st * Cfg::kTile);
+          const uint32_t do_addr = smem_u32(sDO + x * Cfg::kTile);
+          const uint32_t q_addr = smem_u32(sQ + x * Cfg::kTile);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemDP + 64 * (kk >> 2) + 8 * (kk & 3),
+            mma_f16_ts(tmem + Cfg::kTmemDV, buf + 64 * (kk >> 2) + 8 * (kk & 3),
                        sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                        (i > 0 || kk > 0) ? 1u : 0u);
           // each half of dS^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(&ds_full[h], ig & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&ds_full[2 * x + h], use, ctl)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
-              mma_f16_ts(tmem + Cfg::kTmemDK,
-                         tmem + Cfg::kTmemDP + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
+              mma_f16_ts(tmem + Cfg::kTmemDK, buf + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
                          sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                          (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
           if (!ok) break;
-          mma_commit(dk_done);
+          mma_commit(&buf_free[x]);
           // S^T and dP^T of this tile completed before P^T / dS^T existed:
           // its Q and dO are free once dV and dK are
-          mma_commit(&do_empty[st]);
-          mma_commit(&q_empty[st]);
-          last_commit = dk_done;
-          last_parity = ig & 1;
+          mma_commit(&do_empty[x]);
+          mma_commit(&q_empty[x]);
+          last_commit = &buf_free[x];
+          last_parity = use;
           if (i == it.n - 1) {
             mma_commit(acc_done);
             last_commit = acc_done;
@@ -484,8 +480,8 @@ __global__ void __launch_bounds__(512, 1)
     const float* stat_src = (r < 64) ? lse : p.delta;
     const float stat_mul = (r < 64) ? -kLog2e : 1.f;
     float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
-    const uint32_t s_cols = tmem + lane_base + Cfg::kTmemS + 64 * w;
-    const uint32_t dp_cols = tmem + lane_base + Cfg::kTmemDP + 64 * w;
+    // this warpgroup's 64 columns of TMEM tile buffer 0; buffer 1 is 128 further
+    const uint32_t buf_cols = tmem + lane_base + Cfg::kTmemBuf + 64 * w;
     bool ok = true;
     int tbase = 0;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
@@ -530,20 +526,23 @@ __global__ void __launch_bounds__(512, 1)
         const bool masked = (e & kPartialBit) != 0;
         const float4* nlse_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128);
         const float4* del_c = reinterpret_cast<const float4*>(col + (ig & 1) * 128 + 64);
+        const int x = ig & 1;
+        const uint32_t use = (ig >> 1) & 1;
+        const uint32_t cols = buf_cols + 128 * x;
         // phase 1: P^T from S^T.  All 64 columns come in with one wait (a
         // TMEM load takes hundreds of cycles while the tensor pipe is busy);
-        // once they are in registers the S^T buffer can take the next tile.
-        if (!warp_wait(s_full, ig & 1, ctl)) { ok = false; break; }
+        // once they are in registers dP^T can be computed over them.
+        if (!warp_wait(&s_full[x], use, ctl)) { ok = false; break; }
         tc_fence_after();
         uint32_t pb[32];  // P of the 64 columns as bf16 pairs
         {
           uint32_t su[64];
-          tmem_ld32_nowait(s_cols, su);
-          tmem_ld32_nowait(s_cols + 32, su + 32);
+          tmem_ld32_nowait(cols, su);
+          tmem_ld32_nowait(cols + 32, su + 32);
           tmem_wait_ld();
           reg_fence32(su);
           reg_fence32(su + 32);
-          warp_arrive(s_free);
+          warp_arrive(&s_read[x]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (masked)
@@ -556,27 +555,27 @@ __global__ void __launch_bounds__(512, 1)
         }
         // phase 2: load dP^T, write P^T over its first 32 columns (dV starts),
         // then dS^T over the other 32, in two halves (dK starts on each)
-        if (!warp_wait(dp_full, ig & 1, ctl)) { ok = false; break; }
+        if (!warp_wait(&dp_full[x], use, ctl)) { ok = false; break; }
         tc_fence_after();
         {
           uint32_t du[64];
-          tmem_ld32_nowait(dp_cols, du);
-          tmem_ld32_nowait(dp_cols + 32, du + 32);
+          tmem_ld32_nowait(cols, du);
+          tmem_ld32_nowait(cols + 32, du + 32);
           tmem_wait_ld();
           reg_fence32(du);
           reg_fence32(du + 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_st8_nowait(dp_cols + 8 * q4, pb + 8 * q4);
+          for (int q4 = 0; q4 < 4; ++q4) tmem_st8_nowait(cols + 8 * q4, pb + 8 * q4);
           tmem_wait_st();
-          warp_arrive(p_full);
+          warp_arrive(&p_full[x]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t pd[16];
             ds_chunk32(du + 32 * h, pb + 16 * h, del_c + 8 * h, pd);
-            tmem_st8_nowait(dp_cols + 32 + 16 * h, pd);
-            tmem_st8_nowait(dp_cols + 32 + 16 * h + 8, pd + 8);
+            tmem_st8_nowait(cols + 32 + 16 * h, pd);
+            tmem_st8_nowait(cols + 32 + 16 * h + 8, pd + 8);
             tmem_wait_st();
-            warp_arrive(&ds_full[h]);
+            warp_arrive(&ds_full[2 * x + h]);
           }
         }
       }
