@@ -70,12 +70,12 @@ def kernels_per_rank_step(w) -> int:
     """Kernels one rank's step launches: the planner's four (positions,
     block classes, scans + launch orders, lists) plus one per launch order
     too long for the in-block sort, the forward's two (V to fp16,
-    attention) and the backward's three (Delta, dK/dV, dQ), plus the sum of
-    the dK/dV partials when the key tiles' lists are split."""
+    attention) and the backward's two (dQ with Delta, dK/dV), plus the sum
+    of the dK/dV partials when the key tiles' lists are split."""
     g = w.n_heads // w.n_kv_heads
     nq = w.batch * ((w.seq_len // w.cp_size) // (128 // g))
     nk = w.batch * (w.seq_len // 128)
-    return (4 + int(nq > PLAN_SORT_MAX) + int(nk > PLAN_SORT_MAX) + 2 + 3
+    return (4 + int(nq > PLAN_SORT_MAX) + int(nk > PLAN_SORT_MAX) + 2 + 2
             + int(kv_segments(w) > 1))
 
 
@@ -191,7 +191,8 @@ def algorithmic_bytes(w: wl.Workload, kernel: str) -> int:
     """Bytes one launch of an attention kernel must move at least: every
     input read once and every output written once (q, dO, dQ bf16; O fp32;
     K, V bf16 (the forward reads V's fp16 copy, same size); dK, dV fp32;
-    LSE, Delta fp32), whole tensors."""
+    LSE, Delta fp32), whole tensors.  The dQ kernel also computes Delta
+    from O and dO."""
     rows = w.batch * w.local_len * w.n_heads
     qsz = rows * w.head_dim * 2                                   # bf16 [B, Lq, Hq, D]
     kvsz = w.batch * w.seq_len * w.n_kv_heads * w.head_dim * 2    # bf16 [B, S, Hkv, D]
@@ -201,7 +202,8 @@ def algorithmic_bytes(w: wl.Workload, kernel: str) -> int:
     if kernel == "dkdv":
         return 2 * qsz + 2 * kvsz + 2 * stat + 2 * 2 * kvsz       # q, dO, k, v, lse, Delta; dk, dv fp32
     if kernel == "dq":
-        return 2 * qsz + 2 * kvsz + 2 * stat + qsz                # q, dO, k, v, lse, Delta; dq
+        # q, dO, k, v, lse, O (fp32) in; dq, Delta out (the kernel computes Delta)
+        return 2 * qsz + 2 * kvsz + stat + 2 * qsz + qsz + stat
     raise ValueError(kernel)
 
 
@@ -475,12 +477,13 @@ def run_gpu(args, w: wl.Workload):
     torch.cuda.synchronize(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    names = ("plan", "fwd", "delta", "dkdv", "dq")
+    names = ("plan", "fwd", "dq", "dkdv")
 
     def step(record: bool):
         evs = []
         for U in units:
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] \
+                if record else None
             if record:
                 e[0].record(stream)
             plan = dma.dma_plan(U["cu"], w.batch, w.seq_len, w.cp_size, U["r"], w.n_heads,
@@ -491,16 +494,15 @@ def run_gpu(args, w: wl.Workload):
             dma.dma_attn_fwd(plan, U["q"], U["k"], U["v"], U["o"], U["lse"])
             if record:
                 e[2].record(stream)
-            dma.dma_attn_bwd_delta(plan, U["o"], U["do"])
+            # the backward: dQ with Delta in one kernel, then dK/dV
+            dma.dma_attn_bwd_dq_delta(plan, U["q"], U["k"], U["v"], U["o"], U["lse"], U["do"],
+                                      U["dq"])
             if record:
                 e[3].record(stream)
             dma.dma_attn_bwd_dkdv(plan, U["q"], U["k"], U["v"], U["lse"], U["do"], U["dk"],
                                   U["dv"])
             if record:
                 e[4].record(stream)
-            dma.dma_attn_bwd_dq(plan, U["q"], U["k"], U["v"], U["lse"], U["do"], U["dq"])
-            if record:
-                e[5].record(stream)
             evs.append(e)
         return evs
 
@@ -596,11 +598,10 @@ def run_gpu(args, w: wl.Workload):
             "hbm_frac": (abytes / (kms[dom] * 1e-3) / 1e9 / hbm_peak) if hbm_peak else None,
             "kernel_ms": {n: round(kms[n], 5) for n in names}}
 
-    # the HBM-bound parts against the measured copy bandwidth: Delta, and the
-    # planner (latency-bound: a handful of small launches)
+    # the HBM-bound part against the measured copy bandwidth: the planner
+    # (latency-bound: a handful of small launches).  Delta is computed inside
+    # the dQ kernel, whose O reads count in its algorithmic bytes.
     hbm = {"peak_gbs": hbm_peak, "peak_source": "measured copy (MEASURED_PEAKS.json hbm_gbs)"}
-    db = delta_bytes(w)
-    hbm["delta"] = {"bytes": db, "ms": kms["delta"], "gbs": db / (kms["delta"] * 1e-3) / 1e9}
     try:
         listed = [int(dma.plan_arrays(U["plan"])["row_ptr"][-1]) for U in units]
         n_docs = len(cu_of[units[0]["c"]]) - 1
@@ -609,9 +610,8 @@ def run_gpu(args, w: wl.Workload):
                        "note": "latency-bound: one memset and four small launches"}
     except Exception as exc:  # the line is printed regardless
         hbm["plan"] = {"error": str(exc)[:120]}
-    for part in ("delta", "plan"):
-        if hbm_peak and "gbs" in hbm[part]:
-            hbm[part]["frac"] = hbm[part]["gbs"] / hbm_peak
+    if hbm_peak and "gbs" in hbm["plan"]:
+        hbm["plan"]["frac"] = hbm["plan"]["gbs"] / hbm_peak
     # the same step counted without the backward's recompute (4D + 8D per pair)
     flops_mfu = sum(flops_of(copy_of[c], cu_of[c], (r,), fwd=4, bwd=8)
                     for sh in shares for c, r in sh)

@@ -31,7 +31,7 @@ EXPORTED = [
     "dma_plan_check", "dma_plan_destroy", "dma_status_str", "dma_cp_gather",
     "dma_cp_scatter", "dma_plan_get_view", "dma_plan_set_wait_timeout",
     "dma_debug_wait_probe", "dma_attn_bwd_delta", "dma_attn_bwd_dkdv", "dma_attn_bwd_dq",
-    "dma_attn_fwd_noalloc",
+    "dma_attn_fwd_noalloc", "dma_attn_bwd_dq_delta",
 ]
 
 
@@ -76,6 +76,7 @@ def _load():
         "dma_attn_bwd_delta": (i32, [vp] * 4),
         "dma_attn_bwd_dkdv": (i32, [vp] * 9),
         "dma_attn_bwd_dq": (i32, [vp] * 8),
+        "dma_attn_bwd_dq_delta": (i32, [vp] * 9),
         "dma_attn_fwd_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, i32, f32] +
                                  [vp] * 7),
     }
@@ -267,6 +268,22 @@ def dma_attn_bwd_dq(plan: Plan, q, k, v, lse, dout, dq, stream=None):
     _expect(dq, torch.bfloat16, (B, Lq, Hq, D), "dq")
     _check(lib().dma_attn_bwd_dq(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
                                  _ptr(dout), _ptr(dq), _stream(stream)), "dma_attn_bwd_dq")
+
+
+def dma_attn_bwd_dq_delta(plan: Plan, q, k, v, o, lse, dout, dq, stream=None):
+    import torch
+    B, S, cp, _, Hq, Hkv, D = plan.shape
+    Lq = S // cp
+    _expect(q, torch.bfloat16, (B, Lq, Hq, D), "q")
+    _expect(k, torch.bfloat16, (B, S, Hkv, D), "k")
+    _expect(v, torch.bfloat16, (B, S, Hkv, D), "v")
+    _expect(o, torch.float32, (B, Lq, Hq, D), "o")
+    _expect(lse, torch.float32, (B, Hq, Lq), "lse")
+    _expect(dout, torch.bfloat16, (B, Lq, Hq, D), "dout")
+    _expect(dq, torch.bfloat16, (B, Lq, Hq, D), "dq")
+    _check(lib().dma_attn_bwd_dq_delta(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                       _ptr(lse), _ptr(dout), _ptr(dq), _stream(stream)),
+           "dma_attn_bwd_dq_delta")
 
 
 def dma_plan_check(plan: Plan, stream=None) -> int:

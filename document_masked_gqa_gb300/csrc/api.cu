@@ -205,6 +205,19 @@ dma_status init_plan(dma_plan_s& pl, const int32_t* cu_doc_lens, int n_docs, int
   return DMA_OK;
 }
 
+// O (fp32 [rows][heads][D]) as a TMA load source: box = 32 columns x g
+// heads x P positions (one 128-row query tile, 16 KB), 128-byte swizzled.
+dma_status map_o_load(CUtensorMap* m, const void* base, const dma::PlanDev& p, int rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.head_dim),
+                              static_cast<cuuint64_t>(p.n_heads), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.head_dim) * 4,
+                                 static_cast<cuuint64_t>(p.n_heads) * p.head_dim * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(p.group),
+                             static_cast<cuuint32_t>(p.tile_pos)};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 dma_status check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DMA_ERR_CUDA;
@@ -322,17 +335,20 @@ dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16*
              : DMA_ERR_CUDA;
 }
 
-dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
-                           const dma_bf16* v, const float* lse, const dma_bf16* dout,
-                           dma_bf16* dq, void* stream) {
+namespace {
+// dQ, and with o != nullptr also Delta (into the plan's workspace), in one
+// launch of the dQ kernel
+dma_status bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
+                  const float* o, const float* lse, const dma_bf16* dout, dma_bf16* dq,
+                  void* stream) {
   if (!plan) return DMA_ERR_INVALID_ARG;
   const dma::PlanDev& p = plan->d;
   if (p.batch == 0) return DMA_OK;
   if (!q || !k || !v || !lse || !dout || !dq) return DMA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
-      !aligned16(dq))
+      !aligned16(dq) || (o && !aligned16(o)))
     return DMA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, to;
   dma_status st;
   const int rows = p.batch * p.local_len;
   if ((st = map_rows_heads(&tq, q, p, p.n_heads, rows)) != DMA_OK) return st;
@@ -340,10 +356,25 @@ dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k
   if ((st = map_rows_heads(&tdq, dq, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  return dma::launch_dq(*plan, lse, tq, tk, tv, tdo, tdq, dq, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
+  if (o && (st = map_o_load(&to, o, p, rows)) != DMA_OK) return st;
+  return dma::launch_dq(*plan, lse, tq, tk, tv, tdo, tdq, o ? &to : nullptr, o, dout, dq,
+                        static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;
+}
+}  // namespace
+
+dma_status dma_attn_bwd_dq(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                           const dma_bf16* v, const float* lse, const dma_bf16* dout,
+                           dma_bf16* dq, void* stream) {
+  return bwd_dq(plan, q, k, v, nullptr, lse, dout, dq, stream);
+}
+
+dma_status dma_attn_bwd_dq_delta(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                                 const dma_bf16* v, const float* o, const float* lse,
+                                 const dma_bf16* dout, dma_bf16* dq, void* stream) {
+  if (!o) return DMA_ERR_INVALID_ARG;
+  return bwd_dq(plan, q, k, v, o, lse, dout, dq, stream);
 }
 
 dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, const dma_bf16* v,
@@ -352,11 +383,10 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k, c
   if (!plan) return DMA_ERR_INVALID_ARG;
   if (plan->d.batch == 0) return DMA_OK;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return DMA_ERR_INVALID_ARG;
-  dma_status st = dma_attn_bwd_delta(plan, o, dout, stream);
+  // dQ first: its kernel also produces Delta, which dK/dV reads
+  dma_status st = dma_attn_bwd_dq_delta(plan, q, k, v, o, lse, dout, dq, stream);
   if (st != DMA_OK) return st;
-  st = dma_attn_bwd_dkdv(plan, q, k, v, lse, dout, dk, dv, stream);
-  if (st != DMA_OK) return st;
-  return dma_attn_bwd_dq(plan, q, k, v, lse, dout, dq, stream);
+  return dma_attn_bwd_dkdv(plan, q, k, v, lse, dout, dk, dv, stream);
 }
 
 dma_status dma_plan_check(dma_plan_t plan, void* stream) {

@@ -495,20 +495,24 @@ __global__ void __launch_bounds__(512, 1)
       const long long stat_base =
           (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (qcol & (g - 1))) * Lq +
           (qcol >> lg);
-      // list entries of this tile (e) and the next (e_nx), loaded a tile ahead
+      // list entries of this tile (e) and the next two (e1, e2): they run two
+      // tiles ahead and the statistics one tile ahead, so that no load waits
+      // on the one before it
       uint32_t e = static_cast<uint32_t>(it.list[0]);
-      uint32_t e_nx = it.n > 1 ? static_cast<uint32_t>(it.list[1]) : 0u;
+      uint32_t e1 = it.n > 1 ? static_cast<uint32_t>(it.list[1]) : 0u;
+      uint32_t e2 = it.n > 2 ? static_cast<uint32_t>(it.list[2]) : 0u;
       float nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
       for (int i = 0; i < it.n; ++i) {
         const int ig = tbase + i;
         if (i > 0) {
-          e = e_nx;
-          if (i + 1 < it.n) e_nx = static_cast<uint32_t>(it.list[i + 1]);
+          e = e1;
+          e1 = e2;
+          if (i + 2 < it.n) e2 = static_cast<uint32_t>(it.list[i + 2]);
         }
         {
           // stage this tile's statistics, fetch the next tile's
           const float cur = nxt;
-          if (i + 1 < it.n) nxt = stat_src[stat_base + static_cast<int>(e_nx & kIndexMask) * P];
+          if (i + 1 < it.n) nxt = stat_src[stat_base + static_cast<int>(e1 & kIndexMask) * P];
           col[(ig & 1) * 128 + r] = cur * stat_mul;
           __syncwarp();
           if (lane == 0) mbar_arrive(&col_ready[w]);
@@ -660,11 +664,14 @@ struct DqCfg {
   static constexpr int kRegion = 16384;
   static constexpr int kChunks = D / 64;
   // one ring of tile-sized slots carries every load in stream order: per
-  // work item Q, dO, then K_j, V_j for each key tile j of its row list
+  // work item Q, dO, (when the kernel also computes Delta) O in two slots,
+  // then K_j, V_j for each key tile j of its row list
   static constexpr int kSlots = (D == 128) ? 6 : 8;
   static constexpr int kDS = kSlots * kTile;     // dS (128 x 128 bf16)
-  static constexpr int kBar = kDS + 128 * 128 * 2;
-  static constexpr int kNumBars = 2 * kSlots + 8;
+  // item descriptors published by the producer, two entries of 8 ints
+  static constexpr int kDesc = kDS + 128 * 128 * 2;
+  static constexpr int kBar = kDesc + 2 * 8 * 4;
+  static constexpr int kNumBars = 2 * kSlots + 14;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -672,7 +679,7 @@ struct DqCfg {
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
   static constexpr uint32_t kTmemQ = 384, kTmemDO = 384 + D / 2;
   static_assert(kTmemDO + D / 2 <= 512, "dQ TMEM layout exceeds 512 columns");
-  static_assert(kNeed <= kMaxSmem, "dQ shared-memory layout exceeds 227 KB");
+  static_assert(kNeed + 1024 <= kMaxSmem, "dQ shared-memory layout exceeds 227 KB");
 };
 
 // Work item `item` of the dQ pass: (sample, query tile) in longest-list-first
@@ -699,14 +706,23 @@ __device__ __forceinline__ DqItem dq_item(const PlanDev& p, int item) {
 // slot load (sidx), the number of key tiles processed so far (tbase, which
 // fixes the parity of every per-tile barrier) and the number of non-empty
 // items so far (ibase, the parity of epi_full and epi_free).
-template <int D>
+//
+// kDelta: the kernel also computes Delta = rowsum(dO * O) of each query row
+// (the backward preprocess) from the item's dO (already in TMEM) and O
+// (loaded through the ring), uses it, and stores it for the dK/dV pass: the
+// rows' O is read while the tensor cores work, instead of in a pass of its
+// own.  Otherwise Delta is read from the plan's workspace.
+template <int D, bool kDelta>
 __global__ void __launch_bounds__(640, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-              const __grid_constant__ CUtensorMap tdq, const PlanDev p,
-              const float* __restrict__ lse, __nv_bfloat16* __restrict__ dq, int n_items) {
+              const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap to,
+              const PlanDev p, const float* __restrict__ lse, const float* __restrict__ o,
+              const __nv_bfloat16* __restrict__ dout, __nv_bfloat16* __restrict__ dq,
+              int n_items) {
   using Cfg = DqCfg<D>;
   constexpr int NS = Cfg::kSlots;
+  constexpr int NO = kDelta ? 2 : 0;  // ring slots of an item's O (fp32, D / 64 boxes each)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (__syncthreads_or(threadIdx.x == 0 &&
@@ -722,17 +738,23 @@ __global__ void __launch_bounds__(640, 1)
   const int g = p.group, Lq = p.local_len;
 
   uint8_t* sDS = smem + Cfg::kDS;
+  int* sDesc = reinterpret_cast<int*>(smem + Cfg::kDesc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* slot_full = bars;           // [NS]
   uint64_t* slot_empty = bars + NS;     // [NS]
   uint64_t* s_full = bars + 2 * NS;     // S of a key tile computed
   uint64_t* s_free = s_full + 1;        // the row warps have read S
   uint64_t* dp_full = s_full + 2;       // dP computed
-  uint64_t* dp_free = s_full + 3;       // the row warps have read dP
+  uint64_t* dp_free = s_full + 3;       // the row warps have read dP (and, first tile of
+                                        // an item, its dO columns from TMEM)
   uint64_t* ds_full = s_full + 4;       // dS written to shared memory
   uint64_t* ds_done = s_full + 5;       // dQ += dS K done reading dS
   uint64_t* epi_full = s_full + 6;      // an item's dQ tile staged in the dS buffer
   uint64_t* epi_free = s_full + 7;      // its store has read the dS buffer
+  uint64_t* desc_full = s_full + 8;     // [2] an item descriptor published
+  uint64_t* desc_empty = s_full + 10;   // [2] ... and read by every row warp
+  uint64_t* xch_full = s_full + 12;     // every row warp posted its Delta parts
+  uint64_t* xch_free = s_full + 13;     // ... and read the sums (the dS buffer is free)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTile; };
@@ -751,6 +773,12 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(ds_done, 1);
     mbar_init(epi_full, 16);
     mbar_init(epi_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&desc_full[i], 1);
+      mbar_init(&desc_empty[i], 16);
+    }
+    mbar_init(xch_full, 16);
+    mbar_init(xch_free, 16);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -767,21 +795,46 @@ __global__ void __launch_bounds__(640, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ producer: the stream
+      // Per item it first publishes the item's descriptor for the row warps
+      // (all items, empty ones too, then an end marker), then loads Q, dO,
+      // (O), and K_j, V_j for every key tile of the item's list.
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tdo);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int sidx = 0;
+      if (kDelta) tma_prefetch_desc(&to);
+      int sidx = 0, nd = 0;
       bool ok = true;
       auto acquire = [&](int idx) -> bool {
         if (!mbar_wait(&slot_empty[idx % NS], ((idx / NS) & 1) ^ 1u, ctl)) return false;
         mbar_arrive_expect_tx(&slot_full[idx % NS], Cfg::kTile);
         return true;
       };
+      // descriptor entry nd % 2: b, kvh, l0, n (-1: no more items), list offset,
+      // first list entry
+      auto publish = [&](const DqItem* it) -> bool {
+        const int e = nd & 1;
+        if (nd >= 2 && !mbar_wait(&desc_empty[e], ((nd >> 1) - 1) & 1, ctl)) return false;
+        int* d = sDesc + 8 * e;
+        if (it) {
+          d[0] = it->b;
+          d[1] = it->kvh;
+          d[2] = it->l0;
+          d[3] = it->n;
+          d[4] = static_cast<int>(it->list - p.row_idx);
+          d[5] = it->n > 0 ? it->list[0] : 0;
+        } else {
+          d[3] = -1;
+        }
+        mbar_arrive(&desc_full[e]);
+        ++nd;
+        return true;
+      };
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
         const DqItem it = dq_item(p, item);
+        if (!publish(&it)) { ok = false; break; }
         if (it.n == 0) continue;
         const int qrow = it.b * Lq + it.l0;
         if (!acquire(sidx)) { ok = false; break; }
@@ -796,6 +849,19 @@ __global__ void __launch_bounds__(640, 1)
           tma_load_3d(slot_ptr(sidx) + c * Cfg::kRegion, &tdo, &slot_full[sidx % NS], c * 64,
                       it.kvh * g, qrow);
         ++sidx;
+        if (kDelta) {
+          // O (fp32): boxes of 32 columns x 128 rows (16 KB), D / 64 per slot
+#pragma unroll
+          for (int s2 = 0; s2 < NO; ++s2) {
+            if (!acquire(sidx)) { ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(slot_ptr(sidx) + c * 16384, &to, &slot_full[sidx % NS],
+                          32 * (s2 * (D / 64) + c), it.kvh * g, qrow);
+            ++sidx;
+          }
+          if (!ok) break;
+        }
         for (int j = 0; j < it.n; ++j) {
           const int kt = static_cast<int>(static_cast<uint32_t>(it.list[j]) & kIndexMask);
           const int krow = it.b * p.seq_len + kt * kTileN;
@@ -813,6 +879,7 @@ __global__ void __launch_bounds__(640, 1)
           ++sidx;
         }
       }
+      if (ok) ok = publish(nullptr);
       if (!ok) {  // drain this CTA's copies still in flight
         for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
           drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
@@ -840,11 +907,14 @@ __global__ void __launch_bounds__(640, 1)
         if (it.n == 0) continue;
         if (warp == 1 || warp == 2) {
           // the item's Q (warp 1) or dO (warp 2) into TMEM by tcgen05.cp,
-          // once the previous item's last S (or dP) has read the old one; the
-          // copy is ordered before this thread's next MMAs, and the slot goes
-          // back to the producer when it completes
+          // once the previous item is done with the old one (its last S has
+          // completed; the row warps have read its last dP, and with it the
+          // dO columns they read for Delta); the copy is ordered before this
+          // thread's next MMAs, and the slot goes back to the producer when
+          // it completes
           const int cidx = sidx + (warp == 1 ? 0 : 1);
-          if (tbase > 0 && !mbar_wait(warp == 1 ? s_full : dp_full, (tbase - 1) & 1, ctl)) {
+          if (tbase > 0 && !mbar_wait(warp == 1 ? s_full : (kDelta ? dp_free : dp_full),
+                                      (tbase - 1) & 1, ctl)) {
             ok = false;
             break;
           }
@@ -860,7 +930,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         for (int j = 0; j < it.n; ++j) {
           const int t = tbase + j;
-          const int kidx = sidx + 2 + 2 * j, vidx = kidx + 1;
+          const int kidx = sidx + 2 + NO + 2 * j, vidx = kidx + 1;
           if (warp == 1) {
             if (!mbar_wait(&slot_full[kidx % NS], (kidx / NS) & 1, ctl)) { ok = false; break; }
             if (t > 0 && !mbar_wait(s_free, (t - 1) & 1, ctl)) { ok = false; break; }
@@ -922,7 +992,7 @@ __global__ void __launch_bounds__(640, 1)
           bulk_wait_read_all();
           mbar_arrive(epi_free);
         }
-        sidx += 2 + 2 * it.n;
+        sidx += 2 + NO + 2 * it.n;
         tbase += it.n;
         ++ibase;
       }
@@ -932,7 +1002,8 @@ __global__ void __launch_bounds__(640, 1)
   } else {
     // ----------------------------------------------------------- query rows
     // four warpgroups: thread (r, q) owns query row r and key columns
-    // [32q, 32q + 32) of each key tile
+    // [32q, 32q + 32) of each key tile, and head_dim columns
+    // [q D/4, (q + 1) D/4) of the row for Delta and the dQ epilogue
     const int r = (threadIdx.x - 128) & 127;
     const int q = (threadIdx.x - 128) >> 7;
     const int cbase = 32 * q;
@@ -945,38 +1016,54 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t ds_row = smem_u32(sDS) + (q >> 1) * Cfg::kRegion + r * 128;
     const int ch0 = (q & 1) * 4;
     constexpr int DQ = D / 4;  // head_dim columns of dQ this warpgroup writes
+    float* xch = reinterpret_cast<float*>(sDS);  // [4][128] Delta partials, at item start
     bool ok = true;
-    int tbase = 0, ibase = 0;
-    // this row's data of the next item, loaded at the end of the previous
-    // one so that the loads overlap its epilogue
-    int pf_item = -1, pf_lo = 0;
+    int tbase = 0, ibase = 0, nd = 0, sidx = 0;
+    // this row's data of the next item, loaded during the current one
+    int pf_lo = 0;
     float pf_lse = 0.f, pf_del = 0.f;
-    uint32_t pf_e0 = 0;
-    DqItem pf_it{};  // the next item's descriptor, from the same lookup
-    auto row_stat = [&](const DqItem& di) -> long long {
-      return (static_cast<long long>(di.b) * p.n_heads + di.kvh * g + h) * Lq + di.l0 + pos;
-    };
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
-      const DqItem it = (item == pf_item) ? pf_it : dq_item(p, item);
+    bool pf = false;
+    for (;;) {
+      // the next item's descriptor, published by the producer
+      const int de = nd & 1;
+      if (!warp_wait(&desc_full[de], (nd >> 1) & 1, ctl)) { ok = false; break; }
+      DqItem it;
+      const int* dsc = sDesc + 8 * de;
+      it.b = dsc[0];
+      it.kvh = dsc[1];
+      it.l0 = dsc[2];
+      it.n = dsc[3];
+      it.list = p.row_idx + dsc[4];
+      uint32_t e_next = static_cast<uint32_t>(dsc[5]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&desc_empty[de]);
+      ++nd;
+      if (it.n < 0) break;
       const int l = it.l0 + pos;
       const int hq = it.kvh * g + h;
-      uint4* dst = reinterpret_cast<uint4*>(
-          dq + ((static_cast<long long>(it.b) * Lq + l) * p.n_heads + hq) * D + q * DQ);
+      const long long stat =
+          (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + h) * Lq + it.l0 + pos;
+      const long long orow = (static_cast<long long>(it.b) * Lq + l) * p.n_heads + hq;
       if (it.n == 0) {
+        // (every row attends at least its own key, so an item has at least
+        // one key tile; kept for completeness) dQ = 0, Delta from memory
+        uint4* dst = reinterpret_cast<uint4*>(dq + orow * D + q * DQ);
 #pragma unroll
         for (int c = 0; c < DQ / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        if (kDelta && q == 0) {
+          float acc = 0.f;
+          for (int d = 0; d < D; ++d)
+            acc = fmaf(o[orow * D + d], __bfloat162float(dout[orow * D + d]), acc);
+          p.delta[stat] = acc;
+        }
+        pf = false;
         continue;
       }
       const int qabs =
           (l < C) ? (p.cp_rank * C + l) : ((2 * p.cp_size - 1 - p.cp_rank) * C + l - C);
-      const bool pf = pf_item == item;
-      const long long stat = row_stat(it);
       const int lo_r = pf ? pf_lo : p.doc_lo[static_cast<long long>(it.b) * Lq + l];
       const float lse2 = (pf ? pf_lse : lse[stat]) * kLog2e;
-      const float del = pf ? pf_del : p.delta[stat];
-      uint32_t e_next = pf ? pf_e0 : static_cast<uint32_t>(it.list[0]);
+      float del = (!kDelta && pf) ? pf_del : (kDelta ? 0.f : p.delta[stat]);
       for (int j = 0; j < it.n; ++j) {
         const int t = tbase + j;
         const uint32_t e = e_next;  // list entries run one tile ahead
@@ -1017,11 +1104,67 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         uint32_t pk[16];
         {
+          if (kDelta && j == 0) {
+            // Delta of this row: its dO (bf16 pairs in TMEM, copied there for
+            // dP) times its O (fp32, from the ring), this warpgroup's D/4
+            // columns, then the four warpgroups' parts added in order
+            uint32_t od[DQ / 2];
+            if constexpr (DQ == 32) {
+              tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
+              tmem_wait_ld();
+              reg_fence16(od);
+            } else {
+              tmem_ld8_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
+              tmem_wait_ld();
+              reg_fence8(od);
+            }
+            // the O box holding these columns: box (q D/4) / 32, D / 64 boxes a slot
+            const int box = (q * DQ) / 32;
+            const int oidx = sidx + 2 + box / (D / 64);
+            if (!warp_wait(&slot_full[oidx % NS], (oidx / NS) & 1, ctl)) { ok = false; break; }
+            // row r of the box: 128 bytes, 16-byte chunks swizzled by r & 7
+            const uint32_t orow_s =
+                smem_u32(slot_ptr(oidx)) + (box % (D / 64)) * 16384 + r * 128;
+            const int cb0 = ((q * DQ) % 32) / 4;
+            float part = 0.f;
+#pragma unroll
+            for (int c = 0; c < DQ / 4; ++c) {
+              float4 ov;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(ov.x), "=f"(ov.y), "=f"(ov.z), "=f"(ov.w)
+                           : "r"(orow_s + (((cb0 + c) ^ (r & 7)) << 4)));
+              const uint32_t w0 = od[2 * c], w1 = od[2 * c + 1];
+              part = fmaf(ov.x, __uint_as_float(w0 << 16), part);
+              part = fmaf(ov.y, __uint_as_float(w0 & 0xFFFF0000u), part);
+              part = fmaf(ov.z, __uint_as_float(w1 << 16), part);
+              part = fmaf(ov.w, __uint_as_float(w1 & 0xFFFF0000u), part);
+            }
+            // the parts go through the dS buffer: the previous item's dQ
+            // store must have read it
+            if (ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+            xch[q * 128 + r] = part;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xch_full);
+            if (!warp_wait(xch_full, ibase & 1, ctl)) { ok = false; break; }
+            del = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
+            if (threadIdx.x == 128) {
+              // every row warp has read O: its slots go back to the producer
+#pragma unroll
+              for (int s2 = 0; s2 < NO; ++s2) mbar_arrive(&slot_empty[(sidx + 2 + s2) % NS]);
+            }
+            if (q == 0) p.delta[stat] = del;
+            // dS overwrites the parts only once every warp has read them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xch_free);
+            if (!warp_wait(xch_free, ibase & 1, ctl)) { ok = false; break; }
+          }
           uint32_t du[32];
           tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase, du);
           tmem_wait_ld();
           reg_fence32(du);
-          warp_arrive(dp_free);  // dP is in registers: the buffer can take the next dP
+          // dP (and, first tile of an item, the item's dO) read: the buffer
+          // can take the next dP
+          warp_arrive(dp_free);
           const uint64_t delx2 = f2(del, del);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -1035,7 +1178,10 @@ __global__ void __launch_bounds__(640, 1)
         }
         if (t > 0 && !warp_wait(ds_done, (t - 1) & 1, ctl)) { ok = false; break; }
         // the dS buffer may still be read by the store of the previous dQ tile
-        if (j == 0 && ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+        if (!kDelta && j == 0 && ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           st_shared_v4(ds_row + (((ch0 + c) ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1],
@@ -1045,28 +1191,22 @@ __global__ void __launch_bounds__(640, 1)
         if (lane == 0) mbar_arrive(ds_full);
       }
       if (!ok) break;
-      // the next non-empty item's row data: loaded now, used after this
-      // epilogue
+      // the next item's row data: its descriptor is published (the producer
+      // publishes it before loading that item), so the loads are issued now
+      // and land during this item's epilogue
+      pf = false;
       {
-        int nx = n_items;
-        DqItem nit{};
-        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
-          const int cand = snake_item(kx);
-          if (cand >= n_items) continue;
-          nit = dq_item(p, cand);
-          if (nit.n != 0) {
-            nx = cand;
-            break;
-          }
-        }
-        if (nx < n_items) {
-          const long long nstat = row_stat(nit);
-          pf_lo = p.doc_lo[static_cast<long long>(nit.b) * Lq + nit.l0 + pos];
+        const int de2 = nd & 1;
+        if (!warp_wait(&desc_full[de2], (nd >> 1) & 1, ctl)) { ok = false; break; }
+        const int* d2 = sDesc + 8 * de2;
+        const int nb = d2[0], nkvh = d2[1], nl0 = d2[2], nn = d2[3];
+        if (nn > 0) {
+          const long long nstat =
+              (static_cast<long long>(nb) * p.n_heads + nkvh * g + h) * Lq + nl0 + pos;
+          pf_lo = p.doc_lo[static_cast<long long>(nb) * Lq + nl0 + pos];
           pf_lse = lse[nstat];
-          pf_del = p.delta[nstat];
-          pf_e0 = static_cast<uint32_t>(nit.list[0]);
-          pf_it = nit;
-          pf_item = nx;
+          if (!kDelta) pf_del = p.delta[nstat];
+          pf = true;
         }
       }
       // epilogue: dQ (scaled, bf16) staged in the dS buffer in the layout of
@@ -1101,6 +1241,7 @@ __global__ void __launch_bounds__(640, 1)
       // the next item's first dQ product overwrites the accumulator only
       // after every warp has arrived on ds_full for it, i.e. after this read
       warp_arrive(epi_full);
+      sidx += 2 + NO + 2 * it.n;
       tbase += it.n;
       ++ibase;
     }
@@ -1163,17 +1304,30 @@ cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensor
 template <int D>
 cudaError_t launch_dq_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s) {
+                        const CUtensorMap& tdq, const CUtensorMap* to, const float* o,
+                        const dma_bf16* dout, dma_bf16* dq, cudaStream_t s) {
   const PlanDev& p = pl.d;
   const int items = p.batch * p.n_qtiles * p.n_kv_heads;
   if (items == 0) return cudaSuccess;
   // persistent: one CTA per SM (TMEM and shared memory allow no more)
   const int grid = items < pl.num_sms ? items : pl.num_sms;
-  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DqCfg<D>::kAlloc);
-  if (e != cudaSuccess) return e;
-  dq_kernel<D><<<grid, 640, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdq, p, lse,
-                                                   reinterpret_cast<__nv_bfloat16*>(dq), items);
+  const auto* pdo = reinterpret_cast<const __nv_bfloat16*>(dout);
+  auto* pdq = reinterpret_cast<__nv_bfloat16*>(dq);
+  if (to) {  // Delta computed here
+    cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dq_kernel<D, true><<<grid, 640, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdq, *to, p, lse, o,
+                                                          pdo, pdq, items);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dq_kernel<D, false><<<grid, 640, DqCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdq, tq, p, lse, o,
+                                                           pdo, pdq, items);
+  }
   return cudaGetLastError();
 }
 
@@ -1207,9 +1361,10 @@ cudaError_t launch_kv_reduce(const dma_plan_s& pl, float* dk, float* dv, cudaStr
 
 cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s) {
-  return pl.d.head_dim == 128 ? launch_dq_d<128>(pl, lse, tq, tk, tv, tdo, tdq, dq, s)
-                              : launch_dq_d<64>(pl, lse, tq, tk, tv, tdo, tdq, dq, s);
+                      const CUtensorMap& tdq, const CUtensorMap* to, const float* o,
+                      const dma_bf16* dout, dma_bf16* dq, cudaStream_t s) {
+  return pl.d.head_dim == 128 ? launch_dq_d<128>(pl, lse, tq, tk, tv, tdo, tdq, to, o, dout, dq, s)
+                              : launch_dq_d<64>(pl, lse, tq, tk, tv, tdo, tdq, to, o, dout, dq, s);
 }
 
 }  // namespace dma

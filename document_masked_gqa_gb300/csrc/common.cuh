@@ -95,9 +95,12 @@ cudaError_t launch_delta(const dma_plan_s& p, const float* o, const dma_bf16* do
 cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                         const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s);
+// to != nullptr: the dQ kernel also computes Delta from O (map `to`, fp32)
+// and stores it in the plan's workspace
 cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const CUtensorMap& tdq, dma_bf16* dq, cudaStream_t s);
+                      const CUtensorMap& tdq, const CUtensorMap* to, const float* o,
+                      const dma_bf16* dout, dma_bf16* dq, cudaStream_t s);
 cudaError_t launch_kv_reduce(const dma_plan_s& p, float* dk, float* dv, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s);

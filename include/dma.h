@@ -143,10 +143,15 @@ dma_status dma_attn_fwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
 
 /*
  * Backward: dq (bf16), and this rank's partial dk, dv (fp32), given the
- * forward's o and lse and the upstream gradient dout.  Three launches:
- * Delta = rowsum(dout * o) into the plan workspace, a key-stationary dK/dV
- * kernel reduced over the group's query heads, and a query-stationary dQ
- * kernel.  dk and dv are fully overwritten.
+ * forward's o and lse and the upstream gradient dout.  The backward
+ * recomputes the scores ("Training Infrastructure and Systems",
+ * "FlashAttention: never write the score matrix", "Tiling"); dk and dv are
+ * kept in fp32 ("The Llama 3 Herd of Models - part 3/16", 3.3.2, "Numerical
+ * stability").  Two launches (three when the key tiles' query lists are
+ * split, see below): a query-stationary dQ kernel that also computes
+ * Delta = rowsum(dout * o) into the plan workspace, then a key-stationary
+ * dK/dV kernel reduced over the group's query heads.  dk and dv are fully
+ * overwritten.
  */
 dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
                         const dma_bf16* v, const float* o, const float* lse,
@@ -154,14 +159,22 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
                         float* dv, void* stream);
 
 /*
- * The three launches dma_attn_bwd makes, callable one by one (same stream
- * order required: delta before the other two, which are independent of each
- * other and may run on different streams once delta has completed).
- *   dma_attn_bwd_delta: Delta = rowsum(dout * o) into the plan workspace.
+ * The launches of the backward, callable one by one (in stream order):
+ *   dma_attn_bwd_dq_delta: dq (bf16) and Delta = rowsum(dout * o) into the
+ *                       plan workspace, in one kernel; what dma_attn_bwd runs.
+ *   dma_attn_bwd_delta: Delta alone (a pass over o and dout of its own).
+ *   dma_attn_bwd_dq   : dq from the Delta already in the workspace.
  *   dma_attn_bwd_dkdv : dk, dv (fp32, fully overwritten) from q, k, v, lse,
- *                       dout and the plan's Delta.
- *   dma_attn_bwd_dq   : dq (bf16) from the same inputs.
+ *                       dout and the workspace's Delta; with fewer than 256
+ *                       (key tile, K/V head) pairs each key tile's query list
+ *                       is split over several work items whose fp32 partials
+ *                       (in the workspace) a second kernel adds in a fixed
+ *                       order.
+ * Delta must be in place (dq_delta or delta) before dq or dkdv runs.
  */
+dma_status dma_attn_bwd_dq_delta(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
+                                 const dma_bf16* v, const float* o, const float* lse,
+                                 const dma_bf16* dout, dma_bf16* dq, void* stream);
 dma_status dma_attn_bwd_delta(dma_plan_t plan, const float* o, const dma_bf16* dout,
                               void* stream);
 dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,

@@ -65,7 +65,8 @@ def test_algorithmic_bytes_per_launch():
     # dK/dV: q, dO, k, v, LSE, Delta in; dK, dV fp32 out: about 473 MB
     assert bench.algorithmic_bytes(w, "dkdv") == 2 * q + 2 * kv + 2 * st + 4 * kv
     assert 472e6 < bench.algorithmic_bytes(w, "dkdv") < 474e6
-    assert bench.algorithmic_bytes(w, "dq") == 3 * q + 2 * kv + 2 * st
+    # dQ with Delta: q, dO, k, v, LSE, O (fp32) in; dQ, Delta out
+    assert bench.algorithmic_bytes(w, "dq") == 5 * q + 2 * kv + 2 * st
     assert bench.algorithmic_bytes(w, "fwd") == q + 2 * kv + 2 * q + st
 
 
@@ -164,23 +165,24 @@ def test_two_processes_split_the_emulated_ranks_and_reassemble():
 
 
 def test_kernels_per_step_follow_the_planner():
-    # four planner kernels, V to fp16 + forward, Delta + dK/dV + dQ
+    # four planner kernels, V to fp16 + forward, dQ with Delta + dK/dV
     for name in ["8b", "sparse", "405b-1doc"]:
-        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 9
+        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 8
     # fewer than 256 (key tile, K/V head) items: the dK/dV lists are split
-    # and a tenth kernel sums the partials (tiny: 2 items, 70b: 64)
+    # and a ninth kernel sums the partials (tiny: 2 items, 70b: 64)
     assert bench.kv_segments(wl.WORKLOADS["tiny"]) == 8
     assert bench.kv_segments(wl.WORKLOADS["70b"]) == 4
     assert bench.kv_segments(wl.WORKLOADS["8b"]) == 1
     for name in ["tiny", "70b"]:
-        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 10
+        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 9
     # launch orders over 2048 units take one extra ranking kernel each: the
-    # 128K single-rank workload has 16384 query tiles of 8 positions
-    assert bench.kernels_per_rank_step(wl.WORKLOADS["causal-128k"]) == 10
+    # 128K single-rank workload has 16384 query tiles of 8 positions (and
+    # 1024 key tiles: no split)
+    assert bench.kernels_per_rank_step(wl.WORKLOADS["causal-128k"]) == 9
     rows = wl.custom("rows", 32768, 1, 1, 16, 1, 64, "uniform", 64, 4096, seed=14)
     both = wl.custom("both", 16384, 1, 17, 2, 2, 64, "uniform", 64, 4096, seed=15)
-    assert bench.kernels_per_rank_step(rows) == 10
-    assert bench.kernels_per_rank_step(both) == 11
+    assert bench.kernels_per_rank_step(rows) == 9
+    assert bench.kernels_per_rank_step(both) == 10
 
 
 def test_source_hash_ignores_comments():

@@ -125,3 +125,39 @@ def test_bwd_405b_sampled_rows_and_tail_keys(name):
         rhs = do_l.double().numpy().reshape(w.batch, w.local_len, w.n_kv_heads, w.group,
                                             w.head_dim).sum(axis=(1, 3))
         assert rel_fro(lhs, rhs) <= TOL_GRAD
+
+
+@pytest.mark.parametrize("name", ["70b", "8b"])
+def test_split_backward_entry_points(name):
+    """The backward's parts called one by one: Delta by its own pass, then
+    dQ reading it, then dK/dV, against the oracle; and the fused dQ + Delta
+    launch gives the same dQ up to the order of Delta's sum."""
+    import document_masked_gqa_gb300 as dma
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    inp = wl.tensors(w)
+    dev = torch.device("cuda:0")
+    cu_d = torch.from_numpy(cu).to(dev)
+    k, v = inp["k"].to(dev), inp["v"].to(dev)
+    r = w.ranks[-1]
+    plan = dma.dma_plan(cu_d, w.batch, w.seq_len, w.cp_size, r, w.n_heads, w.n_kv_heads,
+                        w.head_dim)
+    q = dma.dma_cp_gather(plan, inp["q"].to(dev))
+    do = dma.dma_cp_gather(plan, inp["do"].to(dev))
+    o, lse = dma.dma_attn_fwd(plan, q, k, v)
+    dq = torch.empty_like(q)
+    dk = torch.empty(w.batch, w.seq_len, w.n_kv_heads, w.head_dim, device=dev)
+    dv = torch.empty_like(dk)
+    dma.dma_attn_bwd_delta(plan, o, do)
+    dma.dma_attn_bwd_dq(plan, q, k, v, lse, do, dq)
+    dma.dma_attn_bwd_dkdv(plan, q, k, v, lse, do, dk, dv)
+    torch.cuda.synchronize()
+    assert dma.dma_plan_check(plan) == 0
+    ref = oracle_rank(w, r, inp, cu, backward=True, threads=8)
+    for key, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert rel_fro(got.float().cpu().numpy(), ref[key]) <= TOL_GRAD, (name, key)
+    # the fused launch gives the same gradients up to the order of Delta's sum
+    dq2 = torch.empty_like(q)
+    dma.dma_attn_bwd_dq_delta(plan, q, k, v, o, lse, do, dq2)
+    torch.cuda.synchronize()
+    assert rel_fro(dq2.float().cpu().numpy(), dq.float().cpu().numpy()) <= 1e-3
