@@ -671,7 +671,7 @@ struct DqCfg {
   // item descriptors published by the producer, two entries of 8 ints
   static constexpr int kDesc = kDS + 128 * 128 * 2;
   static constexpr int kBar = kDesc + 2 * 8 * 4;
-  static constexpr int kNumBars = 2 * kSlots + 14;
+  static constexpr int kNumBars = 2 * kSlots + 16;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -755,6 +755,7 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* desc_empty = s_full + 10;   // [2] ... and read by every row warp
   uint64_t* xch_full = s_full + 12;     // every row warp posted its Delta parts
   uint64_t* xch_free = s_full + 13;     // ... and read the sums (the dS buffer is free)
+  uint64_t* do_ready = s_full + 14;     // an item's dO copied into TMEM
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
   auto slot_ptr = [&](int idx) { return smem + (idx % NS) * Cfg::kTile; };
@@ -779,6 +780,7 @@ __global__ void __launch_bounds__(640, 1)
     }
     mbar_init(xch_full, 16);
     mbar_init(xch_free, 16);
+    mbar_init(do_ready, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -795,9 +797,10 @@ __global__ void __launch_bounds__(640, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ producer: the stream
-      // Per item it first publishes the item's descriptor for the row warps
-      // (all items, empty ones too, then an end marker), then loads Q, dO,
-      // (O), and K_j, V_j for every key tile of the item's list.
+      // It publishes the descriptors of the CTA's items for the row warps, one
+      // item ahead (all items, empty ones too, then an end marker), and per
+      // non-empty item loads Q, dO, (O), and K_j, V_j for every key tile of
+      // the item's list.
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tdo);
       tma_prefetch_desc(&tk);
@@ -830,11 +833,26 @@ __global__ void __launch_bounds__(640, 1)
         ++nd;
         return true;
       };
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
-        const DqItem it = dq_item(p, item);
-        if (!publish(&it)) { ok = false; break; }
+      // the CTA's items in order; each item's successor is published as the
+      // item's loads begin, so that the row warps find it well before they
+      // finish the item
+      int kn = -1;
+      auto next_item = [&](DqItem& out) -> bool {
+        for (++kn; kn * static_cast<int>(gridDim.x) < n_items; ++kn) {
+          const int cand = snake_item(kn);
+          if (cand >= n_items) continue;
+          out = dq_item(p, cand);
+          return true;
+        }
+        return false;
+      };
+      DqItem nx{};
+      bool have_nx = next_item(nx);
+      if (!publish(have_nx ? &nx : nullptr)) ok = false;
+      while (ok && have_nx) {
+        const DqItem it = nx;
+        have_nx = next_item(nx);
+        if (!publish(have_nx ? &nx : nullptr)) { ok = false; break; }
         if (it.n == 0) continue;
         const int qrow = it.b * Lq + it.l0;
         if (!acquire(sidx)) { ok = false; break; }
@@ -879,7 +897,6 @@ __global__ void __launch_bounds__(640, 1)
           ++sidx;
         }
       }
-      if (ok) ok = publish(nullptr);
       if (!ok) {  // drain this CTA's copies still in flight
         for (int idx = max(0, sidx - NS); idx < sidx; ++idx)
           drain_wait(&slot_full[idx % NS], (idx / NS) & 1, 100000000ull);
@@ -927,6 +944,7 @@ __global__ void __launch_bounds__(640, 1)
             tmem_cp_128x256b(dst_t + 8 * kk,
                              sdesc_sw128(src + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024));
           mma_commit(&slot_empty[cidx % NS]);
+          if (kDelta && warp == 2) mma_commit(do_ready);  // the row warps read it for Delta
         }
         for (int j = 0; j < it.n; ++j) {
           const int t = tbase + j;
@@ -1064,6 +1082,63 @@ __global__ void __launch_bounds__(640, 1)
       const int lo_r = pf ? pf_lo : p.doc_lo[static_cast<long long>(it.b) * Lq + l];
       const float lse2 = (pf ? pf_lse : lse[stat]) * kLog2e;
       float del = (!kDelta && pf) ? pf_del : (kDelta ? 0.f : p.delta[stat]);
+      if (kDelta) {
+        // once the item's dO is in TMEM (copied there for dP)
+        if (!warp_wait(do_ready, ibase & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        // Delta of this row: its dO (bf16 pairs in TMEM, copied there for
+        // dP) times its O (fp32, from the ring), this warpgroup's D/4
+        // columns, then the four warpgroups' parts added in order
+        uint32_t od[DQ / 2];
+        if constexpr (DQ == 32) {
+          tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
+          tmem_wait_ld();
+          reg_fence16(od);
+        } else {
+          tmem_ld8_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
+          tmem_wait_ld();
+          reg_fence8(od);
+        }
+        // the O box holding these columns: box (q D/4) / 32, D / 64 boxes a slot
+        const int box = (q * DQ) / 32;
+        const int oidx = sidx + 2 + box / (D / 64);
+        if (!warp_wait(&slot_full[oidx % NS], (oidx / NS) & 1, ctl)) { ok = false; break; }
+        // row r of the box: 128 bytes, 16-byte chunks swizzled by r & 7
+        const uint32_t orow_s =
+            smem_u32(slot_ptr(oidx)) + (box % (D / 64)) * 16384 + r * 128;
+        const int cb0 = ((q * DQ) % 32) / 4;
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < DQ / 4; ++c) {
+          float4 ov;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(ov.x), "=f"(ov.y), "=f"(ov.z), "=f"(ov.w)
+                       : "r"(orow_s + (((cb0 + c) ^ (r & 7)) << 4)));
+          const uint32_t w0 = od[2 * c], w1 = od[2 * c + 1];
+          part = fmaf(ov.x, __uint_as_float(w0 << 16), part);
+          part = fmaf(ov.y, __uint_as_float(w0 & 0xFFFF0000u), part);
+          part = fmaf(ov.z, __uint_as_float(w1 << 16), part);
+          part = fmaf(ov.w, __uint_as_float(w1 & 0xFFFF0000u), part);
+        }
+        // the parts go through the dS buffer: the previous item's dQ
+        // store must have read it
+        if (ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+        xch[q * 128 + r] = part;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xch_full);
+        if (!warp_wait(xch_full, ibase & 1, ctl)) { ok = false; break; }
+        del = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
+        if (threadIdx.x == 128) {
+          // every row warp has read O: its slots go back to the producer
+#pragma unroll
+          for (int s2 = 0; s2 < NO; ++s2) mbar_arrive(&slot_empty[(sidx + 2 + s2) % NS]);
+        }
+        if (q == 0) p.delta[stat] = del;
+        // dS overwrites the parts only once every warp has read them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xch_free);
+        if (!warp_wait(xch_free, ibase & 1, ctl)) { ok = false; break; }
+      }
       for (int j = 0; j < it.n; ++j) {
         const int t = tbase + j;
         const uint32_t e = e_next;  // list entries run one tile ahead
@@ -1104,60 +1179,6 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         uint32_t pk[16];
         {
-          if (kDelta && j == 0) {
-            // Delta of this row: its dO (bf16 pairs in TMEM, copied there for
-            // dP) times its O (fp32, from the ring), this warpgroup's D/4
-            // columns, then the four warpgroups' parts added in order
-            uint32_t od[DQ / 2];
-            if constexpr (DQ == 32) {
-              tmem_ld16_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
-              tmem_wait_ld();
-              reg_fence16(od);
-            } else {
-              tmem_ld8_nowait(tmem + lane_base + Cfg::kTmemDO + q * (DQ / 2), od);
-              tmem_wait_ld();
-              reg_fence8(od);
-            }
-            // the O box holding these columns: box (q D/4) / 32, D / 64 boxes a slot
-            const int box = (q * DQ) / 32;
-            const int oidx = sidx + 2 + box / (D / 64);
-            if (!warp_wait(&slot_full[oidx % NS], (oidx / NS) & 1, ctl)) { ok = false; break; }
-            // row r of the box: 128 bytes, 16-byte chunks swizzled by r & 7
-            const uint32_t orow_s =
-                smem_u32(slot_ptr(oidx)) + (box % (D / 64)) * 16384 + r * 128;
-            const int cb0 = ((q * DQ) % 32) / 4;
-            float part = 0.f;
-#pragma unroll
-            for (int c = 0; c < DQ / 4; ++c) {
-              float4 ov;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(ov.x), "=f"(ov.y), "=f"(ov.z), "=f"(ov.w)
-                           : "r"(orow_s + (((cb0 + c) ^ (r & 7)) << 4)));
-              const uint32_t w0 = od[2 * c], w1 = od[2 * c + 1];
-              part = fmaf(ov.x, __uint_as_float(w0 << 16), part);
-              part = fmaf(ov.y, __uint_as_float(w0 & 0xFFFF0000u), part);
-              part = fmaf(ov.z, __uint_as_float(w1 << 16), part);
-              part = fmaf(ov.w, __uint_as_float(w1 & 0xFFFF0000u), part);
-            }
-            // the parts go through the dS buffer: the previous item's dQ
-            // store must have read it
-            if (ibase > 0 && !warp_wait(epi_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-            xch[q * 128 + r] = part;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xch_full);
-            if (!warp_wait(xch_full, ibase & 1, ctl)) { ok = false; break; }
-            del = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
-            if (threadIdx.x == 128) {
-              // every row warp has read O: its slots go back to the producer
-#pragma unroll
-              for (int s2 = 0; s2 < NO; ++s2) mbar_arrive(&slot_empty[(sidx + 2 + s2) % NS]);
-            }
-            if (q == 0) p.delta[stat] = del;
-            // dS overwrites the parts only once every warp has read them
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xch_free);
-            if (!warp_wait(xch_free, ibase & 1, ctl)) { ok = false; break; }
-          }
           uint32_t du[32];
           tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemDP + cbase, du);
           tmem_wait_ld();
