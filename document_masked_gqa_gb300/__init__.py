@@ -10,7 +10,7 @@ from ._lib import (  # noqa: F401
     DMA_ERR_UNSUPPORTED, DMA_ERR_WORKSPACE, DMA_OK, DMA_WARN_V_SATURATED, TILE_FULL, TILE_PARTIAL,
     TILE_SKIP, DmaError, Plan, dma_attn_bwd, dma_attn_bwd_delta, dma_attn_bwd_dkdv,
     dma_attn_bwd_dq, dma_attn_bwd_dq_delta, dma_attn_fwd, dma_cp_gather,
-    dma_cp_scatter, dma_debug_wait_probe, dma_plan, dma_plan_check,
+    dma_cp_permute, dma_cp_scatter, dma_cp_unpermute, dma_debug_wait_probe, dma_plan, dma_plan_check,
     dma_plan_set_wait_timeout, dma_plan_workspace_bytes, lib, plan_arrays,
     status_str,
 )

@@ -31,7 +31,7 @@ EXPORTED = [
     "dma_plan_check", "dma_plan_destroy", "dma_status_str", "dma_cp_gather",
     "dma_cp_scatter", "dma_plan_get_view", "dma_plan_set_wait_timeout",
     "dma_debug_wait_probe", "dma_attn_bwd_delta", "dma_attn_bwd_dkdv", "dma_attn_bwd_dq",
-    "dma_attn_fwd_noalloc", "dma_attn_bwd_dq_delta",
+    "dma_attn_fwd_noalloc", "dma_attn_bwd_dq_delta", "dma_cp_unpermute", "dma_cp_permute",
 ]
 
 
@@ -77,6 +77,8 @@ def _load():
         "dma_attn_bwd_dkdv": (i32, [vp] * 9),
         "dma_attn_bwd_dq": (i32, [vp] * 8),
         "dma_attn_bwd_dq_delta": (i32, [vp] * 9),
+        "dma_cp_unpermute": (i32, [vp, vp, i32, i32, i32, sz, vp]),
+        "dma_cp_permute": (i32, [vp, vp, i32, i32, i32, sz, vp]),
         "dma_attn_fwd_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, i32, f32] +
                                  [vp] * 7),
     }
@@ -318,6 +320,39 @@ def dma_cp_scatter(plan: Plan, local, full, stream=None):
     _check(lib().dma_cp_scatter(plan.handle, _ptr(local), _ptr(full), row_bytes,
                                 _stream(stream)), "dma_cp_scatter")
     return full
+
+
+def dma_cp_unpermute(gathered, full=None, stream=None):
+    """[cp, B, 2C, ...] rank-major rows (an all-gather of every rank's local
+    rows) -> [B, S, ...] natural order."""
+    import torch
+    cp, B, Lq = gathered.shape[:3]
+    if full is None:
+        full = torch.empty((B, cp * Lq) + tuple(gathered.shape[3:]), dtype=gathered.dtype,
+                           device=gathered.device)
+    _expect(gathered, gathered.dtype, tuple(gathered.shape), "gathered")
+    _expect(full, gathered.dtype, (B, cp * Lq) + tuple(gathered.shape[3:]), "full")
+    row_bytes = math.prod(gathered.shape[3:]) * gathered.element_size()
+    _check(lib().dma_cp_unpermute(_ptr(gathered), _ptr(full), B, cp * Lq, cp, row_bytes,
+                                  _stream(stream)), "dma_cp_unpermute")
+    return full
+
+
+def dma_cp_permute(full, cp_size, gathered=None, stream=None):
+    """[B, S, ...] natural order -> [cp, B, 2C, ...] rank-major rows (the
+    input of a reduce-scatter whose block r is rank r's rows)."""
+    import torch
+    B, S = full.shape[:2]
+    Lq = S // cp_size
+    if gathered is None:
+        gathered = torch.empty((cp_size, B, Lq) + tuple(full.shape[2:]), dtype=full.dtype,
+                               device=full.device)
+    _expect(full, full.dtype, tuple(full.shape), "full")
+    _expect(gathered, full.dtype, (cp_size, B, Lq) + tuple(full.shape[2:]), "gathered")
+    row_bytes = math.prod(full.shape[2:]) * full.element_size()
+    _check(lib().dma_cp_permute(_ptr(full), _ptr(gathered), B, S, cp_size, row_bytes,
+                                _stream(stream)), "dma_cp_permute")
+    return gathered
 
 
 def dma_debug_wait_probe(timeout_ns: int, status_dev, stream=None) -> int:

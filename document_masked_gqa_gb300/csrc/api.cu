@@ -443,6 +443,32 @@ dma_status dma_cp_scatter(dma_plan_t plan, const void* local, void* full, size_t
              : DMA_ERR_CUDA;
 }
 
+namespace {
+dma_status cp_chunk_copy(const void* src, void* dst, int batch, int seq_len, int cp_size,
+                         size_t row_bytes, bool to_natural, void* stream) {
+  if (batch < 0 || seq_len <= 0 || cp_size < 1 || row_bytes == 0 ||
+      seq_len % (2 * cp_size) != 0)
+    return DMA_ERR_INVALID_ARG;
+  if (batch == 0) return DMA_OK;
+  if (!src || !dst) return DMA_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * seq_len >= (1ll << 31)) return DMA_ERR_UNSUPPORTED;
+  return dma::launch_cp_chunk_copy(src, dst, batch, seq_len, cp_size, row_bytes, to_natural,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DMA_OK
+             : DMA_ERR_CUDA;
+}
+}  // namespace
+
+dma_status dma_cp_unpermute(const void* gathered, void* full, int batch, int seq_len,
+                            int cp_size, size_t row_bytes, void* stream) {
+  return cp_chunk_copy(gathered, full, batch, seq_len, cp_size, row_bytes, true, stream);
+}
+
+dma_status dma_cp_permute(const void* full, void* gathered, int batch, int seq_len,
+                          int cp_size, size_t row_bytes, void* stream) {
+  return cp_chunk_copy(full, gathered, batch, seq_len, cp_size, row_bytes, false, stream);
+}
+
 dma_status dma_plan_get_view(dma_plan_t plan, dma_plan_view* out) {
   if (!plan || !out) return DMA_ERR_INVALID_ARG;
   const dma::PlanDev& p = plan->d;

@@ -104,4 +104,6 @@ cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& 
 cudaError_t launch_kv_reduce(const dma_plan_s& p, float* dk, float* dv, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s);
+cudaError_t launch_cp_chunk_copy(const void* src, void* dst, int batch, int seq_len, int cp_size,
+                                 size_t row_bytes, bool to_natural, cudaStream_t s);
 }  // namespace dma

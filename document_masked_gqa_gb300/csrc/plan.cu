@@ -271,6 +271,32 @@ __global__ void cp_copy_kernel(PlanDev p, const uint8_t* __restrict__ src, uint8
   }
 }
 
+// Chunk-order copies between the rank-major layout of an all-gather over the
+// CP ranks, [cp_size][batch][2 C][row] (rank r's block holds its chunks r
+// and 2 CP - 1 - r), and natural sequence order, [batch][seq_len][row].
+// One block per (rank, sample, local row); `to_natural` selects the
+// direction.
+__global__ void cp_chunk_copy_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                     int batch, int seq_len, int cp_size, size_t row_bytes,
+                                     int to_natural) {
+  const long long i = blockIdx.x;  // ((rank * batch) + b) * 2C + l
+  const int C = seq_len / (2 * cp_size), Lq = 2 * C;
+  const int l = static_cast<int>(i % Lq);
+  const long long rb = i / Lq;
+  const int b = static_cast<int>(rb % batch), r = static_cast<int>(rb / batch);
+  const int pos = (l < C) ? (r * C + l) : ((2 * cp_size - 1 - r) * C + (l - C));
+  const long long nat = static_cast<long long>(b) * seq_len + pos;
+  const uint8_t* s = src + (to_natural ? i : nat) * row_bytes;
+  uint8_t* d = dst + (to_natural ? nat : i) * row_bytes;
+  if ((row_bytes & 15) == 0 && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(s);
+    uint4* d4 = reinterpret_cast<uint4*>(d);
+    for (size_t k = threadIdx.x; k < row_bytes / 16; k += blockDim.x) d4[k] = s4[k];
+  } else {
+    for (size_t k = threadIdx.x; k < row_bytes; k += blockDim.x) d[k] = s[k];
+  }
+}
+
 // The status a caller sees for a plan: the error word if set, else
 // DMA_WARN_V_SATURATED if the warning word says V was saturated, else OK.
 __global__ void status_out_kernel(const uint32_t* __restrict__ st, uint32_t* __restrict__ out) {
@@ -322,6 +348,16 @@ cudaError_t launch_cp_copy(const dma_plan_s& pl, const void* src, void* dst, siz
   if (rows == 0) return cudaSuccess;
   cp_copy_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
       p, static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), row_bytes, gather ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cp_chunk_copy(const void* src, void* dst, int batch, int seq_len, int cp_size,
+                                 size_t row_bytes, bool to_natural, cudaStream_t s) {
+  const long long rows = static_cast<long long>(batch) * seq_len;
+  if (rows == 0) return cudaSuccess;
+  cp_chunk_copy_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
+      static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), batch, seq_len, cp_size,
+      row_bytes, to_natural ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -209,6 +209,27 @@ dma_status dma_cp_scatter(dma_plan_t plan, const void* local, void* full,
                           size_t row_bytes, void* stream);
 
 /*
+ * Chunk-order copies for a real context-parallel exchange ("The Llama 3 Herd
+ * of Models - part 3/16", 3.3.2: K and V are all-gathered across the CP
+ * ranks before attention; "Numerical stability": the gradients are
+ * reduce-scattered in FP32).  An all-gather of every rank's local rows (its
+ * chunks r and 2*CP-1-r, in the local order of the plan) lands rank-major:
+ *   gathered : [cp_size][batch][2*C][row_bytes]   (C = seq_len / (2*cp_size))
+ * while the kernels read K and V in natural sequence order:
+ *   full     : [batch][seq_len][row_bytes]
+ * dma_cp_unpermute copies gathered -> full (after the all-gather of K, V);
+ * dma_cp_permute copies full -> gathered (before the reduce-scatter of a
+ * rank's partial dK, dV, so that block r of the result is rank r's rows).
+ * Plain device pointers, no plan needed; bit-exact; asynchronous on stream.
+ * Errors: DMA_ERR_INVALID_ARG for null pointers, row_bytes == 0 or seq_len
+ * not divisible by 2*cp_size.
+ */
+dma_status dma_cp_unpermute(const void* gathered, void* full, int batch, int seq_len,
+                            int cp_size, size_t row_bytes, void* stream);
+dma_status dma_cp_permute(const void* full, void* gathered, int batch, int seq_len,
+                          int cp_size, size_t row_bytes, void* stream);
+
+/*
  * Read-only view of the plan's device arrays (for tests and tools).
  * All pointers are device pointers into the caller's workspace.
  *   qpos      int32 [2C]             global position of each local row
