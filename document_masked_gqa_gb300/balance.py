@@ -17,6 +17,15 @@ of `granule` positions, so that every chunk carries about the same work.
 That alternative is a report only: the kernels of this package run the
 pages' equal-length chunks.
 
+A second model counts what the kernels actually do: the block-mask
+builder's classes of (query tile, key tile) pairs.  A full or a partial pair
+costs a whole 128 x 128 tile of tensor work whatever its number of allowed
+pairs, partial pairs add the masking, and every work item has a fixed cost
+(its first loads, its epilogue).  ``rank_costs`` counts, per rank, the
+non-skipped and partial tile pairs and the work items; ``fit_costs`` fits
+the per-tile and per-item constants to measured per-rank step times by
+least squares; ``predict_ms`` applies them.
+
 Host-side planning arithmetic (numpy), no device work.
 """
 from __future__ import annotations
@@ -151,6 +160,85 @@ def report(cu_doc_lens, batch: int, seq_len: int, cp_size: int, granule: int = 1
                       "pairs_per_rank": alt.sum(axis=1).tolist(),
                       "imbalance": imbalance(alt)},
     }
+
+
+TILE = 128  # positions per key tile; a query tile holds TILE rows (TILE / g positions)
+KV_SPLIT_ITEMS, KV_MAX_SEGS = 256, 8  # the dK/dV pass splits key tiles below 256 items
+
+
+def _doc_starts(cu_doc_lens, batch: int, seq_len: int, pos: np.ndarray) -> np.ndarray:
+    """[batch, len(pos)] first position (within the sample) of the document
+    holding each position."""
+    cu = np.asarray(cu_doc_lens, dtype=np.int64)
+    out = np.empty((batch, len(pos)), dtype=np.int64)
+    for b in range(batch):
+        g = b * seq_len + pos
+        d = np.searchsorted(cu, g, side="right") - 1
+        out[b] = cu[d] - b * seq_len
+    return out
+
+
+def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int,
+                group: int) -> dict:
+    """Full and partial (query tile, key tile) pairs of one rank, summed over
+    samples (per K/V head).  A query tile is TILE / group consecutive local
+    positions, whose allowed keys are [start of its document, position]; both
+    ends grow with the position, so the tile meets key tile [k0, k1] iff its
+    first row whose position reaches k0 starts its document at or before
+    k1, and covers it fully iff its last row's document starts at or before
+    k0 and its first position is at or past k1."""
+    P = TILE // group
+    n = 2 * cp_size
+    C = seq_len // n
+    pos = np.concatenate([np.arange(cp_rank * C, (cp_rank + 1) * C),
+                          np.arange((n - 1 - cp_rank) * C, (n - cp_rank) * C)])
+    nqt, nkt = len(pos) // P, seq_len // TILE
+    lo = _doc_starts(cu_doc_lens, batch, seq_len, pos)
+    k0 = (np.arange(nkt) * TILE)[None, :]
+    k1 = k0 + TILE - 1
+    q_first = pos[::P][:, None]
+    full = partial = 0
+    for b in range(batch):
+        lo_b = lo[b].reshape(nqt, P)
+        r_star = np.clip(k0 - q_first, 0, P)                  # first row with position >= k0
+        meets = r_star < P
+        lo_at = np.take_along_axis(lo_b, np.minimum(r_star, P - 1), axis=1)
+        meets &= lo_at <= k1
+        covers = (lo_b[:, -1:] <= k0) & (k1 <= q_first)
+        full += int((meets & covers).sum())
+        partial += int((meets & ~covers).sum())
+    return {"full": full, "partial": partial}
+
+
+def rank_costs(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int,
+               n_heads: int, n_kv_heads: int) -> np.ndarray:
+    """Cost features of one rank's step: [tile pairs (full + partial), partial
+    pairs, work items, 1], tile pairs and items over all samples and K/V
+    heads.  Items: the forward's and dQ's (query tile, K/V head) pairs and
+    dK/dV's (key tile, K/V head, list segment) triples."""
+    g = n_heads // n_kv_heads
+    c = tile_counts(cu_doc_lens, batch, seq_len, cp_size, cp_rank, g)
+    nqt = (seq_len // cp_size) // (TILE // g)
+    nkt = seq_len // TILE
+    kv_items = batch * nkt * n_kv_heads
+    segs = 1 if kv_items >= KV_SPLIT_ITEMS else min(KV_MAX_SEGS, -(-KV_SPLIT_ITEMS // kv_items))
+    items = 2 * batch * nqt * n_kv_heads + kv_items * segs
+    return np.array([(c["full"] + c["partial"]) * n_kv_heads, c["partial"] * n_kv_heads,
+                     items, 1.0], dtype=np.float64)
+
+
+def fit_costs(features, times_ms) -> np.ndarray:
+    """Least-squares constants (ms per tile pair, per partial pair, per item,
+    and a fixed part) from rows of rank_costs features and measured step
+    times of those ranks."""
+    a = np.asarray(features, dtype=np.float64)
+    t = np.asarray(times_ms, dtype=np.float64)
+    coef, *_ = np.linalg.lstsq(a, t, rcond=None)
+    return coef
+
+
+def predict_ms(features, coef) -> np.ndarray:
+    return np.asarray(features, dtype=np.float64) @ np.asarray(coef, dtype=np.float64)
 
 
 def _main(argv=None) -> int:

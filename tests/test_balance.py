@@ -108,3 +108,37 @@ def test_equal_work_bounds_on_the_grid():
               for c in range(8)]
     # every chunk within a few granules' work of the ideal share
     assert max(chunks) / (sum(chunks) / 8) < 1.1
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b", "70b", "sparse", "405b-logu"])
+def test_tile_counts_match_oracle_block_mask(name):
+    """Host counts of full / partial tile pairs against the oracle's tile
+    classes, which look at every element of the explicit mask."""
+    from oracle import blockmask as ob
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    ranks = w.ranks if name != "405b-logu" else (15,)  # the oracle's brute force is slow at 128K
+    for r in ranks:
+        got = balance.tile_counts(cu, w.batch, w.seq_len, w.cp_size, r, w.group)
+        cls = ob.tile_classes(cu, w.batch, w.seq_len, w.cp_size, r, w.group)
+        assert got["full"] == int((cls == ob.FULL).sum()), (name, r)
+        assert got["partial"] == int((cls == ob.PARTIAL).sum()), (name, r)
+
+
+def test_cost_fit_recovers_known_constants():
+    """fit_costs on times made from known constants (plus tiny noise) returns
+    them; predict_ms reproduces the times."""
+    rng = np.random.default_rng(3)
+    coef = np.array([2.0e-4, 5.0e-5, 1.0e-3, 0.03])
+    feats = []
+    for name in ["8b", "70b", "sparse", "405b-logu", "405b-1doc"]:
+        w = wl.WORKLOADS[name]
+        cu = wl.cu_doc_lens(w)
+        for r in w.ranks:
+            feats.append(balance.rank_costs(cu, w.batch, w.seq_len, w.cp_size, r, w.n_heads,
+                                            w.n_kv_heads))
+    feats = np.array(feats)
+    times = balance.predict_ms(feats, coef) * (1 + 1e-6 * rng.standard_normal(len(feats)))
+    got = balance.fit_costs(feats, times)
+    assert np.allclose(got, coef, rtol=1e-3, atol=1e-6)
+    assert np.allclose(balance.predict_ms(feats, got), times, rtol=1e-4)
