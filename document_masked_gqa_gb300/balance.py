@@ -146,13 +146,15 @@ def doc_aware_bounds(cu_doc_lens, batch: int, seq_len: int, cp_size: int,
     return out
 
 
-def report(cu_doc_lens, batch: int, seq_len: int, cp_size: int, granule: int = 128) -> dict:
+def report(cu_doc_lens, batch: int, seq_len: int, cp_size: int, granule: int = 128,
+           n_heads: int | None = None, n_kv_heads: int | None = None) -> dict:
     """Per-rank work and imbalance of the pages' chunking and of the
-    document-aware alternative."""
+    document-aware alternative; with the head counts also the tile-cost
+    model's predicted step time per rank (COST_MS_GB300)."""
     pages = rank_work(cu_doc_lens, batch, seq_len, cp_size)
     bounds = doc_aware_bounds(cu_doc_lens, batch, seq_len, cp_size, granule)
     alt = rank_work(cu_doc_lens, batch, seq_len, cp_size, bounds)
-    return {
+    out = {
         "cp_size": cp_size,
         "pairs_per_rank": pages.sum(axis=1).tolist(),
         "imbalance": imbalance(pages),
@@ -160,6 +162,13 @@ def report(cu_doc_lens, batch: int, seq_len: int, cp_size: int, granule: int = 1
                       "pairs_per_rank": alt.sum(axis=1).tolist(),
                       "imbalance": imbalance(alt)},
     }
+    if n_heads and n_kv_heads:
+        feats = [rank_costs(cu_doc_lens, batch, seq_len, cp_size, r, n_heads, n_kv_heads)
+                 for r in range(cp_size)]
+        ms = predict_ms(feats)
+        out["tile_cost_model"] = {"predicted_ms_per_rank": [round(float(x), 4) for x in ms],
+                                  "imbalance": imbalance(ms)}
+    return out
 
 
 TILE = 128  # positions per key tile; a query tile holds TILE rows (TILE / g positions)
@@ -181,7 +190,8 @@ def _doc_starts(cu_doc_lens, batch: int, seq_len: int, pos: np.ndarray) -> np.nd
 def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int,
                 group: int) -> dict:
     """Full and partial (query tile, key tile) pairs of one rank, summed over
-    samples (per K/V head).  A query tile is TILE / group consecutive local
+    samples (per K/V head), and the longest row list (key tiles of one query
+    tile) and column list (query tiles of one key tile).  A query tile is TILE / group consecutive local
     positions, whose allowed keys are [start of its document, position]; both
     ends grow with the position, so the tile meets key tile [k0, k1] iff its
     first row whose position reaches k0 starts its document at or before
@@ -198,6 +208,7 @@ def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: in
     k1 = k0 + TILE - 1
     q_first = pos[::P][:, None]
     full = partial = 0
+    max_row = max_col = 0
     for b in range(batch):
         lo_b = lo[b].reshape(nqt, P)
         r_star = np.clip(k0 - q_first, 0, P)                  # first row with position >= k0
@@ -207,15 +218,21 @@ def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: in
         covers = (lo_b[:, -1:] <= k0) & (k1 <= q_first)
         full += int((meets & covers).sum())
         partial += int((meets & ~covers).sum())
-    return {"full": full, "partial": partial}
+        max_row = max(max_row, int(meets.sum(axis=1).max()))
+        max_col = max(max_col, int(meets.sum(axis=0).max()))
+    return {"full": full, "partial": partial, "max_row": max_row, "max_col": max_col}
 
 
 def rank_costs(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int,
-               n_heads: int, n_kv_heads: int) -> np.ndarray:
-    """Cost features of one rank's step: [tile pairs (full + partial), partial
-    pairs, work items, 1], tile pairs and items over all samples and K/V
-    heads.  Items: the forward's and dQ's (query tile, K/V head) pairs and
-    dK/dV's (key tile, K/V head, list segment) triples."""
+               n_heads: int, n_kv_heads: int, n_sms: int = 152) -> np.ndarray:
+    """Cost features of one rank's step: [tile-pair makespan, partial pairs,
+    work items, 1].  The makespan counts, for each of the three attention
+    kernels, the tile pairs the busiest of n_sms persistent CTAs must run at
+    least: the kernel's tile pairs (all samples and K/V heads) shared evenly,
+    or its longest work item, whichever is more (the forward and dQ walk row
+    lists, dK/dV column lists cut into its list segments).  Items: the
+    forward's and dQ's (query tile, K/V head) pairs and dK/dV's (key tile,
+    K/V head, list segment) triples."""
     g = n_heads // n_kv_heads
     c = tile_counts(cu_doc_lens, batch, seq_len, cp_size, cp_rank, g)
     nqt = (seq_len // cp_size) // (TILE // g)
@@ -223,22 +240,34 @@ def rank_costs(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int
     kv_items = batch * nkt * n_kv_heads
     segs = 1 if kv_items >= KV_SPLIT_ITEMS else min(KV_MAX_SEGS, -(-KV_SPLIT_ITEMS // kv_items))
     items = 2 * batch * nqt * n_kv_heads + kv_items * segs
-    return np.array([(c["full"] + c["partial"]) * n_kv_heads, c["partial"] * n_kv_heads,
-                     items, 1.0], dtype=np.float64)
+    tiles = (c["full"] + c["partial"]) * n_kv_heads
+    makespan = (2 * max(tiles / n_sms, c["max_row"])
+                + max(tiles / n_sms, -(-c["max_col"] // segs)))
+    return np.array([makespan, c["partial"] * n_kv_heads, items, 1.0], dtype=np.float64)
 
 
 def fit_costs(features, times_ms) -> np.ndarray:
-    """Least-squares constants (ms per tile pair, per partial pair, per item,
-    and a fixed part) from rows of rank_costs features and measured step
-    times of those ranks."""
+    """Non-negative least-squares constants (ms per tile pair of makespan,
+    per partial pair, per item, and a fixed part) from rows of rank_costs
+    features and measured step times of those ranks."""
+    from scipy.optimize import nnls
     a = np.asarray(features, dtype=np.float64)
     t = np.asarray(times_ms, dtype=np.float64)
-    coef, *_ = np.linalg.lstsq(a, t, rcond=None)
+    coef, _ = nnls(a, t)
     return coef
 
 
-def predict_ms(features, coef) -> np.ndarray:
-    return np.asarray(features, dtype=np.float64) @ np.asarray(coef, dtype=np.float64)
+# Constants fitted (fit_costs) to the measured per-rank step times of the
+# 8B, 70B, sparse-stress and both 405B workloads on one GB300 (152 SMs):
+# ms per tile pair of makespan, per partial pair, per work item, fixed.
+COST_MS_GB300 = np.array([1.31844e-03, 0.0, 4.14717e-06, 9.95450e-02])
+
+
+def predict_ms(features, coef=None) -> np.ndarray:
+    """Step time (ms) of each row of rank_costs features; default constants:
+    COST_MS_GB300."""
+    c = COST_MS_GB300 if coef is None else coef
+    return np.asarray(features, dtype=np.float64) @ np.asarray(c, dtype=np.float64)
 
 
 def _main(argv=None) -> int:
@@ -254,7 +283,8 @@ def _main(argv=None) -> int:
     args = ap.parse_args(argv)
     w = wl.WORKLOADS[args.workload]
     cp = args.cp_size or w.cp_size
-    rep = report(wl.cu_doc_lens(w), w.batch, w.seq_len, cp, args.granule)
+    rep = report(wl.cu_doc_lens(w), w.batch, w.seq_len, cp, args.granule, w.n_heads,
+                 w.n_kv_heads)
     rep["workload"] = w.name
     print(json.dumps(rep))
     return 0
