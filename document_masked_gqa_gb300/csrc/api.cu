@@ -64,7 +64,7 @@ WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int
     off = align_up(off + bytes, 256);
     return at;
   };
-  w.status = take(16);
+  w.status = take(dma::kStatusBytes);
   w.qpos = take(4 * Lq);
   w.doc_lo = take(4 * B * Lq);
   w.doc_hi = take(4 * B * static_cast<size_t>(seq_len));
@@ -179,6 +179,7 @@ dma_status init_plan(dma_plan_s& pl, const int32_t* cu_doc_lens, int n_docs, int
     if (t > 0) p.timeout_ns = t;
   }
   p.status = reinterpret_cast<uint32_t*>(ws + w.status);
+  p.sched = reinterpret_cast<int32_t*>(ws + w.status + dma::kSchedOffset);
   p.qpos = reinterpret_cast<int32_t*>(ws + w.qpos);
   p.doc_lo = reinterpret_cast<int32_t*>(ws + w.doc_lo);
   p.doc_hi = reinterpret_cast<int32_t*>(ws + w.doc_hi);

@@ -171,9 +171,11 @@ struct DkdvCfg {
   static constexpr int kStage = kDO + 2 * kTile;
   static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
   static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 28;
+  // work items published by the producer to the other roles (ItemRing)
+  static constexpr int kRing = 8;
+  static constexpr int kNumBars = 28 + 2 * kRing;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kNeed = kMisc + 16;
+  static constexpr int kNeed = kMisc + 16 + 4 * kRing;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
   // TMEM: dV [0,128), dK [128,256), tile buffers [256,384) and [384,512);
   // once dP^T has been read, warpgroup w's P^T sits in columns
@@ -207,10 +209,11 @@ __device__ __forceinline__ DkdvItem dkdv_item(const PlanDev& p, int item) {
   return it;
 }
 
-// Persistent: CTA c takes work items in snake order.  Every role keeps the
-// same counters across non-empty items: query tiles so far (tbase: the Q /
-// dO stage and the parity of every per-tile barrier) and items so far
-// (ibase: parity of kv_full, kv_empty, acc_done, acc_free).
+// Persistent: the producer thread takes work items from the plan's counter
+// one at a time and publishes them to every other role (ItemRing).  Every
+// role keeps the same counters across non-empty items: query tiles so far
+// (tbase: the Q / dO stage and the parity of every per-tile barrier) and
+// items so far (ibase: parity of kv_full, kv_empty, acc_done, acc_free).
 template <int D>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -220,11 +223,17 @@ __global__ void __launch_bounds__(512, 1)
   using Cfg = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  int32_t* const ctr = p.sched + kSchedDkdv;
   if (__syncthreads_or(threadIdx.x == 0 &&
-                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u))
+                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u)) {
+    if (threadIdx.x == 0) items_exit(ctr);
     return;
+  }
   if (pad + Cfg::kNeed > static_cast<uint32_t>(Cfg::kAlloc)) {  // cannot lay out the tiles
-    if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_UNSUPPORTED));
+    if (threadIdx.x == 0) {
+      atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_UNSUPPORTED));
+      items_exit(ctr);
+    }
     return;
   }
   uint8_t* smem = smem_raw + pad;
@@ -255,6 +264,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* acc_done = bars + 25;  // an item's dV, dK complete
   uint64_t* kv_empty = bars + 26;  // an item's last S^T and dP^T done (two commits)
   uint64_t* acc_free = bars + 27;  // the epilogue warps have read an item's dV, dK
+  uint64_t* item_full = bars + 28;  // [kRing]
+  uint64_t* item_empty = item_full + Cfg::kRing;
+  const ItemRing<Cfg::kRing> ring{reinterpret_cast<volatile int*>(smem + Cfg::kMisc + 16), item_full,
+                                  item_empty};
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
 
@@ -277,6 +290,12 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(acc_done, 1);
     mbar_init(kv_empty, 2);
     mbar_init(acc_free, 4);
+    // readers of the item ring: three issuers, eight element-wise warps, four
+    // epilogue warps
+    for (int i = 0; i < Cfg::kRing; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 15);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -299,9 +318,15 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tv);
       int last_t = -1, ibase = 0, tbase = 0;
       bool kv_pending = false, ok = true;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
+      // the next index is taken one item ahead, so that the atomic's latency
+      // is hidden; every index is published, empty items too (the epilogue
+      // writes their zero rows)
+      int next_idx = take_item(ctr);
+      for (int rk = 0; ok; ++rk) {
+        const int item = next_idx < n_items ? next_idx : -1;
+        if (item >= 0) next_idx = take_item(ctr);
+        if (!ring.put(rk, item, ctl)) { ok = false; break; }
+        if (item < 0) break;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         const int krow0 = it.b * p.seq_len + it.kt * kTileN;
@@ -361,9 +386,10 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t last_parity = 0;
       bool ok = true;
       int tbase = 0, ibase = 0;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
+      for (int rk = 0; ok; ++rk) {
+        int item;
+        if (!ring.get(rk, item, ctl)) { ok = false; break; }
+        if (item < 0) break;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
@@ -408,9 +434,10 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t last_parity = 0;
       bool ok = true;
       int tbase = 0, ibase = 0;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
+      for (int rk = 0; ok; ++rk) {
+        int item;
+        if (!ring.get(rk, item, ctl)) { ok = false; break; }
+        if (item < 0) break;
         const DkdvItem it = dkdv_item(p, item);
         if (it.n == 0) continue;
         for (int i = 0; i < it.n; ++i) {
@@ -484,9 +511,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t buf_cols = tmem + lane_base + Cfg::kTmemBuf + 64 * w;
     bool ok = true;
     int tbase = 0;
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+    for (int rk = 0; ok; ++rk) {
+      int item;
+      if (!ring.get_warp(rk, item, ctl)) { ok = false; break; }
+      if (item < 0) break;
       const DkdvItem it = dkdv_item(p, item);
       if (it.n == 0) continue;
       const int key = it.kt * kTileN + r;  // position within the sample
@@ -597,9 +625,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t stg = smem_u32(smem + Cfg::kStage) + wq * 4096;
     bool ok = true;
     int ibase = 0;
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
+    for (int rk = 0; ok; ++rk) {
+      int item;
+      if (!ring.get_warp(rk, item, ctl)) { ok = false; break; }
+      if (item < 0) break;
       const DkdvItem it = dkdv_item(p, item);
       const int row0 = (it.seg * p.batch + it.b) * p.seq_len + it.kt * kTileN + 32 * wq;
       const bool empty = it.n == 0;
@@ -654,6 +683,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) items_exit(ctr);
 }
 
 // ------------------------------------------------------------------- dQ

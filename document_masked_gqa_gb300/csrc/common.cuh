@@ -29,6 +29,10 @@ __host__ __device__ inline int kv_segments(int batch, int seq_len, int n_kv_head
   return static_cast<int>(s < kKvMaxSegs ? s : kKvMaxSegs);
 }
 
+constexpr int kSchedFwd = 0, kSchedDkdv = 2;
+// bytes at the start of the workspace: status words [0, 16), work counters [32, 48)
+constexpr int kStatusBytes = 64, kSchedOffset = 32;
+
 // Device-visible shape and workspace pointers of one rank's plan.
 struct PlanDev {
   int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
@@ -37,6 +41,9 @@ struct PlanDev {
   float scale_log2;  // scale * log2(e)
   uint64_t timeout_ns;
   uint32_t* status;   // [0] error word (kernels do nothing once set), [1] warning bits
+  int32_t* sched;     // work counters of the persistent kernels, two per kernel
+                      // (next item, CTAs exited): forward at kSchedFwd, dK/dV at
+                      // kSchedDkdv; zeroed with the status words by the plan
   int32_t* qpos;      // [Lq]
   int32_t* doc_lo;    // [B][Lq]
   int32_t* doc_hi;    // [B][S] end (exclusive) of each key position's document

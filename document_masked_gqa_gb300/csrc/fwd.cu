@@ -68,9 +68,11 @@ struct FwdCfg {
   static constexpr int kMeta = kXchg + (2 * 2 * 128 + 2 * 2 * 128 + 2 * 128) * 4;
   static constexpr int kMetaInts = 4 + 2 * 128;
   static constexpr int kBar = kMeta + 2 * kMetaInts * 4;
-  static constexpr int kNumBars = 4 * kKVSlots + 3 * 3 + 2 + 1 + 2 + 1 + 2 + 2;
+  // work items published by the producer to the other roles (ItemRing)
+  static constexpr int kRing = 8;
+  static constexpr int kNumBars = 4 * kKVSlots + 3 * 3 + 2 + 1 + 2 + 1 + 2 + 2 + 2 * kRing;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kEnd = kMisc + 16;
+  static constexpr int kEnd = kMisc + 16 + 4 * kRing;
   static constexpr int kSmemBytes = kEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM: three S buffers (128 columns each; P overwrites part of one as
@@ -108,8 +110,10 @@ __device__ __forceinline__ FwdItem fwd_item(const PlanDev& p, int item) {
   return it;
 }
 
-// Persistent: CTA c takes work items in snake order.  Every role keeps the
-// same counters across non-empty items: the key tiles processed so far
+// Persistent: the producer thread takes work items from the plan's counter
+// one at a time and publishes them to the S and P V issuers and the epilogue
+// warps (ItemRing); the softmax warps get theirs from the epilogue warps'
+// metadata.  Every role keeps the same counters across non-empty items: the key tiles processed so far
 // (tbase: K / V slot t % kKVSlots, S buffer t % 3 and every per-tile barrier
 // parity follow from the global tile index t) and the items so far (ibase:
 // Q buffer and metadata buffer ibase % 2, parity of l_ready and o_free).
@@ -122,11 +126,14 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int NS = Cfg::kKVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  int32_t* const ctr = p.sched + kSchedFwd;
 
   // a failed plan or an earlier expired wait: do nothing (CTA-uniform)
   if (__syncthreads_or(threadIdx.x == 0 &&
-                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u))
+                       *reinterpret_cast<volatile uint32_t*>(p.status) != 0u)) {
+    if (threadIdx.x == 0) items_exit(ctr);
     return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.group, Lq = p.local_len;
@@ -147,6 +154,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* o_free = meta_ready + 2;   // the epilogue warps have read an item's O
   uint64_t* q_full = o_free + 1;       // [2] an item's Q in Q buffer item % 2
   uint64_t* q_empty = q_full + 2;      // [2] ... and all its S products done
+  uint64_t* item_full = q_empty + 2;   // [kRing]
+  uint64_t* item_empty = item_full + Cfg::kRing;
+  const ItemRing<Cfg::kRing> ring{reinterpret_cast<volatile int*>(smem + Cfg::kMisc + 16), item_full,
+                                  item_empty};
   uint8_t* sQ = smem + Cfg::kQbuf;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + Cfg::kMisc + 4);
@@ -174,6 +185,12 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(l_ready, 8);
     mbar_init(o_free, 4);
+    // readers of the item ring: the producer's V cursor, the two issuers, the
+    // four epilogue warps
+    for (int i = 0; i < Cfg::kRing; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 7);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -199,30 +216,43 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       struct Cursor {
-        int k;     // snake step of the current item
-        int j;     // tile within it
+        int r;     // ring entries read (the K cursor: published)
+        int j;     // tile within the current item
         int t;     // global tile index
         int item;  // non-empty items entered so far - 1
         FwdItem it;
         bool done;
       };
-      // move a cursor to the first tile of the next non-empty item
-      auto next_item = [&](Cursor& c) {
-        for (++c.k; c.k * static_cast<int>(gridDim.x) < n_items; ++c.k) {
-          const int item = snake_item(c.k);
-          if (item >= n_items) continue;
+      // move a cursor to the first tile of the next non-empty item: the K
+      // cursor takes the next index from the counter (one item ahead, so
+      // that the atomic's latency is hidden) and publishes it unless its
+      // list is empty; the V cursor reads what the K cursor published
+      int next_idx = take_item(ctr);
+      auto next_item = [&](Cursor& c, bool is_k) -> bool {
+        for (;;) {
+          int item;
+          if (is_k) {
+            item = next_idx < n_items ? next_idx : -1;
+            if (item >= 0) {
+              next_idx = take_item(ctr);
+              if (fwd_item(p, item).n == 0) continue;
+            }
+            if (!ring.put(c.r++, item, ctl)) return false;
+          } else if (!ring.get(c.r++, item, ctl)) {
+            return false;
+          }
+          if (item < 0) {
+            c.done = true;
+            return true;
+          }
           c.it = fwd_item(p, item);
-          if (c.it.n == 0) continue;
           c.j = 0;
           ++c.item;
-          return;
+          return true;
         }
-        c.done = true;
       };
-      Cursor kc{-1, 0, 0, -1, FwdItem{}, false}, vc = kc;
-      next_item(kc);
-      next_item(vc);
-      bool ok = true;
+      Cursor kc{0, 0, 0, -1, FwdItem{}, false}, vc = kc;
+      bool ok = next_item(kc, true) && next_item(vc, false);
       int q_issued = 0;  // Q loads issued (item index of the next one)
       while (ok && !vc.done) {
         const bool do_k = !kc.done && kc.t <= vc.t + 1;
@@ -251,7 +281,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int ch = 0; ch < Cfg::kChunks; ++ch)
           tma_load_2d(dst + ch * Cfg::kRegion, do_k ? &tk : &tv, full, c.it.kvh * D + ch * 64, krow);
         ++c.t;
-        if (++c.j == c.it.n) next_item(c);
+        if (++c.j == c.it.n && !next_item(c, do_k)) ok = false;
       }
       if (!ok) {  // drain this CTA's copies still in flight
         for (int t = max(0, kc.t - NS); t < kc.t; ++t)
@@ -277,9 +307,10 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t last_parity = 0;
       bool ok = true;
       int tbase = 0, ibase = 0;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
+      for (int rk = 0; ok; ++rk) {
+        int item;
+        if (!ring.get(rk, item, ctl)) { ok = false; break; }
+        if (item < 0) break;
         const FwdItem it = fwd_item(p, item);
         if (it.n == 0) continue;
         const int qb = ibase & 1;
@@ -518,31 +549,36 @@ __global__ void __launch_bounds__(512, 1)
       stage_meta(qb, mi);
       warp_arrive(&meta_ready[qb]);
     };
-    bool first = true;
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      const int item = snake_item(k);
-      if (item >= n_items) continue;
-      const FwdItem it = fwd_item(p, item);
-      if (it.n == 0) continue;
-      if (first) {
-        post_meta(ibase & 1, &it);
-        first = false;
-      }
-      // the next item's metadata into the other buffer, so that the softmax
-      // warps run on into the next item without a gap
-      {
-        bool more = false;
-        for (int kx = k + 1; kx * static_cast<int>(gridDim.x) < n_items; ++kx) {
-          const int cand = snake_item(kx);
-          if (cand >= n_items) continue;
-          const FwdItem nx = fwd_item(p, cand);
-          if (nx.n == 0) continue;
-          post_meta((ibase + 1) & 1, &nx);
-          more = true;
-          break;
+    // the next non-empty item from the ring (found = false at the end)
+    int rk = 0;
+    auto read_item = [&](FwdItem& out, bool& found) -> bool {
+      for (;;) {
+        int item;
+        if (!ring.get_warp(rk++, item, ctl)) return false;
+        if (item < 0) {
+          found = false;
+          return true;
         }
-        if (!more) post_meta((ibase + 1) & 1, nullptr);  // end of this CTA's items
+        out = fwd_item(p, item);
+        if (out.n > 0) {
+          found = true;
+          return true;
+        }
       }
+    };
+    FwdItem nx{};
+    bool have = false;
+    ok = read_item(nx, have);
+    if (ok) post_meta(0, have ? &nx : nullptr);  // nothing at all: releases the softmax warps
+    while (ok && have) {
+      const FwdItem it = nx;
+      // the next item's metadata into the other buffer, so that the softmax
+      // warps run on into the next item without a gap (n = 0: the end)
+      if (!read_item(nx, have)) {
+        ok = false;
+        break;
+      }
+      post_meta((ibase + 1) & 1, have ? &nx : nullptr);
       const int t_last = tbase + it.n - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(l_ready, ibase & 1, ctl)) ||
           !__all_sync(0xffffffffu,
@@ -589,7 +625,6 @@ __global__ void __launch_bounds__(512, 1)
       tbase += it.n;
       ++ibase;
     }
-    if (ok && first) post_meta(0, nullptr);  // no items at all: release the softmax warps
     if (lane == 0) bulk_wait_all();
   }
 
@@ -599,6 +634,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+  if (threadIdx.x == 0) items_exit(ctr);
 }
 
 // V (bf16) -> fp16 copy for the P V product, 8 elements per thread.  NaN and

@@ -324,7 +324,7 @@ __global__ void wait_probe_kernel(uint64_t timeout_ns, uint32_t* status) {
 
 cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t) * 4, s);
+  cudaError_t e = cudaMemsetAsync(p.status, 0, kStatusBytes, s);  // status words, work counters
   if (e != cudaSuccess) return e;
   if (p.batch == 0) return cudaSuccess;
   const long long n = static_cast<long long>(p.batch) * p.seq_len;

@@ -434,4 +434,60 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// ------------------------------------------- work items of a persistent kernel
+// The persistent kernels take their work items in list order (longest list
+// first) from a global counter, one item at a time: the CTA's producer thread
+// takes the next index when it enters an item, so an SM that runs ahead of
+// the others (shorter items, a faster clock, less contention) takes more of
+// them and all SMs finish close together.  The producer publishes each index
+// (-1 once the list is exhausted) to the CTA's other roles through a ring of
+// R shared-memory slots; every reader takes every slot in order and releases
+// it as soon as it has copied the index.
+template <int R>
+struct ItemRing {
+  volatile int* slot;  // [R]
+  uint64_t* full;      // [R] one arrival: the producer
+  uint64_t* empty;     // [R] one arrival per reader
+  // publish entry k (waits until every reader has released entry k - R)
+  __device__ __forceinline__ bool put(int k, int item, const WaitCtl& c) const {
+    const int s = k % R;
+    if (!mbar_wait(&empty[s], ((k / R) & 1) ^ 1u, c)) return false;
+    slot[s] = item;
+    mbar_arrive(&full[s]);
+    return true;
+  }
+  // entry k, read by one thread
+  __device__ __forceinline__ bool get(int k, int& item, const WaitCtl& c) const {
+    const int s = k % R;
+    if (!mbar_wait(&full[s], (k / R) & 1, c)) return false;
+    item = slot[s];
+    mbar_arrive(&empty[s]);
+    return true;
+  }
+  // entry k, read by a whole warp (one arrival)
+  __device__ __forceinline__ bool get_warp(int k, int& item, const WaitCtl& c) const {
+    const int s = k % R;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / R) & 1, c))) return false;
+    item = slot[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
+    return true;
+  }
+};
+
+// ctr[0]: next item of the list; ctr[1]: CTAs of the launch that have exited.
+__device__ __forceinline__ int take_item(int32_t* ctr) { return atomicAdd(ctr, 1); }
+
+// Called once per CTA (one thread) as it exits, on every path: the last CTA
+// of the launch puts both counters back to zero for the next launch.  Every
+// CTA has taken its last index before it gets here.
+__device__ __forceinline__ void items_exit(int32_t* ctr) {
+  __threadfence();
+  if (atomicAdd(ctr + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(ctr, 0);
+    atomicExch(ctr + 1, 0);
+    __threadfence();
+  }
+}
+
 }  // namespace dma
