@@ -169,11 +169,12 @@ struct DkdvCfg {
   // dK / dV staging of the epilogue warps: per warp one 4 KB block of
   // 32 rows x 32 fp32 in the 128-byte swizzled layout of a TMA store
   static constexpr int kStage = kDO + 2 * kTile;
-  static constexpr int kCOL = kStage + 4 * 4096;  // [warpgroup][2][64 -LSE*log2e, 64 Delta]
-  static constexpr int kBar = kCOL + 2 * 2 * 128 * 4;
+  // per element-wise warp: [2 stages][64 -LSE*log2e, 64 Delta]
+  static constexpr int kCOL = kStage + 4 * 4096;
+  static constexpr int kBar = kCOL + 8 * 2 * 128 * 4;
   // work items published by the producer to the other roles (ItemRing)
   static constexpr int kRing = 8;
-  static constexpr int kNumBars = 28 + 2 * kRing;
+  static constexpr int kNumBars = 26 + 2 * kRing;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kNeed = kMisc + 16 + 4 * kRing;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
@@ -260,11 +261,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* ds_full = bars + 17;   // [2 buffers][2 halves] dS^T written: query columns
                                    // [0, 32) and [64, 96) of the tile, then the rest
   uint64_t* buf_free = bars + 21;  // [2] dV and dK of the buffer's tile done
-  uint64_t* col_ready = bars + 23; // [2] per warpgroup: statistics staged
-  uint64_t* acc_done = bars + 25;  // an item's dV, dK complete
-  uint64_t* kv_empty = bars + 26;  // an item's last S^T and dP^T done (two commits)
-  uint64_t* acc_free = bars + 27;  // the epilogue warps have read an item's dV, dK
-  uint64_t* item_full = bars + 28;  // [kRing]
+  uint64_t* acc_done = bars + 23;  // an item's dV, dK complete
+  uint64_t* kv_empty = bars + 24;  // an item's last S^T and dP^T done (two commits)
+  uint64_t* acc_free = bars + 25;  // the epilogue warps have read an item's dV, dK
+  uint64_t* item_full = bars + 26;  // [kRing]
   uint64_t* item_empty = item_full + Cfg::kRing;
   const ItemRing<Cfg::kRing> ring{reinterpret_cast<volatile int*>(smem + Cfg::kMisc + 16), item_full,
                                   item_empty};
@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
-      mbar_init(&col_ready[i], 4);  // the four warps of the warpgroup
       mbar_init(&s_full[i], 1);
       mbar_init(&dp_full[i], 1);
       mbar_init(&buf_free[i], 1);
@@ -501,12 +500,11 @@ __global__ void __launch_bounds__(512, 1)
     const int lg = 31 - __clz(g);
     const float sl2 = p.scale_log2;
     const int C = p.chunk, ca = p.cp_rank, cb = 2 * p.cp_size - 1 - p.cp_rank;
-    // statistics of this warpgroup's columns: thread r < 64 stages
-    // -LSE*log2e of column 64w + r, thread r >= 64 Delta of column 64w + r - 64
-    const int qcol = 64 * w + (r & 63);
-    const float* stat_src = (r < 64) ? lse : p.delta;
-    const float stat_mul = (r < 64) ? -kLog2e : 1.f;
-    float* col = sCOL + w * 256;  // [2 stages][128] floats per warpgroup
+    // statistics of this warpgroup's 64 columns, staged by each warp for
+    // itself, so that no warp waits for another: lane l holds -LSE*log2e
+    // and Delta of columns 64w + l and 64w + 32 + l
+    const int qcol = 64 * w + lane;
+    float* col = sCOL + (warp - 4) * 256;  // [2 stages][64 -LSE*log2e, 64 Delta]
     // this warpgroup's 64 columns of TMEM tile buffer 0; buffer 1 is 128 further
     const uint32_t buf_cols = tmem + lane_base + Cfg::kTmemBuf + 64 * w;
     bool ok = true;
@@ -520,16 +518,17 @@ __global__ void __launch_bounds__(512, 1)
       const int key = it.kt * kTileN + r;  // position within the sample
       // queries that may attend this key: positions [key, doc_end)
       const int doc_end = p.doc_hi[static_cast<long long>(it.b) * p.seq_len + key];
-      const long long stat_base =
-          (static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (qcol & (g - 1))) * Lq +
-          (qcol >> lg);
+      // (B Hq Lq < 2^31: the plan rejects larger shapes)
+      const int stat_base = (it.b * p.n_heads + it.kvh * g + (qcol & (g - 1))) * Lq + (qcol >> lg);
+      const int s32 = 32 >> lg;  // column + 32: 32 / g positions further
       // list entries of this tile (e) and the next two (e1, e2): they run two
       // tiles ahead and the statistics one tile ahead, so that no load waits
       // on the one before it
       uint32_t e = static_cast<uint32_t>(it.list[0]);
       uint32_t e1 = it.n > 1 ? static_cast<uint32_t>(it.list[1]) : 0u;
       uint32_t e2 = it.n > 2 ? static_cast<uint32_t>(it.list[2]) : 0u;
-      float nxt = stat_src[stat_base + static_cast<int>(e & kIndexMask) * P];
+      int so = stat_base + static_cast<int>(e & kIndexMask) * P;
+      float nl0 = lse[so], nl1 = lse[so + s32], nd0 = p.delta[so], nd1 = p.delta[so + s32];
       for (int i = 0; i < it.n; ++i) {
         const int ig = tbase + i;
         if (i > 0) {
@@ -539,12 +538,19 @@ __global__ void __launch_bounds__(512, 1)
         }
         {
           // stage this tile's statistics, fetch the next tile's
-          const float cur = nxt;
-          if (i + 1 < it.n) nxt = stat_src[stat_base + static_cast<int>(e1 & kIndexMask) * P];
-          col[(ig & 1) * 128 + r] = cur * stat_mul;
+          float* cs = col + (ig & 1) * 128;
+          cs[lane] = nl0 * -kLog2e;
+          cs[lane + 32] = nl1 * -kLog2e;
+          cs[lane + 64] = nd0;
+          cs[lane + 96] = nd1;
+          if (i + 1 < it.n) {
+            so = stat_base + static_cast<int>(e1 & kIndexMask) * P;
+            nl0 = lse[so];
+            nl1 = lse[so + s32];
+            nd0 = p.delta[so];
+            nd1 = p.delta[so + s32];
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&col_ready[w]);
-          if (!warp_wait(&col_ready[w], ig & 1, ctl)) { ok = false; break; }
         }
         // allowed query positions of this key in the tile: [key, doc_end);
         // in tile columns: [lo_c, hi_c)

@@ -590,34 +590,37 @@ __global__ void __launch_bounds__(512, 1)
       const float l_tot = xsum[((ibase & 1) * 2) * 128 + r] + xsum[((ibase & 1) * 2 + 1) * 128 + r];
       const float m_ref = xm[(ibase & 1) * 128 + r];
       const float inv = 1.f / l_tot;
-      uint32_t u[D];
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32)
-        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemO + c0, u + c0);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) reg_fence32(u + c0);
-      warp_arrive(o_free);
       // O / l in blocks of 32 columns x this warp's 32 rows, each written
-      // with one TMA store (rows = 32/g positions x the g heads)
+      // with one TMA store (rows = 32/g positions x the g heads); O is read
+      // out of TMEM 64 columns at a time and handed back after the last read
       const int zrow = it.b * Lq + it.l0 + ((32 * wq) >> lg);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        // the previous block's store must have read the staging buffer
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+      for (int h0 = 0; h0 < D; h0 += 64) {
+        uint32_t u[64];
+        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemO + h0, u);
+        tmem_ld32_nowait(tmem + lane_base + Cfg::kTmemO + h0 + 32, u + 32);
+        tmem_wait_ld();
+        reg_fence32(u);
+        reg_fence32(u + 32);
+        if (h0 + 64 >= D) warp_arrive(o_free);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(stage + lane * 128 + ((ch ^ (lane & 7)) << 4),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 1]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 2]) * inv),
-                       __float_as_uint(__uint_as_float(u[c0 + 4 * ch + 3]) * inv));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&to, smem + Cfg::kStage + wq * 4096, c0, it.kvh * g, zrow);
-          bulk_commit();
+        for (int c1 = 0; c1 < 64; c1 += 32) {
+          // the previous block's store must have read the staging buffer
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(stage + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                         __float_as_uint(__uint_as_float(u[c1 + 4 * ch]) * inv),
+                         __float_as_uint(__uint_as_float(u[c1 + 4 * ch + 1]) * inv),
+                         __float_as_uint(__uint_as_float(u[c1 + 4 * ch + 2]) * inv),
+                         __float_as_uint(__uint_as_float(u[c1 + 4 * ch + 3]) * inv));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&to, smem + Cfg::kStage + wq * 4096, h0 + c1, it.kvh * g, zrow);
+            bulk_commit();
+          }
         }
       }
       lse[(static_cast<long long>(it.b) * p.n_heads + it.kvh * g + (r & (g - 1))) * Lq + it.l0 +
