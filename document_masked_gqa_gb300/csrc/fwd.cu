@@ -82,6 +82,15 @@ struct FwdCfg {
   static_assert(kSmemBytes <= 232448, "forward shared-memory layout exceeds 227 KB");
 };
 
+// Register split of the 512 threads launched at 128 registers each: the
+// producer / issuer warpgroup (warps 0-3) and the epilogue warpgroup give
+// registers to the softmax warps (measured: the softmax runs faster with the
+// room).  Each warpgroup sets its share at one call site at the top of its
+// branch, the same count for its four warps.
+constexpr uint32_t kFwdCtlRegs = 88, kFwdSmRegs = 168, kFwdEpiRegs = 88;
+static_assert(4 * kFwdCtlRegs + 8 * kFwdSmRegs + 4 * kFwdEpiRegs <= 16 * 128,
+              "forward register split exceeds the launch's 512 x 128 registers");
+
 // Wait for a phase ignoring the abort flag, bounded by limit_ns (used only to
 // drain this CTA's own copies before it exits after an abort).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -204,166 +213,171 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ producer: the stream
-      // Two cursors walk this CTA's key tiles in order: the K cursor (which
-      // also loads an item's Q when it enters the item) runs one tile ahead
-      // of the V cursor, so that the S products never wait for a V slot to
-      // free.  Tile t's K goes to K slot t % NS once S_{t-NS} is done, its V
-      // to V slot t % NS once P_{t-NS} V_{t-NS} is done.
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      struct Cursor {
-        int r;     // ring entries read (the K cursor: published)
-        int j;     // tile within the current item
-        int t;     // global tile index
-        int item;  // non-empty items entered so far - 1
-        FwdItem it;
-        bool done;
-      };
-      // move a cursor to the first tile of the next non-empty item: the K
-      // cursor takes the next index from the counter (one item ahead, so
-      // that the atomic's latency is hidden) and publishes it unless its
-      // list is empty; the V cursor reads what the K cursor published
-      int next_idx = take_item(ctr);
-      auto next_item = [&](Cursor& c, bool is_k) -> bool {
-        for (;;) {
-          int item;
-          if (is_k) {
-            item = next_idx < n_items ? next_idx : -1;
-            if (item >= 0) {
-              next_idx = take_item(ctr);
-              if (fwd_item(p, item).n == 0) continue;
+  if (warp < 4) {
+    // warpgroup 0: producer (warp 0), issuers (warps 1, 3); warp 2 has no role
+    reg_dealloc<kFwdCtlRegs>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------ producer: the stream
+        // Two cursors walk this CTA's key tiles in order: the K cursor (which
+        // also loads an item's Q when it enters the item) runs one tile ahead
+        // of the V cursor, so that the S products never wait for a V slot to
+        // free.  Tile t's K goes to K slot t % NS once S_{t-NS} is done, its V
+        // to V slot t % NS once P_{t-NS} V_{t-NS} is done.
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        struct Cursor {
+          int r;     // ring entries read (the K cursor: published)
+          int j;     // tile within the current item
+          int t;     // global tile index
+          int item;  // non-empty items entered so far - 1
+          FwdItem it;
+          bool done;
+        };
+        // move a cursor to the first tile of the next non-empty item: the K
+        // cursor takes the next index from the counter (one item ahead, so
+        // that the atomic's latency is hidden) and publishes it unless its
+        // list is empty; the V cursor reads what the K cursor published
+        int next_idx = take_item(ctr);
+        auto next_item = [&](Cursor& c, bool is_k) -> bool {
+          for (;;) {
+            int item;
+            if (is_k) {
+              item = next_idx < n_items ? next_idx : -1;
+              if (item >= 0) {
+                next_idx = take_item(ctr);
+                if (fwd_item(p, item).n == 0) continue;
+              }
+              if (!ring.put(c.r++, item, ctl)) return false;
+            } else if (!ring.get(c.r++, item, ctl)) {
+              return false;
             }
-            if (!ring.put(c.r++, item, ctl)) return false;
-          } else if (!ring.get(c.r++, item, ctl)) {
-            return false;
-          }
-          if (item < 0) {
-            c.done = true;
+            if (item < 0) {
+              c.done = true;
+              return true;
+            }
+            c.it = fwd_item(p, item);
+            c.j = 0;
+            ++c.item;
             return true;
           }
-          c.it = fwd_item(p, item);
-          c.j = 0;
-          ++c.item;
-          return true;
-        }
-      };
-      Cursor kc{0, 0, 0, -1, FwdItem{}, false}, vc = kc;
-      bool ok = next_item(kc, true) && next_item(vc, false);
-      int q_issued = 0;  // Q loads issued (item index of the next one)
-      while (ok && !vc.done) {
-        const bool do_k = !kc.done && kc.t <= vc.t + 1;
-        Cursor& c = do_k ? kc : vc;
-        if (do_k && c.j == 0 && q_issued == c.item) {
-          // entering an item: its Q into buffer item % 2 once the S products
-          // of the item two back are done
-          const int qb = c.item & 1;
-          if (!mbar_wait(&q_empty[qb], ((c.item >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&q_full[qb], Cfg::kTileBytes);
+        };
+        Cursor kc{0, 0, 0, -1, FwdItem{}, false}, vc = kc;
+        bool ok = next_item(kc, true) && next_item(vc, false);
+        int q_issued = 0;  // Q loads issued (item index of the next one)
+        while (ok && !vc.done) {
+          const bool do_k = !kc.done && kc.t <= vc.t + 1;
+          Cursor& c = do_k ? kc : vc;
+          if (do_k && c.j == 0 && q_issued == c.item) {
+            // entering an item: its Q into buffer item % 2 once the S products
+            // of the item two back are done
+            const int qb = c.item & 1;
+            if (!mbar_wait(&q_empty[qb], ((c.item >> 1) & 1) ^ 1u, ctl)) { ok = false; break; }
+            mbar_arrive_expect_tx(&q_full[qb], Cfg::kTileBytes);
+#pragma unroll
+            for (int ch = 0; ch < Cfg::kChunks; ++ch)
+              tma_load_3d(sQ + qb * Cfg::kTileBytes + ch * Cfg::kRegion, &tq, &q_full[qb], ch * 64,
+                          c.it.kvh * g, c.it.b * Lq + c.it.l0);
+            ++q_issued;
+          }
+          const int kt = static_cast<int>(static_cast<uint32_t>(c.it.list[c.j]) & kIndexMask);
+          const int krow = c.it.b * p.seq_len + kt * kTileN;
+          const int sl = c.t % NS;
+          const uint32_t ph = ((c.t / NS) & 1) ^ 1u;
+          uint64_t* full = do_k ? &k_full[sl] : &v_full[sl];
+          if (!mbar_wait(do_k ? &k_empty[sl] : &v_empty[sl], ph, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+          uint8_t* dst = do_k ? k_slot(c.t) : v_slot(c.t);
 #pragma unroll
           for (int ch = 0; ch < Cfg::kChunks; ++ch)
-            tma_load_3d(sQ + qb * Cfg::kTileBytes + ch * Cfg::kRegion, &tq, &q_full[qb], ch * 64,
-                        c.it.kvh * g, c.it.b * Lq + c.it.l0);
-          ++q_issued;
+            tma_load_2d(dst + ch * Cfg::kRegion, do_k ? &tk : &tv, full, c.it.kvh * D + ch * 64, krow);
+          ++c.t;
+          if (++c.j == c.it.n && !next_item(c, do_k)) ok = false;
         }
-        const int kt = static_cast<int>(static_cast<uint32_t>(c.it.list[c.j]) & kIndexMask);
-        const int krow = c.it.b * p.seq_len + kt * kTileN;
-        const int sl = c.t % NS;
-        const uint32_t ph = ((c.t / NS) & 1) ^ 1u;
-        uint64_t* full = do_k ? &k_full[sl] : &v_full[sl];
-        if (!mbar_wait(do_k ? &k_empty[sl] : &v_empty[sl], ph, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(full, Cfg::kTileBytes);
-        uint8_t* dst = do_k ? k_slot(c.t) : v_slot(c.t);
-#pragma unroll
-        for (int ch = 0; ch < Cfg::kChunks; ++ch)
-          tma_load_2d(dst + ch * Cfg::kRegion, do_k ? &tk : &tv, full, c.it.kvh * D + ch * 64, krow);
-        ++c.t;
-        if (++c.j == c.it.n && !next_item(c, do_k)) ok = false;
+        if (!ok) {  // drain this CTA's copies still in flight
+          for (int t = max(0, kc.t - NS); t < kc.t; ++t)
+            drain_wait(&k_full[t % NS], (t / NS) & 1, 100000000ull);
+          for (int t = max(0, vc.t - NS); t < vc.t; ++t)
+            drain_wait(&v_full[t % NS], (t / NS) & 1, 100000000ull);
+          for (int i = max(0, q_issued - 2); i < q_issued; ++i)
+            drain_wait(&q_full[i & 1], (i >> 1) & 1, 100000000ull);
+        }
       }
-      if (!ok) {  // drain this CTA's copies still in flight
-        for (int t = max(0, kc.t - NS); t < kc.t; ++t)
-          drain_wait(&k_full[t % NS], (t / NS) & 1, 100000000ull);
-        for (int t = max(0, vc.t - NS); t < vc.t; ++t)
-          drain_wait(&v_full[t % NS], (t / NS) & 1, 100000000ull);
-        for (int i = max(0, q_issued - 2); i < q_issued; ++i)
-          drain_wait(&q_full[i & 1], (i >> 1) & 1, 100000000ull);
-      }
-    }
-  } else if (warp == 1 || warp == 3) {
-    if (lane == 0) {
-      // ------------------------------------------------------ MMA issuers
-      // warp 1: S_t = Q K_t^T into TMEM buffer t % 3 (Q and K from shared
-      // memory); the buffer is reused for S_{t+3} once P_t V_t (which reads
-      // P_t from it) has completed.  warp 3: once the softmax has written P_t
-      // over S_t: O += P_t V_t with A = P_t from TMEM.  Two issuing threads
-      // keep the tensor pipe fed while the softmax warps keep the schedulers
-      // busy.
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
-      uint64_t* last_commit = nullptr;
-      uint32_t last_parity = 0;
-      bool ok = true;
-      int tbase = 0, ibase = 0;
-      for (int rk = 0; ok; ++rk) {
-        int item;
-        if (!ring.get(rk, item, ctl)) { ok = false; break; }
-        if (item < 0) break;
-        const FwdItem it = fwd_item(p, item);
-        if (it.n == 0) continue;
-        const int qb = ibase & 1;
-        if (warp == 1 && !mbar_wait(&q_full[qb], (ibase >> 1) & 1, ctl)) { ok = false; break; }
-        const uint32_t q_addr = smem_u32(sQ + qb * Cfg::kTileBytes);
-        for (int j = 0; j < it.n; ++j) {
-          const int t = tbase + j, sb = t % 3;
-          const uint32_t use = (t / 3) & 1;  // parity of this use of buffer sb
-          const uint32_t kv_ph = (t / NS) & 1;
-          if (warp == 1) {
-            if (!mbar_wait(&k_full[t % NS], kv_ph, ctl)) { ok = false; break; }
-            if (t >= 3 && !mbar_wait(&o_done[sb], use ^ 1u, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(k_slot(t));
-            const uint32_t d_s = tmem + 128 * sb;
+    } else if (warp == 1 || warp == 3) {
+      if (lane == 0) {
+        // ------------------------------------------------------ MMA issuers
+        // warp 1: S_t = Q K_t^T into TMEM buffer t % 3 (Q and K from shared
+        // memory); the buffer is reused for S_{t+3} once P_t V_t (which reads
+        // P_t from it) has completed.  warp 3: once the softmax has written P_t
+        // over S_t: O += P_t V_t with A = P_t from TMEM.  Two issuing threads
+        // keep the tensor pipe fed while the softmax warps keep the schedulers
+        // busy.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
+        uint64_t* last_commit = nullptr;
+        uint32_t last_parity = 0;
+        bool ok = true;
+        int tbase = 0, ibase = 0;
+        for (int rk = 0; ok; ++rk) {
+          int item;
+          if (!ring.get(rk, item, ctl)) { ok = false; break; }
+          if (item < 0) break;
+          const FwdItem it = fwd_item(p, item);
+          if (it.n == 0) continue;
+          const int qb = ibase & 1;
+          if (warp == 1 && !mbar_wait(&q_full[qb], (ibase >> 1) & 1, ctl)) { ok = false; break; }
+          const uint32_t q_addr = smem_u32(sQ + qb * Cfg::kTileBytes);
+          for (int j = 0; j < it.n; ++j) {
+            const int t = tbase + j, sb = t % 3;
+            const uint32_t use = (t / 3) & 1;  // parity of this use of buffer sb
+            const uint32_t kv_ph = (t / NS) & 1;
+            if (warp == 1) {
+              if (!mbar_wait(&k_full[t % NS], kv_ph, ctl)) { ok = false; break; }
+              if (t >= 3 && !mbar_wait(&o_done[sb], use ^ 1u, ctl)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t k_addr = smem_u32(k_slot(t));
+              const uint32_t d_s = tmem + 128 * sb;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-              mma_bf16_ss(d_s, sdesc_sw128(q_addr + off, 16, 1024),
-                          sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+                mma_bf16_ss(d_s, sdesc_sw128(q_addr + off, 16, 1024),
+                            sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&s_full[sb]);
+              mma_commit(&k_empty[t % NS]);
+              last_commit = &s_full[sb];
+              last_parity = use;
+            } else {
+              // the item's first P V overwrites O: the previous item's O must
+              // have been read out by the epilogue warps
+              if (j == 0 && ibase > 0 && !mbar_wait(o_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+              if (!mbar_wait(&p_full[sb], use, ctl)) { ok = false; break; }
+              if (!mbar_wait(&v_full[t % NS], kv_ph, ctl)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t v_addr = smem_u32(v_slot(t));
+              const uint32_t pb = tmem + 128 * sb;
+#pragma unroll
+              for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
+                mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
+                           sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(&o_done[sb]);
+              mma_commit(&v_empty[t % NS]);
+              last_commit = &o_done[sb];
+              last_parity = use;
             }
-            mma_commit(&s_full[sb]);
-            mma_commit(&k_empty[t % NS]);
-            last_commit = &s_full[sb];
-            last_parity = use;
-          } else {
-            // the item's first P V overwrites O: the previous item's O must
-            // have been read out by the epilogue warps
-            if (j == 0 && ibase > 0 && !mbar_wait(o_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(&p_full[sb], use, ctl)) { ok = false; break; }
-            if (!mbar_wait(&v_full[t % NS], kv_ph, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t v_addr = smem_u32(v_slot(t));
-            const uint32_t pb = tmem + 128 * sb;
-#pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 64w.. sits at columns 64w..
-              mma_f16_ts(tmem + Cfg::kTmemO, pb + 8 * kk + (kk >= 4 ? 32 : 0),
-                         sdesc_sw128(v_addr + kk * 2048, Cfg::kRegion, 1024), idesc_o,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&o_done[sb]);
-            mma_commit(&v_empty[t % NS]);
-            last_commit = &o_done[sb];
-            last_parity = use;
           }
+          if (!ok) break;
+          if (warp == 1) mma_commit(&q_empty[qb]);  // the item's Q reads are done once these complete
+          tbase += it.n;
+          ++ibase;
         }
-        if (!ok) break;
-        if (warp == 1) mma_commit(&q_empty[qb]);  // the item's Q reads are done once these complete
-        tbase += it.n;
-        ++ibase;
+        if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
       }
-      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp < 12) {
+    reg_alloc<kFwdSmRegs>();
     // ---------------------------------------------------------------- softmax
     // two warpgroups; thread (r, w) owns row r and key columns [64w, 64w+64)
     // of every tile.  Per tile the two post their partial row maxima and
@@ -510,7 +524,9 @@ __global__ void __launch_bounds__(512, 1)
       tbase += it.n;
       ++ibase;
     }
-  } else if (warp >= 12) {
+    tmem_wait_ld();  // (after an abort a score load may still be in flight)
+  } else {
+    reg_dealloc<kFwdEpiRegs>();
     // --------------------------------------------------------------- epilogue
     // per item: once its last P V is done and the softmax warps have posted
     // the row statistics, read O out of TMEM (row r = lane of warp w - 12),

@@ -434,6 +434,20 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Register split between warp roles: the warps of a role give registers
+// back (reg_dealloc) or ask for more (reg_alloc).  The four warps of a
+// warpgroup must make the same call with the same count, and the sum over
+// the CTA's warps must stay within what the launch allocated (threads x
+// registers per thread); otherwise an increase can wait forever.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------- work items of a persistent kernel
 // The persistent kernels take their work items in list order (longest list
 // first) from a global counter, one item at a time: the CTA's producer thread
