@@ -35,6 +35,13 @@ namespace dma {
 namespace {
 
 constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block on sm_103
+// dK/dV register split of the 512 threads launched at 128 registers each: the
+// producer-issuer warpgroup (warps 0-3) and the epilogue warpgroup give
+// registers to the element-wise warps.  Each warpgroup sets its share at one
+// call site at the top of its branch, the same count for its four warps.
+constexpr uint32_t kDkdvCtlRegs = 64, kDkdvEwRegs = 184, kDkdvEpiRegs = 80;
+static_assert(4 * kDkdvCtlRegs + 8 * kDkdvEwRegs + 4 * kDkdvEpiRegs <= 16 * 128,
+              "dK/dV register split exceeds the launch's 512 x 128 registers");
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -308,189 +315,194 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // --------------------------------------- producer: K, V, then Q, dO
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tdo);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      int last_t = -1, ibase = 0, tbase = 0;
-      bool kv_pending = false, ok = true;
-      // the next index is taken one item ahead, so that the atomic's latency
-      // is hidden; every index is published, empty items too (the epilogue
-      // writes their zero rows)
-      int next_idx = take_item(ctr);
-      for (int rk = 0; ok; ++rk) {
-        const int item = next_idx < n_items ? next_idx : -1;
-        if (item >= 0) next_idx = take_item(ctr);
-        if (!ring.put(rk, item, ctl)) { ok = false; break; }
-        if (item < 0) break;
-        const DkdvItem it = dkdv_item(p, item);
-        if (it.n == 0) continue;
-        const int krow0 = it.b * p.seq_len + it.kt * kTileN;
-        kv_pending = false;
-        // K and V of the previous item are read until its last S^T / dP^T
-        if (ibase > 0 && !mbar_wait(kv_empty, (ibase - 1) & 1, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
+  if (warp < 4) {
+    // warpgroup 0: producer (warp 0), issuers (warps 1-3)
+    reg_dealloc<kDkdvCtlRegs>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // --------------------------------------- producer: K, V, then Q, dO
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        int last_t = -1, ibase = 0, tbase = 0;
+        bool kv_pending = false, ok = true;
+        // the next index is taken one item ahead, so that the atomic's latency
+        // is hidden; every index is published, empty items too (the epilogue
+        // writes their zero rows)
+        int next_idx = take_item(ctr);
+        for (int rk = 0; ok; ++rk) {
+          const int item = next_idx < n_items ? next_idx : -1;
+          if (item >= 0) next_idx = take_item(ctr);
+          if (!ring.put(rk, item, ctl)) { ok = false; break; }
+          if (item < 0) break;
+          const DkdvItem it = dkdv_item(p, item);
+          if (it.n == 0) continue;
+          const int krow0 = it.b * p.seq_len + it.kt * kTileN;
+          kv_pending = false;
+          // K and V of the previous item are read until its last S^T / dP^T
+          if (ibase > 0 && !mbar_wait(kv_empty, (ibase - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
 #pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c) {
-          tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, it.kvh * D + c * 64, krow0);
-          tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, it.kvh * D + c * 64, krow0);
-        }
-        kv_pending = true;
-        for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, st = ig & 1;
-          const uint32_t ph = (ig >> 1) & 1;
-          const int qt = static_cast<int>(static_cast<uint32_t>(it.list[i]) & kIndexMask);
-          if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
-#pragma unroll
-          for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64,
-                        it.kvh * g, it.b * Lq + qt * P);
-          if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
-#pragma unroll
-          for (int c = 0; c < Cfg::kChunks; ++c)
-            tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
-                        it.kvh * g, it.b * Lq + qt * P);
-          last_t = ig;
-        }
-        tbase += it.n;
-        ++ibase;
-      }
-      if (!ok) {  // drain this CTA's copies still in flight
-        if (kv_pending) drain_wait(kv_full, ibase & 1, 100000000ull);
-        for (int ii = max(0, last_t - 1); ii <= last_t; ++ii) {
-          drain_wait(&q_full[ii & 1], (ii >> 1) & 1, 100000000ull);
-          drain_wait(&do_full[ii & 1], (ii >> 1) & 1, 100000000ull);
-        }
-      }
-    }
-  } else if (warp == 1 || warp == 2) {
-    if (lane == 0) {
-      // --------------------------------------- MMA issuers: S^T and dP^T
-      // warp 1: S^T(t) = K Q^T into buffer t % 2 once dV(t-2) and dK(t-2),
-      // which read P^T and dS^T there, are done.  warp 2: dP^T(t) = V dO^T
-      // into the same buffer once the element-wise warps hold S^T(t) in
-      // registers.
-      const bool is_s = warp == 1;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t a_addr = smem_u32(is_s ? sK : sV);
-      uint8_t* const b_tiles = is_s ? sQ : sDO;
-      uint64_t* const b_full = is_s ? q_full : do_full;
-      uint64_t* const done_bar = is_s ? s_full : dp_full;
-      uint64_t* last_commit = nullptr;
-      uint32_t last_parity = 0;
-      bool ok = true;
-      int tbase = 0, ibase = 0;
-      for (int rk = 0; ok; ++rk) {
-        int item;
-        if (!ring.get(rk, item, ctl)) { ok = false; break; }
-        if (item < 0) break;
-        const DkdvItem it = dkdv_item(p, item);
-        if (it.n == 0) continue;
-        if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
-        for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, x = ig & 1;
-          const uint32_t use = (ig >> 1) & 1;  // parity of this use of buffer x
-          if (is_s) {
-            if (ig >= 2 && !mbar_wait(&buf_free[x], use ^ 1u, ctl)) { ok = false; break; }
-          } else {
-            if (!mbar_wait(&s_read[x], use, ctl)) { ok = false; break; }
+          for (int c = 0; c < Cfg::kChunks; ++c) {
+            tma_load_2d(sK + c * Cfg::kRegion, &tk, kv_full, it.kvh * D + c * 64, krow0);
+            tma_load_2d(sV + c * Cfg::kRegion, &tv, kv_full, it.kvh * D + c * 64, krow0);
           }
-          if (!mbar_wait(&b_full[x], use, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t b_addr = smem_u32(b_tiles + x * Cfg::kTile);
-          const uint32_t d_tmem = tmem + Cfg::kTmemBuf + 128 * x;
+          kv_pending = true;
+          for (int i = 0; i < it.n; ++i) {
+            const int ig = tbase + i, st = ig & 1;
+            const uint32_t ph = (ig >> 1) & 1;
+            const int qt = static_cast<int>(static_cast<uint32_t>(it.list[i]) & kIndexMask);
+            if (!mbar_wait(&q_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+            mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + off, 16, 1024),
-                        sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            for (int c = 0; c < Cfg::kChunks; ++c)
+              tma_load_3d(sQ + st * Cfg::kTile + c * Cfg::kRegion, &tq, &q_full[st], c * 64,
+                          it.kvh * g, it.b * Lq + qt * P);
+            if (!mbar_wait(&do_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+            mbar_arrive_expect_tx(&do_full[st], Cfg::kTile);
+#pragma unroll
+            for (int c = 0; c < Cfg::kChunks; ++c)
+              tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
+                          it.kvh * g, it.b * Lq + qt * P);
+            last_t = ig;
           }
-          mma_commit(&done_bar[x]);
-          last_commit = &done_bar[x];
-          last_parity = use;
+          tbase += it.n;
+          ++ibase;
         }
-        if (!ok) break;
-        mma_commit(kv_empty);  // this item's K (V) reads are done once these complete
-        tbase += it.n;
-        ++ibase;
+        if (!ok) {  // drain this CTA's copies still in flight
+          if (kv_pending) drain_wait(kv_full, ibase & 1, 100000000ull);
+          for (int ii = max(0, last_t - 1); ii <= last_t; ++ii) {
+            drain_wait(&q_full[ii & 1], (ii >> 1) & 1, 100000000ull);
+            drain_wait(&do_full[ii & 1], (ii >> 1) & 1, 100000000ull);
+          }
+        }
       }
-      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
-    }
-  } else if (warp == 3) {
-    if (lane == 0) {
-      // ------------------------------------------- MMA issuer: dV, then dK
-      // once P^T is in the tile's buffer: dV += P^T dO; then dK += dS^T Q,
-      // each half of dS^T as soon as it is written (A operands from TMEM:
-      // warpgroup w's query columns [64w, 64w + 64) sit in 32 columns of the
-      // buffer, 8 per 16-deep step).  The commit after dK covers dV too.
-      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      uint64_t* last_commit = nullptr;
-      uint32_t last_parity = 0;
-      bool ok = true;
-      int tbase = 0, ibase = 0;
-      for (int rk = 0; ok; ++rk) {
-        int item;
-        if (!ring.get(rk, item, ctl)) { ok = false; break; }
-        if (item < 0) break;
-        const DkdvItem it = dkdv_item(p, item);
-        if (it.n == 0) continue;
-        for (int i = 0; i < it.n; ++i) {
-          const int ig = tbase + i, x = ig & 1;
-          const uint32_t use = (ig >> 1) & 1;
-          const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * x;
-          // the item's first products overwrite dV, dK: the previous item's
-          // must have been read out by the epilogue warps
-          if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&do_full[x], use, ctl)) { ok = false; break; }
-          if (!mbar_wait(&q_full[x], use, ctl)) { ok = false; break; }
-          if (!mbar_wait(&p_full[x], use, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t do_addr = smem_u32(sDO + x * Cfg::kTile);
-          const uint32_t q_addr = smem_u32(sQ + x * Cfg::kTile);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tmem + Cfg::kTmemDV, buf + 64 * (kk >> 2) + 8 * (kk & 3),
-                       sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
-                       (i > 0 || kk > 0) ? 1u : 0u);
-          // each half of dS^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(&ds_full[2 * x + h], use, ctl)) { ok = false; break; }
+    } else if (warp == 1 || warp == 2) {
+      if (lane == 0) {
+        // --------------------------------------- MMA issuers: S^T and dP^T
+        // warp 1: S^T(t) = K Q^T into buffer t % 2 once dV(t-2) and dK(t-2),
+        // which read P^T and dS^T there, are done.  warp 2: dP^T(t) = V dO^T
+        // into the same buffer once the element-wise warps hold S^T(t) in
+        // registers.
+        const bool is_s = warp == 1;
+        constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+        const uint32_t a_addr = smem_u32(is_s ? sK : sV);
+        uint8_t* const b_tiles = is_s ? sQ : sDO;
+        uint64_t* const b_full = is_s ? q_full : do_full;
+        uint64_t* const done_bar = is_s ? s_full : dp_full;
+        uint64_t* last_commit = nullptr;
+        uint32_t last_parity = 0;
+        bool ok = true;
+        int tbase = 0, ibase = 0;
+        for (int rk = 0; ok; ++rk) {
+          int item;
+          if (!ring.get(rk, item, ctl)) { ok = false; break; }
+          if (item < 0) break;
+          const DkdvItem it = dkdv_item(p, item);
+          if (it.n == 0) continue;
+          if (!mbar_wait(kv_full, ibase & 1, ctl)) { ok = false; break; }
+          for (int i = 0; i < it.n; ++i) {
+            const int ig = tbase + i, x = ig & 1;
+            const uint32_t use = (ig >> 1) & 1;  // parity of this use of buffer x
+            if (is_s) {
+              if (ig >= 2 && !mbar_wait(&buf_free[x], use ^ 1u, ctl)) { ok = false; break; }
+            } else {
+              if (!mbar_wait(&s_read[x], use, ctl)) { ok = false; break; }
+            }
+            if (!mbar_wait(&b_full[x], use, ctl)) { ok = false; break; }
             tc_fence_after();
+            const uint32_t b_addr = smem_u32(b_tiles + x * Cfg::kTile);
+            const uint32_t d_tmem = tmem + Cfg::kTmemBuf + 128 * x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
-              mma_f16_ts(tmem + Cfg::kTmemDK, buf + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
-                         sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+              mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + off, 16, 1024),
+                          sdesc_sw128(b_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&done_bar[x]);
+            last_commit = &done_bar[x];
+            last_parity = use;
+          }
+          if (!ok) break;
+          mma_commit(kv_empty);  // this item's K (V) reads are done once these complete
+          tbase += it.n;
+          ++ibase;
+        }
+        if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
+      }
+    } else if (warp == 3) {
+      if (lane == 0) {
+        // ------------------------------------------- MMA issuer: dV, then dK
+        // once P^T is in the tile's buffer: dV += P^T dO; then dK += dS^T Q,
+        // each half of dS^T as soon as it is written (A operands from TMEM:
+        // warpgroup w's query columns [64w, 64w + 64) sit in 32 columns of the
+        // buffer, 8 per 16-deep step).  The commit after dK covers dV too.
+        constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
+        uint64_t* last_commit = nullptr;
+        uint32_t last_parity = 0;
+        bool ok = true;
+        int tbase = 0, ibase = 0;
+        for (int rk = 0; ok; ++rk) {
+          int item;
+          if (!ring.get(rk, item, ctl)) { ok = false; break; }
+          if (item < 0) break;
+          const DkdvItem it = dkdv_item(p, item);
+          if (it.n == 0) continue;
+          for (int i = 0; i < it.n; ++i) {
+            const int ig = tbase + i, x = ig & 1;
+            const uint32_t use = (ig >> 1) & 1;
+            const uint32_t buf = tmem + Cfg::kTmemBuf + 128 * x;
+            // the item's first products overwrite dV, dK: the previous item's
+            // must have been read out by the epilogue warps
+            if (i == 0 && ibase > 0 && !mbar_wait(acc_free, (ibase - 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(&do_full[x], use, ctl)) { ok = false; break; }
+            if (!mbar_wait(&q_full[x], use, ctl)) { ok = false; break; }
+            if (!mbar_wait(&p_full[x], use, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t do_addr = smem_u32(sDO + x * Cfg::kTile);
+            const uint32_t q_addr = smem_u32(sQ + x * Cfg::kTile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(tmem + Cfg::kTmemDV, buf + 64 * (kk >> 2) + 8 * (kk & 3),
+                         sdesc_sw128(do_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
                          (i > 0 || kk > 0) ? 1u : 0u);
+            // each half of dS^T as soon as it is written: steps kk = 4w + 2h + {0, 1}
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (!mbar_wait(&ds_full[2 * x + h], use, ctl)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * (e >> 1) + 2 * h + (e & 1);
+                mma_f16_ts(tmem + Cfg::kTmemDK, buf + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
+                           sdesc_sw128(q_addr + kk * 2048, Cfg::kRegion, 1024), idesc_g,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
+            mma_commit(&buf_free[x]);
+            // S^T and dP^T of this tile completed before P^T / dS^T existed:
+            // its Q and dO are free once dV and dK are
+            mma_commit(&do_empty[x]);
+            mma_commit(&q_empty[x]);
+            last_commit = &buf_free[x];
+            last_parity = use;
+            if (i == it.n - 1) {
+              mma_commit(acc_done);
+              last_commit = acc_done;
+              last_parity = ibase & 1;
             }
           }
           if (!ok) break;
-          mma_commit(&buf_free[x]);
-          // S^T and dP^T of this tile completed before P^T / dS^T existed:
-          // its Q and dO are free once dV and dK are
-          mma_commit(&do_empty[x]);
-          mma_commit(&q_empty[x]);
-          last_commit = &buf_free[x];
-          last_parity = use;
-          if (i == it.n - 1) {
-            mma_commit(acc_done);
-            last_commit = acc_done;
-            last_parity = ibase & 1;
-          }
+          tbase += it.n;
+          ++ibase;
         }
-        if (!ok) break;
-        tbase += it.n;
-        ++ibase;
+        if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
       }
-      if (!ok && last_commit) drain_wait(last_commit, last_parity, 100000000ull);
     }
   } else if (warp < 12) {
+    reg_alloc<kDkdvEwRegs>();
     // ----------------------------------------------------------- key rows
     // thread r of warpgroup w owns key r and query columns [64w, 64w + 64)
     // of every query tile
@@ -620,6 +632,7 @@ __global__ void __launch_bounds__(512, 1)
       tbase += it.n;
     }
   } else {
+    reg_dealloc<kDkdvEpiRegs>();
     // --------------------------------------------------------------- epilogue
     // warp w - 12 owns key rows 32 (w - 12) .. + 31 of each item: once its dV
     // and dK are complete it reads them out of TMEM 32 columns at a time,
