@@ -114,8 +114,11 @@ __global__ void mask_classify_kernel(PlanDev p) {
   uint8_t* cls_row = p.tile_class + (static_cast<long long>(b) * p.n_qtiles + t) * p.n_ktiles;
   for (int kt = threadIdx.x; kt < p.n_ktiles; kt += blockDim.x) {
     const int k0 = kt * kTileN, k1 = k0 + kTileN - 1;
-    bool any = false;
-    for (int r = 0; r < P && !any; ++r) any = (s_lo[r] <= k1) && (s_q[r] >= k0);
+    // the tile's positions are consecutive (q_min + r) and their document
+    // starts non-decreasing: the rows at or after key k0 start at r0, and the
+    // smallest document start among them is row r0's
+    const int r0 = k0 - q_min < 0 ? 0 : k0 - q_min;
+    const bool any = r0 < P && s_lo[r0] <= k1;
     uint8_t c = DMA_TILE_SKIP;
     if (any) c = (lo_max <= k0 && k1 <= q_min) ? DMA_TILE_FULL : DMA_TILE_PARTIAL;
     cls_row[kt] = c;
@@ -129,7 +132,7 @@ __global__ void mask_classify_kernel(PlanDev p) {
   if (threadIdx.x == 0) p.row_cnt[b * p.n_qtiles + t] = s_cnt;
 }
 
-// Block-wide exclusive scan helper (blockDim.x == 1024).
+// Block-wide exclusive scan helper (blockDim.x a multiple of 32, at most 1024).
 __device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int x = v;
@@ -213,7 +216,7 @@ __global__ void scan_order_kernel(PlanDev p) {
   }
 }
 
-// grid (n_qtiles + n_ktiles, batch): row lists, then column lists; block 1024
+// grid (n_qtiles + n_ktiles, batch): row lists, then column lists; block 256
 __global__ void fill_lists_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
   const int columns = blockIdx.x >= p.n_qtiles;
@@ -337,7 +340,7 @@ cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   const int nq = p.batch * p.n_qtiles, nk = p.batch * p.n_ktiles;
   if (nq > kSortMax) order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
   if (nk > kSortMax) order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
-  fill_lists_kernel<<<dim3(p.n_qtiles + p.n_ktiles, p.batch), 1024, 0, s>>>(p);
+  fill_lists_kernel<<<dim3(p.n_qtiles + p.n_ktiles, p.batch), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
