@@ -258,9 +258,10 @@ def fit_costs(features, times_ms) -> np.ndarray:
 
 
 # Constants fitted (fit_costs) to the measured per-rank step times of the
-# 8B, 70B, sparse-stress and both 405B workloads on one GB300 (152 SMs):
-# ms per tile pair of makespan, per partial pair, per work item, fixed.
-COST_MS_GB300 = np.array([1.31844e-03, 0.0, 4.14717e-06, 9.95450e-02])
+# 8B, 70B, sparse-stress and both 405B workloads on one GB300 (152 SMs), with
+# the kernels' dynamic work distribution: ms per tile pair of makespan, per
+# partial pair, per work item, fixed.
+COST_MS_GB300 = np.array([1.26963e-03, 0.0, 1.84296e-06, 1.16930e-01])
 
 
 def predict_ms(features, coef=None) -> np.ndarray:

@@ -327,17 +327,21 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tv);
         int last_t = -1, ibase = 0, tbase = 0;
         bool kv_pending = false, ok = true;
-        // the next index is taken one item ahead, so that the atomic's latency
-        // is hidden; every index is published, empty items too (the epilogue
-        // writes their zero rows)
+        // the next index is taken as an item's last query tile loads: late, so
+        // that no SM holds an item it cannot start for long (a long item would
+        // otherwise pin a second one behind it), yet early enough to hide the
+        // atomic's latency.  Every index is published, empty items too (the
+        // epilogue writes their zero rows).
         int next_idx = take_item(ctr);
         for (int rk = 0; ok; ++rk) {
           const int item = next_idx < n_items ? next_idx : -1;
-          if (item >= 0) next_idx = take_item(ctr);
           if (!ring.put(rk, item, ctl)) { ok = false; break; }
           if (item < 0) break;
           const DkdvItem it = dkdv_item(p, item);
-          if (it.n == 0) continue;
+          if (it.n == 0) {
+            next_idx = take_item(ctr);
+            continue;
+          }
           const int krow0 = it.b * p.seq_len + it.kt * kTileN;
           kv_pending = false;
           // K and V of the previous item are read until its last S^T / dP^T
@@ -366,6 +370,7 @@ __global__ void __launch_bounds__(512, 1)
               tma_load_3d(sDO + st * Cfg::kTile + c * Cfg::kRegion, &tdo, &do_full[st], c * 64,
                           it.kvh * g, it.b * Lq + qt * P);
             last_t = ig;
+            if (i == it.n - 1) next_idx = take_item(ctr);
           }
           tbase += it.n;
           ++ibase;
