@@ -261,7 +261,7 @@ def fit_costs(features, times_ms) -> np.ndarray:
 # 8B, 70B, sparse-stress and both 405B workloads on one GB300 (152 SMs), with
 # the kernels' dynamic work distribution: ms per tile pair of makespan, per
 # partial pair, per work item, fixed.
-COST_MS_GB300 = np.array([1.26963e-03, 0.0, 1.84296e-06, 1.16930e-01])
+COST_MS_GB300 = np.array([1.27084e-03, 0.0, 1.97947e-06, 1.13610e-01])
 
 
 def predict_ms(features, coef=None) -> np.ndarray:
