@@ -81,9 +81,10 @@ struct dma_plan_s {
 namespace dma {
 // Launchers implemented in the .cu files (host side).
 #ifdef __CUDACC__
-// Work item of round k for this CTA of a persistent kernel: rounds alternate
-// direction over the CTAs, so that a longest-first item order spreads its
-// work evenly (CTA c takes c, 2G-1-c, 2G+c, ...).
+// Work item of round k for this CTA of the dQ kernel (a static order; the
+// forward and dK/dV kernels take theirs from the plan's work counters):
+// rounds alternate direction over the CTAs, so that a longest-first item
+// order spreads its work evenly (CTA c takes c, 2G-1-c, 2G+c, ...).
 __device__ __forceinline__ int snake_item(int k) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   return k * G + ((k & 1) ? (G - 1 - c) : c);

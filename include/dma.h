@@ -49,7 +49,11 @@
  *
  * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  Nothing synchronizes except dma_plan_check and
- * dma_debug_wait_probe.
+ * dma_debug_wait_probe.  A plan's workspace also holds scratch the kernels
+ * share (Delta, the fp16 copy of V, the work counters from which the forward
+ * and dK/dV kernels take their work items), so the calls made on one plan
+ * must not overlap on the GPU: issue them on one stream (or order them with
+ * events).  Different plans may run concurrently.
  *
  * Errors: arguments the host can check are rejected before any launch with
  * DMA_ERR_INVALID_ARG / DMA_ERR_UNSUPPORTED / DMA_ERR_WORKSPACE.  Problems only
