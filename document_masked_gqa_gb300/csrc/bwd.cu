@@ -10,18 +10,24 @@
 // fp32 ("The Llama 3 Herd of Models - part 3/16", 3.3.2 "Numerical
 // stability": gradients accumulated and reduce-scattered in FP32).
 //
-// Three launches:
-//   delta_kernel  Delta[b, h, l] = sum_d dO * O (HBM-bound, one pass).
-//   dkdv_kernel   work item = (key tile, K/V head): K and V stay in shared
-//                 memory; the item walks the column list of query tiles (all
-//                 g heads of the group packed in each 128-row tile, so the
-//                 GQA reduction over the group happens inside the
-//                 accumulation), a whole 128-row query tile per step shared
-//                 by two element-wise warpgroups; dV, dK accumulate in TMEM.
+// Kernels (the default backward launches dq_kernel<D, true> and then
+// dkdv_kernel, plus kv_reduce_kernel when the key tiles' lists are split):
 //   dq_kernel     work item = (query tile, K/V head): Q and dO are copied into
 //                 TMEM (tcgen05.cp by the S and dP issuers); the item walks
 //                 the row list of key tiles; S, dP and the dQ accumulator in
 //                 TMEM; four row warpgroups split each tile's key columns.
+//                 With kDelta it also computes Delta at each item's start and
+//                 stores it for the dK/dV pass.
+//   dkdv_kernel   work item = (key tile, K/V head[, list segment]): K and V
+//                 stay in shared memory; the item walks the column list of
+//                 query tiles (all g heads of the group packed in each
+//                 128-row tile, so the GQA reduction over the group happens
+//                 inside the accumulation), a whole 128-row query tile per
+//                 step shared by two element-wise warpgroups; dV, dK
+//                 accumulate in TMEM.
+//   kv_reduce_kernel  the list segments' fp32 partials added in order.
+//   delta_kernel  Delta[b, h, l] = sum_d dO * O as a pass of its own
+//                 (HBM-bound), for the split entry points.
 // Both attention kernels are persistent (one CTA per SM) with one TMA
 // producer thread, one tcgen05-issuing thread per product on its own warp,
 // element-wise warpgroups and an epilogue that overlaps the next item;
