@@ -53,30 +53,17 @@ CPU_BASELINE_TARGET_S = 15.0  # seconds of host work the bounded oracle sample a
 PLAN_SORT_MAX = 2048  # launch orders up to this many units are sorted inside the scan kernel
 
 
-KV_SPLIT_ITEMS, KV_MAX_SEGS = 256, 8  # the library's dK/dV list-splitting rule
-
-
-def kv_segments(w) -> int:
-    """Segments each key tile's query list is cut into by the dK/dV pass:
-    1 when there are at least 256 (key tile, K/V head) items, else enough to
-    reach 256 items, at most 8."""
-    items = w.batch * (w.seq_len // 128) * w.n_kv_heads
-    if items <= 0 or items >= KV_SPLIT_ITEMS:
-        return 1
-    return min(KV_MAX_SEGS, -(-KV_SPLIT_ITEMS // items))
-
-
 def kernels_per_rank_step(w) -> int:
     """Kernels one rank's step launches: the planner's four (positions,
-    block classes, scans + launch orders, lists) plus one per launch order
-    too long for the in-block sort, the forward's two (V to fp16,
-    attention) and the backward's two (dQ with Delta, dK/dV), plus the sum
-    of the dK/dV partials when the key tiles' lists are split."""
+    block classes, scans + launch orders + the dK/dV work list, lists) plus
+    one per launch order too long for the in-block sort (and, for the key
+    tiles, one more that lays out the uncut dK/dV work list), the forward's
+    two (V to fp16, attention) and the backward's two (dQ with Delta, dK/dV;
+    cut dK/dV lists are summed inside the dK/dV kernel)."""
     g = w.n_heads // w.n_kv_heads
     nq = w.batch * ((w.seq_len // w.cp_size) // (128 // g))
     nk = w.batch * (w.seq_len // 128)
-    return (4 + int(nq > PLAN_SORT_MAX) + int(nk > PLAN_SORT_MAX) + 2 + 2
-            + int(kv_segments(w) > 1))
+    return 4 + int(nq > PLAN_SORT_MAX) + 2 * int(nk > PLAN_SORT_MAX) + 2 + 2
 
 
 # ------------------------------------------------------------------ counting

@@ -47,7 +47,8 @@ class PlanView(ctypes.Structure):
         "chunk", "local_len", "group", "q_tile_positions", "n_qtiles", "n_ktiles")] + [
         ("softmax_scale", ctypes.c_float)] + [(n, ctypes.c_void_p) for n in (
             "qpos", "doc_lo", "chunk_order", "tile_class", "row_ptr", "row_idx", "col_ptr",
-            "col_idx", "fwd_order", "bwd_order", "status")]
+            "col_idx", "fwd_order", "bwd_order", "status", "kv_slices", "kv_splits",
+            "counts")] + [(n, ctypes.c_int) for n in ("n_sms", "kv_pool_slots")]
 
 
 def _load():
@@ -391,4 +392,10 @@ def plan_arrays(plan: Plan) -> dict:
     nnz_c = int(out["col_ptr"][-1]) if B else 0
     out["row_idx"] = grab(v.row_idx, nnz_r, torch.int32)
     out["col_idx"] = grab(v.col_idx, nnz_c, torch.int32)
+    counts = grab(v.counts, 2, torch.int32) if B else torch.zeros(2, dtype=torch.int32)
+    n_sl, n_sp = int(counts[0]), int(counts[1])
+    out["kv_slices"] = grab(v.kv_slices, 8 * n_sl, torch.int32).reshape(n_sl, 8)
+    out["kv_splits"] = grab(v.kv_splits, 4 * n_sp, torch.int32).reshape(n_sp, 4)
+    out["n_sms"] = int(v.n_sms)
+    out["kv_pool_slots"] = int(v.kv_pool_slots)
     return out

@@ -172,7 +172,93 @@ def report(cu_doc_lens, batch: int, seq_len: int, cp_size: int, granule: int = 1
 
 
 TILE = 128  # positions per key tile; a query tile holds TILE rows (TILE / g positions)
-KV_SPLIT_ITEMS, KV_MAX_SEGS = 256, 8  # the dK/dV pass splits key tiles below 256 items
+# the dK/dV list cutting rule of the planner: segments of at least SEG_MIN
+# query tiles; cut when the greedy-makespan bound exceeds SPLIT_ON = 23/20
+# times the mean work per SM, to within SPLIT_TARGET = 11/10 of it; at most
+# SORT_MAX units
+SEG_MIN, SORT_MAX = 16, 2048
+SPLIT_ON, SPLIT_TARGET = (23, 20), (11, 10)
+
+
+def kv_pool_slots(batch: int, seq_len: int, n_kv_heads: int, n_qtiles: int) -> int:
+    """Slots of the plan's pool of partial dK, dV: one per (sample, key tile)
+    unit, at least 512 / Hkv where the lists are long enough to be cut."""
+    units = batch * (seq_len // TILE)
+    max_extra = units * (-(-n_qtiles // SEG_MIN) - 1)
+    floor_slots = min(-(-512 // n_kv_heads), max_extra)
+    return max(0, max(units, floor_slots))
+
+
+def kv_work_list(col_counts, n_kv_heads: int, n_sms: int, pool_slots: int) -> dict:
+    """The dK/dV work list the planner lays out from the column-list lengths
+    of the units (sample, key tile), in the same steps and arithmetic.
+
+    Greedy list scheduling runs each item, in order, on the SM that frees
+    first, so an item ends no later than the work before it over the SMs
+    plus its own length.  Units sorted longest list first, heads side by side:
+    unit o ends by E_o = (Hkv pre_o + (Hkv - 1) c_o) / P + c_o against the
+    mean m = Hkv sum(c) / P.  When max E_o > SPLIT_ON m, every list longer
+    than L is cut into k = ceil(c / L) contiguous segments (the first c mod k
+    of them one query tile longer), L = the length at the first position
+    from which every E_o <= SPLIT_TARGET m (at least SEG_MIN),
+    lengthened by an eighth while the segments after the first of each cut
+    list need more than pool_slots slots.  Slices are then ordered by length,
+    longest first, ties by unit.
+
+    Returns {"L": L or None, "slices": [(unit, first, n, seg, split, slot)],
+    "splits": [(unit, slot0, segs)]}; `first` is the offset in the unit's
+    list."""
+    cnt = np.asarray(col_counts, dtype=np.int64)
+    n = len(cnt)
+    order = sorted(range(n), key=lambda i: (-int(cnt[i]), i))
+    L = None
+    if 0 < n <= SORT_MAX:
+        c = cnt[order]
+        P = max(int(n_sms), 1)
+        h = int(n_kv_heads)
+        pre = np.concatenate([[0], np.cumsum(c)[:-1]]).astype(np.int64)
+        total = int(c.sum())
+        pm = h * total                                   # P m
+        pe = h * pre + (h - 1) * c + P * c               # P E_o, exact
+        if total > 0 and SPLIT_ON[1] * int(pe.max()) > SPLIT_ON[0] * pm:
+            over = np.nonzero(SPLIT_TARGET[1] * pe > SPLIT_TARGET[0] * pm)[0]
+            o_star = min(int(over.max()) + 1 if len(over) else 0, n - 1)
+            cand = max(SEG_MIN, int(c[o_star]))
+            fits = False
+            for _ in range(4096):
+                if cand >= int(c[0]):
+                    break
+                need = int(sum(-(-int(x) // cand) - 1 for x in c if x > cand))
+                if need <= pool_slots:
+                    fits = True
+                    break
+                cand += max(1, cand // 8)
+            L = cand if fits else None
+
+    def segs_of(x):
+        return -(-int(x) // L) if (L is not None and x > L) else 1
+
+    def seg_len(u):
+        return -(-int(cnt[u]) // segs_of(cnt[u]))
+
+    if L is not None:
+        order = sorted(order, key=lambda u: (-seg_len(u), u))
+    slices, splits, slot = [], [], 0
+    for u in order:
+        c_u, k = int(cnt[u]), segs_of(cnt[u])
+        if k == 1:
+            slices.append((u, 0, c_u, 0, -1, -1))
+            continue
+        split = len(splits)
+        splits.append((u, slot, k))
+        q, r = divmod(c_u, k)  # the first r segments take one more query tile
+        lo = 0
+        for sg in range(k):
+            n_sg = q + (1 if sg < r else 0)
+            slices.append((u, lo, n_sg, sg, split, slot + sg - 1 if sg > 0 else -1))
+            lo += n_sg
+        slot += k - 1
+    return {"L": L, "slices": slices, "splits": splits}
 
 
 def _doc_starts(cu_doc_lens, batch: int, seq_len: int, pos: np.ndarray) -> np.ndarray:
@@ -209,6 +295,7 @@ def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: in
     q_first = pos[::P][:, None]
     full = partial = 0
     max_row = max_col = 0
+    col_counts = []
     for b in range(batch):
         lo_b = lo[b].reshape(nqt, P)
         r_star = np.clip(k0 - q_first, 0, P)                  # first row with position >= k0
@@ -220,7 +307,9 @@ def tile_counts(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: in
         partial += int((meets & ~covers).sum())
         max_row = max(max_row, int(meets.sum(axis=1).max()))
         max_col = max(max_col, int(meets.sum(axis=0).max()))
-    return {"full": full, "partial": partial, "max_row": max_row, "max_col": max_col}
+        col_counts.append(meets.sum(axis=0))
+    return {"full": full, "partial": partial, "max_row": max_row, "max_col": max_col,
+            "col_counts": np.concatenate(col_counts).astype(np.int64)}
 
 
 def rank_costs(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int,
@@ -230,19 +319,18 @@ def rank_costs(cu_doc_lens, batch: int, seq_len: int, cp_size: int, cp_rank: int
     kernels, the tile pairs the busiest of n_sms persistent CTAs must run at
     least: the kernel's tile pairs (all samples and K/V heads) shared evenly,
     or its longest work item, whichever is more (the forward and dQ walk row
-    lists, dK/dV column lists cut into its list segments).  Items: the
-    forward's and dQ's (query tile, K/V head) pairs and dK/dV's (key tile,
-    K/V head, list segment) triples."""
+    lists, dK/dV the slices of its work list, kv_work_list).  Items: the
+    forward's and dQ's (query tile, K/V head) pairs and dK/dV's (slice, K/V
+    head) pairs."""
     g = n_heads // n_kv_heads
     c = tile_counts(cu_doc_lens, batch, seq_len, cp_size, cp_rank, g)
     nqt = (seq_len // cp_size) // (TILE // g)
-    nkt = seq_len // TILE
-    kv_items = batch * nkt * n_kv_heads
-    segs = 1 if kv_items >= KV_SPLIT_ITEMS else min(KV_MAX_SEGS, -(-KV_SPLIT_ITEMS // kv_items))
-    items = 2 * batch * nqt * n_kv_heads + kv_items * segs
+    work = kv_work_list(c["col_counts"], n_kv_heads, n_sms,
+                        kv_pool_slots(batch, seq_len, n_kv_heads, nqt))
+    longest_slice = max((sl[2] for sl in work["slices"]), default=0)
+    items = 2 * batch * nqt * n_kv_heads + len(work["slices"]) * n_kv_heads
     tiles = (c["full"] + c["partial"]) * n_kv_heads
-    makespan = (2 * max(tiles / n_sms, c["max_row"])
-                + max(tiles / n_sms, -(-c["max_col"] // segs)))
+    makespan = 2 * max(tiles / n_sms, c["max_row"]) + max(tiles / n_sms, longest_slice)
     return np.array([makespan, c["partial"] * n_kv_heads, items, 1.0], dtype=np.float64)
 
 

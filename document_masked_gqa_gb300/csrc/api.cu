@@ -80,10 +80,15 @@ WorkspaceLayout layout_for(int batch, int seq_len, int cp_size, int n_heads, int
   w.bwd_order = take(4 * B * nkt);
   w.delta = take(4 * B * static_cast<size_t>(n_heads) * Lq);
   w.v16 = take(2 * B * static_cast<size_t>(seq_len) * n_kv_heads * head_dim);
-  const int segs = dma::kv_segments(batch, seq_len, n_kv_heads);
-  w.kv_part = take(segs > 1 ? 2 * static_cast<size_t>(segs) * 4 * B * static_cast<size_t>(seq_len) *
-                                  n_kv_heads * head_dim
-                            : 0);
+  const size_t units = B * nkt;
+  const size_t cap = static_cast<size_t>(
+      dma::kv_pool_slots(batch, seq_len, n_kv_heads, static_cast<int>(nqt)));
+  w.kv_slice = take(32 * (units + cap));
+  w.kv_split = take(16 * units);
+  w.kv_done = take(2 * 4 * units);
+  // the pool of partial dK, dV comes last: only the backward uses it
+  w.fwd_total = off;
+  w.kv_pool = take(2 * cap * dma::kTileN * n_kv_heads * head_dim * 4);
   w.total = off;
   return w;
 }
@@ -125,12 +130,12 @@ dma_status map_kv(CUtensorMap* m, const void* base, const dma::PlanDev& p,
   return encode(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// dK / dV (fp32 [B*S][Hkv*D], or `segs` such partials one after another) as
-// TMA store targets: box = 32 columns x 32 key rows, 128-byte swizzled (one
-// warp's block of the epilogue).
-dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p, int segs = 1) {
+// dK / dV (fp32 [rows][Hkv*D]: rows = B*S, or 128 per slot of the plan's
+// pool of partials) as TMA store targets: box = 32 columns x 32 key rows,
+// 128-byte swizzled (one warp's block of the epilogue).
+dma_status map_kv_out_f32(CUtensorMap* m, void* base, const dma::PlanDev& p, long long rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim,
-                              static_cast<cuuint64_t>(segs) * p.batch * p.seq_len};
+                              static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.n_kv_heads) * p.head_dim * 4};
   const cuuint32_t box[2] = {32, 32};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
@@ -195,14 +200,18 @@ dma_status init_plan(dma_plan_s& pl, const int32_t* cu_doc_lens, int n_docs, int
   p.bwd_order = reinterpret_cast<int32_t*>(ws + w.bwd_order);
   p.delta = reinterpret_cast<float*>(ws + w.delta);
   p.v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-  p.kv_segs = dma::kv_segments(batch, seq_len, n_kv_heads);
-  p.kv_part = p.kv_segs > 1 ? reinterpret_cast<float*>(ws + w.kv_part) : nullptr;
+  p.kv_slice = reinterpret_cast<int32_t*>(ws + w.kv_slice);
+  p.kv_split = reinterpret_cast<int32_t*>(ws + w.kv_split);
+  p.kv_done = reinterpret_cast<int32_t*>(ws + w.kv_done);
+  p.kv_cap = dma::kv_pool_slots(batch, seq_len, n_kv_heads, p.n_qtiles);
+  p.kv_pool = reinterpret_cast<float*>(ws + w.kv_pool);
   pl.cu = cu_doc_lens;
   pl.n_docs = n_docs;
   if (cudaGetDevice(&pl.device) != cudaSuccess ||
       cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device) !=
           cudaSuccess)
     return DMA_ERR_CUDA;
+  p.n_sms = pl.num_sms;
   return DMA_OK;
 }
 
@@ -317,21 +326,20 @@ dma_status dma_attn_bwd_dkdv(dma_plan_t plan, const dma_bf16* q, const dma_bf16*
   if ((st = map_rows_heads(&tdo, dout, p, p.n_heads, rows)) != DMA_OK) return st;
   if ((st = map_kv(&tk, k, p)) != DMA_OK) return st;
   if ((st = map_kv(&tv, v, p)) != DMA_OK) return st;
-  CUtensorMap tdk, tdv;
+  CUtensorMap tdk, tdv, tpk, tpv;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.kv_segs > 1) {
-    // per-segment partials into the workspace, then their ordered sum
-    const size_t n = static_cast<size_t>(p.batch) * p.seq_len * p.n_kv_heads * p.head_dim;
-    if ((st = map_kv_out_f32(&tdk, p.kv_part, p, p.kv_segs)) != DMA_OK) return st;
-    if ((st = map_kv_out_f32(&tdv, p.kv_part + p.kv_segs * n, p, p.kv_segs)) != DMA_OK)
-      return st;
-    if (dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv, s) != cudaSuccess)
-      return DMA_ERR_CUDA;
-    return dma::launch_kv_reduce(*plan, dk, dv, s) == cudaSuccess ? DMA_OK : DMA_ERR_CUDA;
-  }
-  if ((st = map_kv_out_f32(&tdk, dk, p)) != DMA_OK) return st;
-  if ((st = map_kv_out_f32(&tdv, dv, p)) != DMA_OK) return st;
-  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv, s) == cudaSuccess
+  const long long kv_rows = static_cast<long long>(p.batch) * p.seq_len;
+  if ((st = map_kv_out_f32(&tdk, dk, p, kv_rows)) != DMA_OK) return st;
+  if ((st = map_kv_out_f32(&tdv, dv, p, kv_rows)) != DMA_OK) return st;
+  // the pool of partials (segments 1.. of split lists): dK slots, then dV
+  const long long prow = static_cast<long long>(p.kv_cap > 0 ? p.kv_cap : 1) * dma::kTileN;
+  if ((st = map_kv_out_f32(&tpk, p.kv_pool, p, prow)) != DMA_OK) return st;
+  if ((st = map_kv_out_f32(&tpv, p.kv_pool + static_cast<size_t>(p.kv_cap) * dma::kTileN *
+                                                 p.n_kv_heads * p.head_dim,
+                           p, prow)) != DMA_OK)
+    return st;
+  return dma::launch_dkdv(*plan, lse, tq, tk, tv, tdo, tdk, tdv, tpk, tpv, dk, dv, s) ==
+                 cudaSuccess
              ? DMA_OK
              : DMA_ERR_CUDA;
 }
@@ -498,6 +506,11 @@ dma_status dma_plan_get_view(dma_plan_t plan, dma_plan_view* out) {
   out->fwd_order = p.fwd_order;
   out->bwd_order = p.bwd_order;
   out->status = p.status;
+  out->kv_slices = p.kv_slice;
+  out->kv_splits = p.kv_split;
+  out->counts = p.sched + dma::kSchedSlices;
+  out->n_sms = p.n_sms;
+  out->kv_pool_slots = p.kv_cap;
   return DMA_OK;
 }
 
@@ -578,7 +591,8 @@ extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_doc
     return DMA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return DMA_ERR_INVALID_ARG;
   const WorkspaceLayout w = layout_for(batch, seq_len, cp_size, n_heads, n_kv_heads, head_dim);
-  if (w.total > kNoAllocScratchBytes) return DMA_ERR_WORKSPACE;  // shape needs > 64 MiB
+  // the forward needs the workspace up to the backward's pool of partials
+  if (w.fwd_total > kNoAllocScratchBytes) return DMA_ERR_WORKSPACE;  // shape needs > 64 MiB
   const dma_status dv = check_device();
   if (dv != DMA_OK) return dv;
   int dev = 0;
@@ -592,6 +606,7 @@ extern "C" dma_status dma_attn_fwd_noalloc(const int32_t* cu_doc_lens, int n_doc
   if (init_plan(pl, cu_doc_lens, n_docs, batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads,
                 head_dim, softmax_scale, ws, w) != DMA_OK)
     return DMA_ERR_CUDA;
+  pl.d.kv_pool = nullptr;  // past the scratch; only the backward would use it
   const dma::PlanDev& p = pl.d;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

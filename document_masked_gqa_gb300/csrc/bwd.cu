@@ -11,21 +11,22 @@
 // stability": gradients accumulated and reduce-scattered in FP32).
 //
 // Kernels (the default backward launches dq_kernel<D, true> and then
-// dkdv_kernel, plus kv_reduce_kernel when the key tiles' lists are split):
+// dkdv_kernel):
 //   dq_kernel     work item = (query tile, K/V head): Q and dO are copied into
 //                 TMEM (tcgen05.cp by the S and dP issuers); the item walks
 //                 the row list of key tiles; S, dP and the dQ accumulator in
 //                 TMEM; four row warpgroups split each tile's key columns.
 //                 With kDelta it also computes Delta at each item's start and
 //                 stores it for the dK/dV pass.
-//   dkdv_kernel   work item = (key tile, K/V head[, list segment]): K and V
-//                 stay in shared memory; the item walks the column list of
-//                 query tiles (all g heads of the group packed in each
-//                 128-row tile, so the GQA reduction over the group happens
-//                 inside the accumulation), a whole 128-row query tile per
-//                 step shared by two element-wise warpgroups; dV, dK
-//                 accumulate in TMEM.
-//   kv_reduce_kernel  the list segments' fp32 partials added in order.
+//   dkdv_kernel   work item = (key tile or a segment of its list, K/V
+//                 head): K and V stay in shared memory; the item walks the
+//                 column list of query tiles (all g heads of the group
+//                 packed in each 128-row tile, so the GQA reduction over the
+//                 group happens inside the accumulation), a whole 128-row
+//                 query tile per step shared by two element-wise
+//                 warpgroups; dV, dK accumulate in TMEM.  Segments 1.. of a
+//                 cut list leave fp32 partials, which the element-wise warps
+//                 add into dK, dV in segment order once all items are taken.
 //   delta_kernel  Delta[b, h, l] = sum_d dO * O as a pass of its own
 //                 (HBM-bound), for the split entry points.
 // Both attention kernels are persistent (one CTA per SM) with one TMA
@@ -189,7 +190,10 @@ struct DkdvCfg {
   static constexpr int kRing = 8;
   static constexpr int kNumBars = 26 + 2 * kRing;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kNeed = kMisc + 16 + 4 * kRing;
+  // kMisc: TMEM address, abort flag, then the ring's slots, then the split
+  // unit the element-wise warps sum (two words, by round parity)
+  static constexpr int kUnit = 16 + 4 * kRing;
+  static constexpr int kNeed = kMisc + kUnit + 8;
   static constexpr int kAlloc = (kNeed + 1024 <= kMaxSmem) ? kNeed + 1024 : kMaxSmem;
   // TMEM: dV [0,128), dK [128,256), tile buffers [256,384) and [384,512);
   // once dP^T has been read, warpgroup w's P^T sits in columns
@@ -198,29 +202,92 @@ struct DkdvCfg {
   static_assert(kNeed <= kMaxSmem, "dK/dV shared-memory layout exceeds 227 KB");
 };
 
-// Work item `item` of the dK/dV pass: (sample, key tile) in longest-list-first
-// order, times the segment of its query-tile list (kv_segs of them, each a
-// contiguous share of the list), times K/V head (the heads of one key tile
-// side by side).  `seg` also selects the partial the item writes.
+// Work item `item` of the dK/dV pass: slice item / Hkv of the plan's work
+// list (a key tile's list of query tiles, or one segment of a list the
+// planner cut) times K/V head item % Hkv (the heads of one slice side by
+// side).  `split` >= 0: the unit's segments are summed at the end of the
+// kernel; `slot` >= 0: this segment writes its partial into that pool slot
+// (segment 0 writes dK, dV).
 struct DkdvItem {
-  int b, kvh, kt, n, seg;
+  int b, kvh, kt, n, seg, split, slot;
   const int32_t* list;
 };
 __device__ __forceinline__ DkdvItem dkdv_item(const PlanDev& p, int item) {
   DkdvItem it;
-  const int ns = p.kv_segs;
-  const int ord = item / (p.n_kv_heads * ns);
-  it.seg = (item / p.n_kv_heads) % ns;
-  it.kvh = item % p.n_kv_heads;
-  const int bk = p.bwd_order[ord];
-  it.b = bk / p.n_ktiles;
-  it.kt = bk % p.n_ktiles;
-  const int cp0 = p.col_ptr[bk];
-  const int n_all = p.col_ptr[bk + 1] - cp0;
-  const int lo = (it.seg * n_all) / ns, hi = ((it.seg + 1) * n_all) / ns;
-  it.n = hi - lo;
-  it.list = p.col_idx + cp0 + lo;
+  const int s = item / p.n_kv_heads;
+  it.kvh = item - s * p.n_kv_heads;
+  const int4* e = reinterpret_cast<const int4*>(p.kv_slice) + 2 * s;
+  const int4 a = e[0], c = e[1];
+  it.b = a.x / p.n_ktiles;
+  it.kt = a.x - it.b * p.n_ktiles;
+  it.list = p.col_idx + a.y;
+  it.n = a.z;
+  it.seg = a.w;
+  it.split = c.x;
+  it.slot = c.y;
   return it;
+}
+
+// Rows [rows0, rows0 + 128 / kSumChunks) of split unit u's dK, dV (all K/V
+// heads) = segment 0's values, already there, plus the pool partials of
+// segments 1, 2, ... added in that order (the same on every run).  Threads
+// t of nt, two float4 positions and four segments' loads in flight each;
+// every load and store bypasses L1 (the partials were written by other SMs
+// during this launch).
+template <int D>
+__device__ __forceinline__ void kv_sum_chunk(const PlanDev& p, int u, int chunk, float* dk,
+                                             float* dv, int t, int nt) {
+  const int4 e = reinterpret_cast<const int4*>(p.kv_split)[u];
+  const int unit = e.x, slot0 = e.y, segs = e.z;
+  const long long row_f = static_cast<long long>(p.n_kv_heads) * D;  // floats per key row
+  const long long tile = kTileN * row_f;
+  constexpr int kRows = kTileN / kSumChunks;
+  const int b = unit / p.n_ktiles, kt = unit - b * p.n_ktiles;
+  const long long row0 = static_cast<long long>(b) * p.seq_len +
+                         static_cast<long long>(kt) * kTileN + chunk * kRows;
+  const int n4 = static_cast<int>(kRows * row_f / 4);
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    float4* out = reinterpret_cast<float4*>((which ? dv : dk) + row0 * row_f);
+    const float4* part = reinterpret_cast<const float4*>(
+        p.kv_pool + (static_cast<long long>(which) * p.kv_cap + slot0) * tile +
+        chunk * kRows * row_f);
+    const long long seg_stride = tile / 4;  // float4 per pool slot
+#pragma unroll 1
+    for (int i0 = t; i0 < n4; i0 += 2 * nt) {
+      const int i1 = i0 + nt;
+      const bool has1 = i1 < n4;
+      float4 a0 = __ldcg(out + i0);
+      float4 a1 = has1 ? __ldcg(out + i1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      int sg = 1;
+#pragma unroll 1
+      for (; sg + 3 < segs; sg += 4) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4* src = part + (sg + k - 1) * seg_stride;
+          x[k] = __ldcg(src + i0);
+          if (has1) y[k] = __ldcg(src + i1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // in segment order
+          a0.x += x[k].x; a0.y += x[k].y; a0.z += x[k].z; a0.w += x[k].w;
+          if (has1) { a1.x += y[k].x; a1.y += y[k].y; a1.z += y[k].z; a1.w += y[k].w; }
+        }
+      }
+      for (; sg < segs; ++sg) {
+        const float4* src = part + (sg - 1) * seg_stride;
+        const float4 x = __ldcg(src + i0);
+        a0.x += x.x; a0.y += x.y; a0.z += x.z; a0.w += x.w;
+        if (has1) {
+          const float4 y = __ldcg(src + i1);
+          a1.x += y.x; a1.y += y.y; a1.z += y.z; a1.w += y.w;
+        }
+      }
+      __stcg(out + i0, a0);
+      if (has1) __stcg(out + i1, a1);
+    }
+  }
 }
 
 // Persistent: the producer thread takes work items from the plan's counter
@@ -233,20 +300,22 @@ __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
-                const PlanDev p, const float* __restrict__ lse, int n_items) {
+                const __grid_constant__ CUtensorMap tpk, const __grid_constant__ CUtensorMap tpv,
+                const PlanDev p, const float* __restrict__ lse, float* dk, float* dv) {
   using Cfg = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   int32_t* const ctr = p.sched + kSchedDkdv;
+  int32_t* const tail = p.sched + kSchedTail;
   if (__syncthreads_or(threadIdx.x == 0 &&
                        *reinterpret_cast<volatile uint32_t*>(p.status) != 0u)) {
-    if (threadIdx.x == 0) items_exit(ctr);
+    if (threadIdx.x == 0) items_exit(ctr, tail);
     return;
   }
   if (pad + Cfg::kNeed > static_cast<uint32_t>(Cfg::kAlloc)) {  // cannot lay out the tiles
     if (threadIdx.x == 0) {
       atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_UNSUPPORTED));
-      items_exit(ctr);
+      items_exit(ctr, tail);
     }
     return;
   }
@@ -338,6 +407,7 @@ __global__ void __launch_bounds__(512, 1)
         // otherwise pin a second one behind it), yet early enough to hide the
         // atomic's latency.  Every index is published, empty items too (the
         // epilogue writes their zero rows).
+        const int n_items = p.sched[kSchedSlices] * p.n_kv_heads;
         int next_idx = take_item(ctr);
         for (int rk = 0; ok; ++rk) {
           const int item = next_idx < n_items ? next_idx : -1;
@@ -642,6 +712,47 @@ __global__ void __launch_bounds__(512, 1)
       }
       tbase += it.n;
     }
+    // ----------------------------------------------- sums of split lists
+    // Once every item is taken, the element-wise warps of each CTA take the
+    // (split unit, row chunk) sums one at a time and, when the epilogue warps
+    // of all the unit's segments have counted them done, add the partials
+    // into dK, dV.  Every segment waited for is held by a running CTA, so the
+    // waits end.  The last chunk of a unit puts its two counters back to
+    // zero for the next launch.
+    const int n_split = p.sched[kSchedSplits];
+    if (n_split > 0) {
+      const int n_sum = n_split * kSumChunks;
+      int32_t* const chunks_done = p.kv_done + p.batch * p.n_ktiles;
+      volatile int* s_unit = reinterpret_cast<volatile int*>(smem + Cfg::kMisc + Cfg::kUnit);
+#pragma unroll 1
+      for (int round = 0;; ++round) {
+        if (t == 0) {
+          int x = n_sum;
+          if (!*abort_flag && *reinterpret_cast<volatile uint32_t*>(p.status) == 0u) {
+            x = atomicAdd(tail, 1);
+            if (x < n_sum) {
+              const int u = x / kSumChunks;
+              const int segs = p.kv_split[4 * u + 2];
+              if (!wait_count(p.kv_done + u, 4 * p.n_kv_heads * segs, ctl)) x = n_sum;
+            }
+          }
+          s_unit[round & 1] = x;
+        }
+        named_bar_sync(1, 256);
+        const int x = s_unit[round & 1];
+        if (x >= n_sum) break;
+        const int u = x / kSumChunks;
+        kv_sum_chunk<D>(p, u, x - u * kSumChunks, dk, dv, t, 256);
+        named_bar_sync(1, 256);  // every thread's stores issued before the count
+        if (t == 0) {
+          __threadfence();
+          if (atomicAdd(chunks_done + u, 1) == kSumChunks - 1) {
+            p.kv_done[u] = 0;  // every chunk has waited on it: nothing reads it now
+            chunks_done[u] = 0;
+          }
+        }
+      }
+    }
   } else {
     reg_dealloc<kDkdvEpiRegs>();
     // --------------------------------------------------------------- epilogue
@@ -660,7 +771,12 @@ __global__ void __launch_bounds__(512, 1)
       if (!ring.get_warp(rk, item, ctl)) { ok = false; break; }
       if (item < 0) break;
       const DkdvItem it = dkdv_item(p, item);
-      const int row0 = (it.seg * p.batch + it.b) * p.seq_len + it.kt * kTileN + 32 * wq;
+      // segments 1.. of a split list go to their pool slot, the rest to dK, dV
+      const bool to_pool = it.slot >= 0;
+      const int row0 = to_pool ? it.slot * kTileN + 32 * wq
+                               : it.b * p.seq_len + it.kt * kTileN + 32 * wq;
+      const CUtensorMap* map_k = to_pool ? &tpk : &tdk;
+      const CUtensorMap* map_v = to_pool ? &tpv : &tdv;
       const bool empty = it.n == 0;
       if (!empty) {
         if (!warp_wait(acc_done, ibase & 1, ctl)) { ok = false; break; }
@@ -696,13 +812,24 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) {
           asm volatile(
               "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                  reinterpret_cast<uint64_t>(is_dk ? &tdk : &tdv)),
+                  reinterpret_cast<uint64_t>(is_dk ? map_k : map_v)),
               "r"(stg), "r"(it.kvh * D + c0), "r"(row0)
               : "memory");
           bulk_commit();
         }
       }
       if (!empty) ++ibase;
+      if (it.split >= 0) {
+        // this warp's rows of the segment count once its stores are complete
+        // (4 warps x Hkv heads x segments complete a split unit)
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(p.kv_done + it.split, 1);
+        }
+        __syncwarp();
+      }
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -713,7 +840,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0) items_exit(ctr);
+  if (threadIdx.x == 0) items_exit(ctr, tail);
 }
 
 // ------------------------------------------------------------------- dQ
@@ -1336,23 +1463,6 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
-// dK, dV = the sum of the kv_segs partials, added in segment order (the
-// same on every run).  4 elements per thread.
-__global__ void kv_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ dk,
-                                 float4* __restrict__ dv, long long n4, int segs) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float4 a = part[i], b = part[segs * n4 + i];
-    for (int s = 1; s < segs; ++s) {
-      const float4 x = part[s * n4 + i], y = part[(segs + s) * n4 + i];
-      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
-    }
-    dk[i] = a;
-    dv[i] = b;
-  }
-}
-
 template <int D>
 cudaError_t launch_delta_d(const dma_plan_s& pl, const float* o, const dma_bf16* dout,
                            cudaStream_t s) {
@@ -1369,16 +1479,21 @@ cudaError_t launch_delta_d(const dma_plan_s& pl, const float* o, const dma_bf16*
 template <int D>
 cudaError_t launch_dkdv_d(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                          const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
+                          const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tpk,
+                          const CUtensorMap& tpv, float* dk, float* dv, cudaStream_t s) {
   const PlanDev& p = pl.d;
-  const int items = p.batch * p.n_ktiles * p.n_kv_heads * p.kv_segs;
-  if (items == 0) return cudaSuccess;
+  // the planner writes the work list on the device; at most one slice per
+  // unit plus one per pool slot
+  const long long items_max =
+      (static_cast<long long>(p.batch) * p.n_ktiles + p.kv_cap) * p.n_kv_heads;
+  if (items_max == 0) return cudaSuccess;
   // persistent: one CTA per SM (TMEM and shared memory allow no more)
-  const int grid = items < pl.num_sms ? items : pl.num_sms;
+  const int grid = items_max < pl.num_sms ? static_cast<int>(items_max) : pl.num_sms;
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DkdvCfg<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<grid, 512, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, p, lse, items);
+  dkdv_kernel<D><<<grid, 512, DkdvCfg<D>::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, tpk, tpv, p, lse,
+                                                       dk, dv);
   return cudaGetLastError();
 }
 
@@ -1422,22 +1537,11 @@ cudaError_t launch_delta(const dma_plan_s& pl, const float* o, const dma_bf16* d
 
 cudaError_t launch_dkdv(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s) {
-  return pl.d.head_dim == 128 ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s)
-                              : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, tdk, tdv, s);
-}
-
-cudaError_t launch_kv_reduce(const dma_plan_s& pl, float* dk, float* dv, cudaStream_t s) {
-  const PlanDev& p = pl.d;
-  const long long n4 =
-      static_cast<long long>(p.batch) * p.seq_len * p.n_kv_heads * p.head_dim / 4;
-  if (n4 == 0) return cudaSuccess;
-  long long blocks = (n4 + 255) / 256;
-  if (blocks > 8LL * pl.num_sms) blocks = 8LL * pl.num_sms;
-  kv_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(p.kv_part), reinterpret_cast<float4*>(dk),
-      reinterpret_cast<float4*>(dv), n4, p.kv_segs);
-  return cudaGetLastError();
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tpk,
+                        const CUtensorMap& tpv, float* dk, float* dv, cudaStream_t s) {
+  return pl.d.head_dim == 128
+             ? launch_dkdv_d<128>(pl, lse, tq, tk, tv, tdo, tdk, tdv, tpk, tpv, dk, dv, s)
+             : launch_dkdv_d<64>(pl, lse, tq, tk, tv, tdo, tdk, tdv, tpk, tpv, dk, dv, s);
 }
 
 cudaError_t launch_dq(const dma_plan_s& pl, const float* lse, const CUtensorMap& tq,

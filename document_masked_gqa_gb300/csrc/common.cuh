@@ -15,35 +15,52 @@ constexpr int kTileN = 128;  // key positions per tile
 constexpr uint32_t kPartialBit = 0x80000000u;
 constexpr uint32_t kIndexMask = 0x7FFFFFFFu;
 
-// dK/dV work items are (key tile, K/V head).  When a shape has fewer than
-// kKvSplitItems of them (a short sequence with one K/V head, say), most SMs
-// would idle, so each key tile's list of query tiles is cut into segments,
-// up to kKvMaxSegs, each its own work item writing an fp32 partial of dK, dV;
-// a reduction sums the partials in segment order.
-constexpr int kKvSplitItems = 256;
-constexpr int kKvMaxSegs = 8;
-__host__ __device__ inline int kv_segments(int batch, int seq_len, int n_kv_heads) {
-  const long long items = static_cast<long long>(batch) * (seq_len / kTileN) * n_kv_heads;
-  if (items <= 0 || items >= kKvSplitItems) return 1;
-  const long long s = (kKvSplitItems + items - 1) / items;
-  return static_cast<int>(s < kKvMaxSegs ? s : kKvMaxSegs);
+// dK/dV work: a key tile's list of query tiles is one work unit per K/V
+// head; a list much longer than the mean work per SM would hold one SM long
+// after the others are done, so the planner may cut the lists longer than a
+// length L into ceil(n / L) contiguous segments (never shorter than
+// kSegMin tiles).  Segment 0 writes dK, dV; the others write fp32 partials
+// into a pool of slots, summed in segment order into dK, dV at the end of the
+// dK/dV kernel.  The planner splits only when its bound on the greedy
+// makespan of the longest-first order exceeds kSplitOn = 23/20 times the
+// mean work per SM, and then picks the longest L whose bound is within
+// kSplitTarget = 11/10 times the mean (see plan.cu).
+constexpr int kSegMin = 16;
+// the final sum of a cut list runs as kSumChunks items of 128 / kSumChunks key rows
+constexpr int kSumChunks = 8;
+constexpr int kSplitOnNum = 23, kSplitOnDen = 20, kSplitTargetNum = 11, kSplitTargetDen = 10;
+// Pool slots (one slot: 128 key rows x all K/V heads x D, for dK and for dV)
+// the workspace holds: as many as there are (sample, key tile) units, at
+// least 512 / Hkv where the lists are long enough to be cut at all.
+__host__ __device__ inline int kv_pool_slots(int batch, int seq_len, int n_kv_heads,
+                                             int n_qtiles) {
+  const long long units = static_cast<long long>(batch) * (seq_len / kTileN);
+  const long long max_extra = units * ((n_qtiles + kSegMin - 1) / kSegMin - 1);
+  long long floor_slots = (512 + n_kv_heads - 1) / n_kv_heads;
+  if (floor_slots > max_extra) floor_slots = max_extra;
+  const long long s = units > floor_slots ? units : floor_slots;
+  return static_cast<int>(s < 0 ? 0 : s);
 }
 
-constexpr int kSchedFwd = 0, kSchedDkdv = 2;
-// bytes at the start of the workspace: status words [0, 16), work counters [32, 48)
+// int32 words at kSchedOffset: the forward's work counters (next item, CTAs
+// exited), the dK/dV kernel's, the number of dK/dV list slices and of split
+// units (written by the planner), and the dK/dV kernel's counter of split
+// units taken for their final sum
+constexpr int kSchedFwd = 0, kSchedDkdv = 2, kSchedSlices = 4, kSchedSplits = 5, kSchedTail = 6;
+// bytes at the start of the workspace: status words [0, 16), the words above [32, 64)
 constexpr int kStatusBytes = 64, kSchedOffset = 32;
 
 // Device-visible shape and workspace pointers of one rank's plan.
 struct PlanDev {
   int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
   int chunk, local_len, group, tile_pos, n_qtiles, n_ktiles;
+  int n_sms;         // SMs of the device (the dK/dV split rule balances over them)
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   uint64_t timeout_ns;
   uint32_t* status;   // [0] error word (kernels do nothing once set), [1] warning bits
-  int32_t* sched;     // work counters of the persistent kernels, two per kernel
-                      // (next item, CTAs exited): forward at kSchedFwd, dK/dV at
-                      // kSchedDkdv; zeroed with the status words by the plan
+  int32_t* sched;     // work counters and dK/dV list counts (kSched*); zeroed
+                      // with the status words by the plan
   int32_t* qpos;      // [Lq]
   int32_t* doc_lo;    // [B][Lq]
   int32_t* doc_hi;    // [B][S] end (exclusive) of each key position's document
@@ -59,13 +76,23 @@ struct PlanDev {
   int32_t* bwd_order; // [B*nKt]
   float* delta;       // [B][Hq][Lq]
   uint16_t* v16;      // [B][S][Hkv][D] fp16 copy of V for the forward's P V
-  int kv_segs;        // segments per key tile's query list (kv_segments)
-  float* kv_part;     // kv_segs > 1: [2][kv_segs][B][S][Hkv][D] partial dK, then dV
+  // dK/dV work list, in launch order: per slice (a unit's list or one
+  // segment of it) 8 int32: unit b*n_ktiles + kt, first entry in col_idx,
+  // length, segment, split-unit index (-1: not split), pool slot (-1:
+  // segment 0 or not split, which write dK, dV), 0, 0
+  int32_t* kv_slice;  // [units + kv_cap][8]
+  // per split unit: unit, first pool slot (of segment 1), segments, 0
+  int32_t* kv_split;  // [units][4]
+  int32_t* kv_done;   // [2][units] per split unit: epilogue warps done with its
+                      // segments, then sum chunks done
+  int kv_cap;         // pool slots (kv_pool_slots)
+  float* kv_pool;     // [2][kv_cap][128][Hkv][D] partial dK, then dV
 };
 
 struct WorkspaceLayout {
   size_t status, qpos, doc_lo, doc_hi, chunk_order, tile_class, row_cnt, row_ptr, row_idx, col_cnt,
-      col_ptr, col_idx, fwd_order, bwd_order, delta, v16, kv_part, total;
+      col_ptr, col_idx, fwd_order, bwd_order, delta, v16, kv_slice, kv_split, kv_done,
+      fwd_total, kv_pool, total;
 };
 
 }  // namespace dma
@@ -100,16 +127,17 @@ cudaError_t launch_fwd(const dma_plan_s& p, const CUtensorMap& tq, const CUtenso
                        cudaStream_t s);
 cudaError_t launch_delta(const dma_plan_s& p, const float* o, const dma_bf16* dout,
                          cudaStream_t s);
+// tpk, tpv: the plan's pool of partial dK, dV (segments 1.. of split lists)
 cudaError_t launch_dkdv(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                        const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s);
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tpk,
+                        const CUtensorMap& tpv, float* dk, float* dv, cudaStream_t s);
 // to != nullptr: the dQ kernel also computes Delta from O (map `to`, fp32)
 // and stores it in the plan's workspace
 cudaError_t launch_dq(const dma_plan_s& p, const float* lse, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const CUtensorMap& tdq, const CUtensorMap* to, const float* o,
                       const dma_bf16* dout, dma_bf16* dq, cudaStream_t s);
-cudaError_t launch_kv_reduce(const dma_plan_s& p, float* dk, float* dv, cudaStream_t s);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, uint32_t* status, cudaStream_t s);
 cudaError_t launch_status_out(const uint32_t* status, uint32_t* out, cudaStream_t s);
 cudaError_t launch_cp_chunk_copy(const void* src, void* dst, int batch, int seq_len, int cp_size,

@@ -51,8 +51,13 @@ __global__ void plan_positions_kernel(PlanDev p, const int32_t* __restrict__ cu,
     if (cu[lo] != want) atomicCAS(p.status, 0u, static_cast<uint32_t>(DMA_ERR_BAD_DOCS));
   }
 
-  // --- column counts start at zero (the block-mask builder adds to them)
-  for (int i = tid; i < p.batch * p.n_ktiles; i += nthreads) p.col_cnt[i] = 0;
+  // --- column counts start at zero (the block-mask builder adds to them), and
+  // so do the dK/dV kernel's per-unit counters of finished segments
+  for (int i = tid; i < p.batch * p.n_ktiles; i += nthreads) {
+    p.col_cnt[i] = 0;
+    p.kv_done[i] = 0;
+    p.kv_done[p.batch * p.n_ktiles + i] = 0;
+  }
 
   // --- chunk order (rank-major) and position map
   for (int j = tid; j < 2 * p.cp_size; j += nthreads)
@@ -133,28 +138,29 @@ __global__ void mask_classify_kernel(PlanDev p) {
 }
 
 // Block-wide exclusive scan helper (blockDim.x a multiple of 32, at most 1024).
-__device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
+template <typename T>
+__device__ T block_exclusive_scan(T v, T* s_tmp, T* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int x = v;
+  T x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) s_tmp[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int w = (lane < (blockDim.x >> 5)) ? s_tmp[lane] : 0;
+    T w = (lane < static_cast<int>(blockDim.x >> 5)) ? s_tmp[lane] : T(0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      const T y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
     s_tmp[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  const int warp_prefix = (wid > 0) ? s_tmp[wid - 1] : 0;
-  const int incl = x + warp_prefix;
+  const T warp_prefix = (wid > 0) ? s_tmp[wid - 1] : T(0);
+  const T incl = x + warp_prefix;
   *total = s_tmp[(blockDim.x >> 5) - 1];
   __syncthreads();
   return incl - v;
@@ -162,13 +168,205 @@ __device__ int block_exclusive_scan(int v, int* s_tmp, int* total) {
 
 constexpr int kSortMax = 2048;  // units the one-block sort of the launch orders takes
 
+// Block-wide maximum (blockDim.x a multiple of 32).
+template <typename T>
+__device__ T block_max(T v, T* s_tmp) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const T y = __shfl_xor_sync(0xffffffffu, v, o);
+    v = y > v ? y : v;
+  }
+  if (lane == 0) s_tmp[wid] = v;
+  __syncthreads();
+  T r = s_tmp[0];
+  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) r = s_tmp[i] > r ? s_tmp[i] : r;
+  __syncthreads();
+  return r;
+}
+
+// Sorts s_key[0, npow) ascending (npow a power of two) with a bitonic
+// network; the whole block takes part.
+__device__ void bitonic_sort(unsigned long long* s_key, int npow) {
+  for (int k = 2; k <= npow; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = s_key[i], b = s_key[ixj];
+          if ((a > b) == ((i & k) == 0)) {
+            s_key[i] = b;
+            s_key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ int key_count(unsigned long long k) {
+  return 0x7FFFFFFF - static_cast<int>(k >> 32);
+}
+
+__device__ __forceinline__ void put_slice(const PlanDev& p, int at, int unit, int first, int n,
+                                          int seg, int split, int slot) {
+  int4* e = reinterpret_cast<int4*>(p.kv_slice + 8 * static_cast<long long>(at));
+  e[0] = make_int4(unit, first, n, seg);
+  e[1] = make_int4(split, slot, 0, 0);
+}
+
+// The dK/dV work list, from the units (sample, key tile) sorted longest list
+// first in s_key (keys as the launch orders' sort leaves them), for n <=
+// kSortMax units; block of 1024 threads, two units per thread.
+//
+// Greedy list scheduling takes each work item, in order, on the SM that
+// frees first, so item j starts no later than the work before it divided by
+// the SMs, and ends no later than that plus its own length.  With the units'
+// K/V heads side by side, unit o (list length c_o, lists before it summing to
+// pre_o) thus ends by E_o = (Hkv pre_o + (Hkv - 1) c_o) / P + c_o, against a
+// mean of m = Hkv sum(c) / P per SM.  Cutting every list longer than L into
+// ceil(c / L) segments leaves the bounds of the units at or after the first
+// one not longer than L as they were and caps those before at about their
+// end plus L.  So: no cut when every E_o <= kSplitOn m; else L = the length
+// at the first position from which every E_o <= kSplitTarget m (at least
+// kSegMin), lengthened while the pool cannot hold the segments.  The cut
+// units' segments are then ordered by their length among the other units.
+// The comparisons run exactly in integers: P E_o against the ratios' numerators
+// and denominators times P m = Hkv sum(c).
+__device__ void plan_dkdv_slices(const PlanDev& p, unsigned long long* s_key, int n, int npow,
+                                 int* s_tmp, long long* s_ll) {
+  const long long Hkv = p.n_kv_heads, P = p.n_sms > 0 ? p.n_sms : 1;
+  // thread t holds launch positions 2t and 2t + 1
+  const int o0 = 2 * static_cast<int>(threadIdx.x);
+  int c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) c[j] = o0 + j < n ? key_count(s_key[o0 + j]) : 0;
+  int carry;
+  const int pre0 = block_exclusive_scan(c[0] + c[1], s_tmp, &carry);
+  const long long hw = Hkv * carry;  // P m
+  long long pe[2];                   // P E_o
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int pre = pre0 + (j ? c[0] : 0);
+    pe[j] = o0 + j < n ? Hkv * pre + (Hkv - 1) * c[j] + P * c[j] : 0;
+  }
+  const long long pe_max = block_max(pe[0] > pe[1] ? pe[0] : pe[1], s_ll);
+  int L = 0x7FFFFFFF;  // no cut
+  if (carry > 0 && kSplitOnDen * pe_max > kSplitOnNum * hw) {
+    long long last = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (o0 + j < n && kSplitTargetDen * pe[j] > kSplitTargetNum * hw) last = o0 + j + 1;
+    const int last_over = static_cast<int>(block_max(last, s_ll)) - 1;
+    const int o_star = last_over + 1 < n ? last_over + 1 : n - 1;
+    const int c_first = key_count(s_key[0]);
+    L = key_count(s_key[o_star]);
+    if (L < kSegMin) L = kSegMin;
+    // L grows by at least an eighth per round (a few hundred rounds reach
+    // any list length); no cut unless the pool holds the segments
+    bool fits = false;
+    for (int round = 0; round < 4096 && L < c_first; ++round) {
+      int need = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (c[j] > L) need += (c[j] + L - 1) / L - 1;
+      int total;
+      (void)block_exclusive_scan(need, s_tmp, &total);
+      if (total <= p.kv_cap) {
+        fits = true;
+        break;
+      }
+      L += L / 8 > 1 ? L / 8 : 1;
+    }
+    if (!fits) L = 0x7FFFFFFF;
+  }
+  if (L == 0x7FFFFFFF) {  // uniform: the launch order, uncut
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (o0 + j < n) {
+        const int unit = static_cast<int>(s_key[o0 + j] & 0xFFFFFFFFull);
+        put_slice(p, o0 + j, unit, p.col_ptr[unit], c[j], 0, -1, -1);
+      }
+    }
+    if (threadIdx.x == 0) {
+      p.sched[kSchedSlices] = n;
+      p.sched[kSchedSplits] = 0;
+    }
+    return;
+  }
+  __syncthreads();  // every read of the first order is done
+  // order the units by their segments' length, longest first
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (o0 + j < n) {
+      const unsigned int unit = static_cast<unsigned int>(s_key[o0 + j] & 0xFFFFFFFFull);
+      const int segs = c[j] > L ? (c[j] + L - 1) / L : 1;
+      const int len = (c[j] + segs - 1) / segs;
+      s_key[o0 + j] = (static_cast<unsigned long long>(0x7FFFFFFF - len) << 32) | unit;
+    }
+  }
+  __syncthreads();
+  bitonic_sort(s_key, npow);
+  // slices, split units and pool slots in launch order, from one scan of
+  // (slices, split units, pool slots) packed 21 bits apiece (n <= 2048 units
+  // and at most as many pool slots as units or 512: each sum < 2^21)
+  int unit[2], cnt[2], segs[2];
+  long long pk[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    unit[j] = 0;
+    cnt[j] = 0;
+    segs[j] = 0;
+    if (o0 + j < n) {
+      unit[j] = static_cast<int>(s_key[o0 + j] & 0xFFFFFFFFull);
+      cnt[j] = p.col_cnt[unit[j]];
+      segs[j] = cnt[j] > L ? (cnt[j] + L - 1) / L : 1;
+    }
+    pk[j] = static_cast<long long>(segs[j]) | (static_cast<long long>(segs[j] > 1) << 21) |
+            (static_cast<long long>(segs[j] > 1 ? segs[j] - 1 : 0) << 42);
+  }
+  long long tot;
+  const long long base = block_exclusive_scan(pk[0] + pk[1], s_ll, &tot);
+  constexpr long long kField = (1ll << 21) - 1;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (o0 + j >= n) continue;
+    const long long at = base + (j ? pk[0] : 0);
+    const int my_at = static_cast<int>(at & kField);
+    const int my_split = static_cast<int>((at >> 21) & kField);
+    const int my_slot = static_cast<int>((at >> 42) & kField);
+    const int first = p.col_ptr[unit[j]];
+    if (segs[j] == 1) {
+      put_slice(p, my_at, unit[j], first, cnt[j], 0, -1, -1);
+    } else {
+      // segment sg: q + 1 query tiles for sg < r, else q (q, r = cnt / segs, cnt % segs)
+      const int q = cnt[j] / segs[j], r = cnt[j] - q * segs[j];
+      int lo = 0;
+      for (int sg = 0; sg < segs[j]; ++sg) {
+        const int len = q + (sg < r ? 1 : 0);
+        put_slice(p, my_at + sg, unit[j], first + lo, len, sg, my_split,
+                  sg > 0 ? my_slot + sg - 1 : -1);
+        lo += len;
+      }
+      reinterpret_cast<int4*>(p.kv_split)[my_split] = make_int4(unit[j], my_slot, segs[j], 0);
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.sched[kSchedSlices] = static_cast<int>(tot & kField);
+    p.sched[kSchedSplits] = static_cast<int>((tot >> 21) & kField);
+  }
+}
+
 // two blocks of 1024, block 0 for the rows and block 1 for the columns:
 // exclusive scan of the counts, then the longest-first launch order when
 // there are at most kSortMax units (order_kernel takes larger ones).  The order sorts the keys
 // (INT_MAX - count, index) ascending with a bitonic network in shared
-// memory: longer lists first, ties by ascending index.
+// memory: longer lists first, ties by ascending index.  Block 1 then lays
+// out the dK/dV work list (plan_dkdv_slices).
 __global__ void scan_order_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
+  __shared__ long long s_ll[32];
   __shared__ unsigned long long s_key[kSortMax];
   {
     const int which = blockIdx.x;
@@ -186,7 +384,14 @@ __global__ void scan_order_kernel(PlanDev p) {
     }
     if (threadIdx.x == 0) ptr[n] = carry;
     __syncthreads();
-    if (n > kSortMax) return;  // uniform across the block
+    if (n > kSortMax) {  // uniform across the block
+      // the dK/dV work list is the launch order itself (kv_slices_kernel)
+      if (which == 1 && threadIdx.x == 0) {
+        p.sched[kSchedSlices] = n;
+        p.sched[kSchedSplits] = 0;
+      }
+      return;
+    }
     int32_t* order = which == 0 ? p.fwd_order : p.bwd_order;
     int npow = 1;
     while (npow < n) npow <<= 1;
@@ -195,25 +400,20 @@ __global__ void scan_order_kernel(PlanDev p) {
                             static_cast<unsigned int>(i))
                          : ~0ull;
     __syncthreads();
-    for (int k = 2; k <= npow; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < npow; i += blockDim.x) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const unsigned long long a = s_key[i], b = s_key[ixj];
-            if ((a > b) == ((i & k) == 0)) {
-              s_key[i] = b;
-              s_key[ixj] = a;
-            }
-          }
-        }
-        __syncthreads();
-      }
-    }
+    bitonic_sort(s_key, npow);
     for (int i = threadIdx.x; i < n; i += blockDim.x)
       order[i] = static_cast<int32_t>(s_key[i] & 0xFFFFFFFFull);
     __syncthreads();
+    if (which == 1) plan_dkdv_slices(p, s_key, n, npow, s_tmp, s_ll);
   }
+}
+
+// The dK/dV work list of more than kSortMax units: the launch order, uncut.
+__global__ void kv_slices_kernel(PlanDev p) {
+  const int o = blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= p.batch * p.n_ktiles) return;
+  const int unit = p.bwd_order[o];
+  put_slice(p, o, unit, p.col_ptr[unit], p.col_cnt[unit], 0, -1, -1);
 }
 
 // grid (n_qtiles + n_ktiles, batch): row lists, then column lists; block 256
@@ -339,7 +539,10 @@ cudaError_t launch_plan_kernels(const dma_plan_s& pl, cudaStream_t s) {
   scan_order_kernel<<<2, 1024, 0, s>>>(p);
   const int nq = p.batch * p.n_qtiles, nk = p.batch * p.n_ktiles;
   if (nq > kSortMax) order_kernel<<<(nq + 255) / 256, 256, 0, s>>>(p.row_cnt, nq, p.fwd_order);
-  if (nk > kSortMax) order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
+  if (nk > kSortMax) {
+    order_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p.col_cnt, nk, p.bwd_order);
+    kv_slices_kernel<<<(nk + 255) / 256, 256, 0, s>>>(p);
+  }
   fill_lists_kernel<<<dim3(p.n_qtiles + p.n_ktiles, p.batch), 256, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -158,6 +158,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Global-memory writes of the async proxy (completed bulk stores) are ordered
+// before this thread's later generic-proxy accesses after this fence.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Named barrier `id` (1..15) over `n` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // -------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -493,14 +510,35 @@ struct ItemRing {
 __device__ __forceinline__ int take_item(int32_t* ctr) { return atomicAdd(ctr, 1); }
 
 // Called once per CTA (one thread) as it exits, on every path: the last CTA
-// of the launch puts both counters back to zero for the next launch.  Every
-// CTA has taken its last index before it gets here.
-__device__ __forceinline__ void items_exit(int32_t* ctr) {
+// of the launch puts both counters (and `also`, another counter of the
+// launch) back to zero for the next launch.  Every CTA has taken its last
+// index before it gets here.
+__device__ __forceinline__ void items_exit(int32_t* ctr, int32_t* also = nullptr) {
   __threadfence();
   if (atomicAdd(ctr + 1, 1) == static_cast<int>(gridDim.x) - 1) {
     atomicExch(ctr, 0);
     atomicExch(ctr + 1, 0);
+    if (also) atomicExch(also, 0);
     __threadfence();
+  }
+}
+
+// Bounded wait, by one thread, until the global counter reaches `target`
+// (acquire).  Gives up when this CTA is aborting, when another CTA has
+// recorded an error, or after the wait limit (recording DMA_ERR_TIMEOUT).
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, const WaitCtl& c) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*c.abort_flag || *reinterpret_cast<volatile uint32_t*>(c.status) != 0u) return false;
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      *c.abort_flag = 1;
+      atomicCAS(c.status, 0u, 5u);
+      __threadfence();
+      return false;
+    }
   }
 }
 

@@ -248,6 +248,19 @@ dma_status dma_cp_permute(const void* full, void* gathered, int batch, int seq_l
  *   fwd_order int32 [batch*n_qtiles]: query tiles (b*n_qtiles + t) by
  *             non-increasing list length, ties by index.
  *   bwd_order int32 [batch*n_ktiles]: key tiles likewise.
+ *   kv_slices int32 [n_kv_slices][8]: the dK/dV work list in launch order.
+ *             Per slice: key tile (b*n_ktiles + kt), first entry in col_idx,
+ *             length, segment, split-unit index (-1 when the tile's list is
+ *             not cut), pool slot (-1 for segment 0 and uncut lists), 0, 0.
+ *             The planner cuts the lists longer than a length L into
+ *             ceil(n / L) contiguous segments when its bound on the greedy
+ *             makespan over n_sms SMs says one SM would otherwise run long
+ *             after the others; slices are ordered by non-increasing length.
+ *   kv_splits int32 [n_kv_splits][4]: per cut list: key tile, pool slot of
+ *             segment 1, segments, 0.
+ *   counts    int32 [2]: n_kv_slices, n_kv_splits (device-written).
+ *   n_sms, kv_pool_slots: SMs the plan balances over; slots of the pool of
+ *             fp32 partial dK, dV (segments 1.. of cut lists) in the workspace.
  */
 typedef struct {
   int batch, seq_len, cp_size, cp_rank, n_heads, n_kv_heads, head_dim;
@@ -264,6 +277,10 @@ typedef struct {
   const int32_t* fwd_order;
   const int32_t* bwd_order;
   const uint32_t* status;
+  const int32_t* kv_slices;
+  const int32_t* kv_splits;
+  const int32_t* counts;
+  int n_sms, kv_pool_slots;
 } dma_plan_view;
 
 dma_status dma_plan_get_view(dma_plan_t plan, dma_plan_view* out);

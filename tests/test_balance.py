@@ -142,3 +142,89 @@ def test_cost_fit_recovers_known_constants():
     got = balance.fit_costs(feats, times)
     assert np.allclose(got, coef, rtol=1e-3, atol=1e-6)
     assert np.allclose(balance.predict_ms(feats, got), times, rtol=1e-4)
+
+
+def _slices_cover(work, counts):
+    got = {}
+    for unit, first, n, seg, split, slot in work["slices"]:
+        got.setdefault(unit, []).append((first, n, seg))
+    assert sorted(got) == list(range(len(counts)))
+    for unit, parts in got.items():
+        parts.sort()
+        assert [p[2] for p in parts] == list(range(len(parts)))
+        pos = 0
+        for first, n, _ in parts:
+            assert first == pos
+            pos += n
+        assert pos == counts[unit]
+
+
+def test_kv_work_list_hand_case():
+    """One list of 100 query tiles and three of 1 over 4 SMs: the mean is
+    25.75 tiles per SM and the long list alone bounds the greedy makespan at
+    100 (> 1.15 x 25.75), while from the second unit on every bound is at most
+    26.5 (< 1.10 x 25.75): L = max(16, 1) = 16, so 7 segments (6 pool slots)
+    of 15 or 14 tiles, ahead of the three short lists."""
+    assert balance.SEG_MIN == 16
+    counts = [1, 100, 1, 1]
+    work = balance.kv_work_list(counts, 1, 4, 20)
+    assert work["L"] == 16
+    assert work["splits"] == [(1, 0, 7)]
+    lens = [n for u, f, n, sg, sp, sl in work["slices"] if u == 1]
+    assert lens == [15] * 2 + [14] * 5  # 100 = 7 x 14 + 2: the first 2 take one more
+    assert [s[0] for s in work["slices"]] == [1] * 7 + [0, 2, 3]
+    assert [s[5] for s in work["slices"][:7]] == [-1] + list(range(6))
+    _slices_cover(work, counts)
+    # a pool of 5 slots: L grows 16, 18 until ceil(100 / L) - 1 <= 5
+    work = balance.kv_work_list(counts, 1, 4, 5)
+    assert work["L"] == 18 and work["splits"] == [(1, 0, 6)]
+    # no pool: no cut, the longest-first order
+    work = balance.kv_work_list(counts, 1, 4, 0)
+    assert work["L"] is None and work["splits"] == []
+    assert [s[0] for s in work["slices"]] == [1, 0, 2, 3]
+
+
+def test_kv_work_list_leaves_even_lists_alone():
+    """1000 lists of 10 tiles on 152 SMs: the bound (75.7) is over 1.15 x the
+    mean (65.8), but no length below 10 brings every bound within 1.10 x the
+    mean before the last unit, so L = 10 = the longest list: nothing to cut."""
+    work = balance.kv_work_list([10] * 1000, 1, 152, 1000)
+    assert work["L"] is None
+    assert [s[0] for s in work["slices"]] == list(range(1000))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_kv_work_list_covers_every_list(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 300))
+    counts = (rng.pareto(1.2, n) * 20).astype(int).tolist()
+    for hkv, sms, cap in [(1, 152, 512), (8, 152, 64), (1, 16, 40), (2, 4, 3)]:
+        work = balance.kv_work_list(counts, hkv, sms, cap)
+        _slices_cover(work, counts)
+        lens = [s[2] for s in work["slices"]]
+        seg_lens = [-(-counts[s[0]] // max(1, sum(1 for t in work["slices"] if t[0] == s[0])))
+                    for s in work["slices"]]
+        assert all(a >= b for a, b in zip(seg_lens[:-1], seg_lens[1:]))
+        slots = sum(k - 1 for _, _, k in work["splits"])
+        assert slots <= cap
+        if work["L"] is not None:
+            assert work["L"] >= balance.SEG_MIN
+            assert max(lens) <= max(work["L"], max((c for c in counts if c <= work["L"]), default=0))
+
+
+@pytest.mark.parametrize("name,cut", [("8b", False), ("70b", True), ("sparse", True),
+                                      ("405b-logu", True)])
+def test_kv_work_list_on_the_workloads(name, cut):
+    """The rule leaves the 8B layer's lists whole (its greedy bound is within
+    1.02 of the mean) and cuts the 70B shard's, the sparse-mask stress's and
+    the log-uniform 405B case's, whose longest lists are several times the
+    mean work per SM."""
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    r = w.ranks[-1]
+    c = balance.tile_counts(cu, w.batch, w.seq_len, w.cp_size, r, w.group)
+    nqt = (w.seq_len // w.cp_size) // (128 // w.group)
+    work = balance.kv_work_list(c["col_counts"], w.n_kv_heads, 152,
+                                balance.kv_pool_slots(w.batch, w.seq_len, w.n_kv_heads, nqt))
+    assert (work["L"] is not None) == cut
+    _slices_cover(work, c["col_counts"].tolist())

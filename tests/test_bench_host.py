@@ -165,24 +165,19 @@ def test_two_processes_split_the_emulated_ranks_and_reassemble():
 
 
 def test_kernels_per_step_follow_the_planner():
-    # four planner kernels, V to fp16 + forward, dQ with Delta + dK/dV
-    for name in ["8b", "sparse", "405b-1doc"]:
+    # four planner kernels, V to fp16 + forward, dQ with Delta + dK/dV (cut
+    # dK/dV lists are summed inside the dK/dV kernel)
+    for name in ["tiny", "8b", "70b", "sparse", "405b-1doc", "405b-logu"]:
         assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 8
-    # fewer than 256 (key tile, K/V head) items: the dK/dV lists are split
-    # and a ninth kernel sums the partials (tiny: 2 items, 70b: 64)
-    assert bench.kv_segments(wl.WORKLOADS["tiny"]) == 8
-    assert bench.kv_segments(wl.WORKLOADS["70b"]) == 4
-    assert bench.kv_segments(wl.WORKLOADS["8b"]) == 1
-    for name in ["tiny", "70b"]:
-        assert bench.kernels_per_rank_step(wl.WORKLOADS[name]) == 9
-    # launch orders over 2048 units take one extra ranking kernel each: the
-    # 128K single-rank workload has 16384 query tiles of 8 positions (and
-    # 1024 key tiles: no split)
+    # launch orders over 2048 units take one extra ranking kernel each, and
+    # over 2048 key tiles one more for the uncut dK/dV work list: the 128K
+    # single-rank workload has 16384 query tiles of 8 positions (and 1024 key
+    # tiles)
     assert bench.kernels_per_rank_step(wl.WORKLOADS["causal-128k"]) == 9
     rows = wl.custom("rows", 32768, 1, 1, 16, 1, 64, "uniform", 64, 4096, seed=14)
     both = wl.custom("both", 16384, 1, 17, 2, 2, 64, "uniform", 64, 4096, seed=15)
     assert bench.kernels_per_rank_step(rows) == 9
-    assert bench.kernels_per_rank_step(both) == 10
+    assert bench.kernels_per_rank_step(both) == 11
 
 
 def test_source_hash_ignores_comments():

@@ -96,6 +96,37 @@ def test_plan_bit_exact(name, w, rank):
         assert np.array_equal((got >> 31) == 1, cls[b, lst, kt] == ob.PARTIAL)
     _check_order(a["fwd_order"].numpy(), [len(x) for x in rows])
     _check_order(a["bwd_order"].numpy(), [len(x) for x in cols])
+    _check_kv_work_list(a, [len(x) for x in cols], w)
+
+
+def _check_kv_work_list(a, lengths, w):
+    """The dK/dV work list: every unit's column list covered exactly once by
+    its slices, and the slices, cuts and pool slots equal to the host mirror
+    of the planner's rule (balance.kv_work_list) for this device's SMs."""
+    from document_masked_gqa_gb300 import balance
+    cp_ = a["col_ptr"].numpy()
+    sl = a["kv_slices"].numpy()
+    sp = a["kv_splits"].numpy()
+    covered = {}
+    for unit, first, n, seg, split, slot, z0, z1 in sl:
+        assert z0 == 0 and z1 == 0
+        covered.setdefault(int(unit), []).append((int(first) - int(cp_[unit]), int(n)))
+    assert sorted(covered) == list(range(len(lengths)))
+    for unit, parts in covered.items():
+        parts.sort()
+        pos = 0
+        for first, n in parts:
+            assert first == pos
+            pos += n
+        assert pos == lengths[unit]
+    nqt = a["tile_class"].shape[1]
+    assert a["kv_pool_slots"] == balance.kv_pool_slots(w.batch, w.seq_len, w.n_kv_heads, nqt)
+    want = balance.kv_work_list(lengths, w.n_kv_heads, a["n_sms"], a["kv_pool_slots"])
+    got = [(int(u), int(f) - int(cp_[u]), int(n), int(sg), int(spl), int(slot))
+           for u, f, n, sg, spl, slot, _, _ in sl]
+    assert got == want["slices"]
+    assert [tuple(int(x) for x in row[:3]) for row in sp] == want["splits"]
+    assert all(row[3] == 0 for row in sp)
 
 
 @pytest.mark.parametrize("name", ["tiny", "70b", "sparse"])
