@@ -169,11 +169,12 @@ dma_status dma_attn_bwd(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
  *   dma_attn_bwd_delta: Delta alone (a pass over o and dout of its own).
  *   dma_attn_bwd_dq   : dq from the Delta already in the workspace.
  *   dma_attn_bwd_dkdv : dk, dv (fp32, fully overwritten) from q, k, v, lse,
- *                       dout and the workspace's Delta; with fewer than 256
- *                       (key tile, K/V head) pairs each key tile's query list
- *                       is split over several work items whose fp32 partials
- *                       (in the workspace) a second kernel adds in a fixed
- *                       order.
+ *                       dout and the workspace's Delta, in one kernel.  The
+ *                       query lists of key tiles that the plan cut into
+ *                       segments (see kv_slices in dma_plan_view) leave fp32
+ *                       partials in the workspace, which the same kernel
+ *                       adds into dk, dv in segment order (the same on
+ *                       every run).
  * Delta must be in place (dq_delta or delta) before dq or dkdv runs.
  */
 dma_status dma_attn_bwd_dq_delta(dma_plan_t plan, const dma_bf16* q, const dma_bf16* k,
