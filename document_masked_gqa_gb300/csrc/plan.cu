@@ -185,11 +185,37 @@ __device__ T block_max(T v, T* s_tmp) {
   return r;
 }
 
+// Block-wide sums of K ints per thread: s_red [32 K] scratch, out [K];
+// every thread may read out[] on return.
+template <int K>
+__device__ void block_sum(const int (&v)[K], int* s_red, int* out) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int q = 0; q < K; ++q) {
+    int x = v[q];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) s_red[wid * K + q] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < K) {
+    int t = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += s_red[w * K + threadIdx.x];
+    out[threadIdx.x] = t;
+  }
+  __syncthreads();
+}
+
 // Sorts s_key[0, npow) ascending (npow a power of two) with a bitonic
-// network; the whole block takes part.
+// network; the whole block takes part.  The steps with a partner distance of
+// 32 or more exchange through shared memory, one barrier each; the
+// distances below 32 stay within a warp's 32 consecutive keys and run in
+// registers with shuffles (a warp's keys all lie below npow or all above it,
+// npow >= 32 and blockDim.x a multiple of 32).
 __device__ void bitonic_sort(unsigned long long* s_key, int npow) {
   for (int k = 2; k <= npow; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
+    int j = k >> 1;
+    for (; j > 0 && (j >= 32 || npow < 32); j >>= 1) {
       for (int i = threadIdx.x; i < npow; i += blockDim.x) {
         const int ixj = i ^ j;
         if (ixj > i) {
@@ -202,6 +228,19 @@ __device__ void bitonic_sort(unsigned long long* s_key, int npow) {
       }
       __syncthreads();
     }
+    if (j == 0) continue;
+    for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+      unsigned long long v = s_key[i];
+      const bool asc = (i & k) == 0;
+      for (int jj = j; jj > 0; jj >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, jj);
+        // the lower index of a pair keeps the smaller key when ascending
+        const bool keep_min = ((i & jj) == 0) == asc;
+        v = keep_min ? (o < v ? o : v) : (o > v ? o : v);
+      }
+      s_key[i] = v;
+    }
+    __syncthreads();
   }
 }
 
@@ -235,7 +274,7 @@ __device__ __forceinline__ void put_slice(const PlanDev& p, int at, int unit, in
 // The comparisons run exactly in integers: P E_o against the ratios' numerators
 // and denominators times P m = Hkv sum(c).
 __device__ void plan_dkdv_slices(const PlanDev& p, unsigned long long* s_key, int n, int npow,
-                                 int* s_tmp, long long* s_ll) {
+                                 int* s_tmp, long long* s_ll, int* s_red) {
   const long long Hkv = p.n_kv_heads, P = p.n_sms > 0 ? p.n_sms : 1;
   // thread t holds launch positions 2t and 2t + 1
   const int o0 = 2 * static_cast<int>(threadIdx.x);
@@ -263,21 +302,43 @@ __device__ void plan_dkdv_slices(const PlanDev& p, unsigned long long* s_key, in
     const int c_first = key_count(s_key[0]);
     L = key_count(s_key[o_star]);
     if (L < kSegMin) L = kSegMin;
-    // L grows by at least an eighth per round (a few hundred rounds reach
-    // any list length); no cut unless the pool holds the segments
+    // L grows by at least an eighth per step (a few hundred steps reach any
+    // list length) until the pool holds the segments, else no cut; each
+    // round of the search tries the next kCand lengths of that sequence
+    constexpr int kCand = 8;
     bool fits = false;
-    for (int round = 0; round < 4096 && L < c_first; ++round) {
-      int need = 0;
+    for (int round = 0; round < 512 && !fits && L < c_first; ++round) {
+      int cand[kCand], need[kCand];
+      int x = L;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-        if (c[j] > L) need += (c[j] + L - 1) / L - 1;
-      int total;
-      (void)block_exclusive_scan(need, s_tmp, &total);
-      if (total <= p.kv_cap) {
-        fits = true;
-        break;
+      for (int q = 0; q < kCand; ++q) {
+        cand[q] = x;
+        need[q] = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          if (c[j] > x) need[q] += (c[j] + x - 1) / x - 1;
+        x += x / 8 > 1 ? x / 8 : 1;
       }
-      L += L / 8 > 1 ? L / 8 : 1;
+      block_sum<kCand>(need, s_red, s_red + 32 * kCand);
+      const int* total = s_red + 32 * kCand;
+      // stop at the first candidate that reaches the longest list (no cut)
+      // or whose segments the pool holds
+      int next = x;
+      bool stop = false;
+#pragma unroll
+      for (int q = 0; q < kCand; ++q) {
+        if (stop) continue;
+        if (cand[q] >= c_first) {
+          stop = true;
+          next = cand[q];
+        } else if (total[q] <= p.kv_cap) {
+          stop = true;
+          fits = true;
+          next = cand[q];
+        }
+      }
+      __syncthreads();  // every thread has read the totals before the next round
+      L = next;
     }
     if (!fits) L = 0x7FFFFFFF;
   }
@@ -367,6 +428,7 @@ __device__ void plan_dkdv_slices(const PlanDev& p, unsigned long long* s_key, in
 __global__ void scan_order_kernel(PlanDev p) {
   __shared__ int s_tmp[32];
   __shared__ long long s_ll[32];
+  __shared__ int s_red[33 * 8];
   __shared__ unsigned long long s_key[kSortMax];
   {
     const int which = blockIdx.x;
@@ -404,7 +466,7 @@ __global__ void scan_order_kernel(PlanDev p) {
     for (int i = threadIdx.x; i < n; i += blockDim.x)
       order[i] = static_cast<int32_t>(s_key[i] & 0xFFFFFFFFull);
     __syncthreads();
-    if (which == 1) plan_dkdv_slices(p, s_key, n, npow, s_tmp, s_ll);
+    if (which == 1) plan_dkdv_slices(p, s_key, n, npow, s_tmp, s_ll, s_red);
   }
 }
 
