@@ -347,9 +347,9 @@ def fit_costs(features, times_ms) -> np.ndarray:
 
 # Constants fitted (fit_costs) to the measured per-rank step times of the
 # 8B, 70B, sparse-stress and both 405B workloads on one GB300 (152 SMs), with
-# the kernels' dynamic work distribution: ms per tile pair of makespan, per
-# partial pair, per work item, fixed.
-COST_MS_GB300 = np.array([1.27084e-03, 0.0, 1.97947e-06, 1.13610e-01])
+# the kernels' dynamic work distribution and the planner's cut dK/dV lists:
+# ms per tile pair of makespan, per partial pair, per work item, fixed.
+COST_MS_GB300 = np.array([1.25330e-03, 5.51287e-07, 0.0, 1.28789e-01])
 
 
 def predict_ms(features, coef=None) -> np.ndarray:
