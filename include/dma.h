@@ -100,6 +100,11 @@ typedef struct dma_plan_s* dma_plan_t;
  * Bytes of device workspace dma_plan needs for this shape (256-byte aligned
  * base required).  Returns 0 for an unsupported or invalid shape.
  * max_docs is accepted for interface stability and does not change the size.
+ * The last part of the layout is the backward's pool of fp32 partial dK, dV
+ * for cut query lists: 2 x kv_pool_slots x 128 x n_kv_heads x head_dim x 4
+ * bytes (kv_pool_slots: max(batch * n_ktiles, min(ceil(512 / n_kv_heads),
+ * what the lists could use)); see dma_plan_view).  The allocation-free
+ * forward needs only the part before it.
  */
 size_t dma_plan_workspace_bytes(int batch, int seq_len, int cp_size,
                                 int n_heads, int n_kv_heads, int head_dim,
@@ -314,8 +319,9 @@ dma_status dma_debug_wait_probe(uint64_t timeout_ns, uint32_t* status_dev,
  * 64 MiB array compiled into the library; the caller passes only inputs and
  * outputs.
  *   - Every GPU that loads the library holds the 64 MiB until the process
- *     exits.  Shapes whose scratch exceeds it return DMA_ERR_WORKSPACE
- *     (dma_plan_workspace_bytes gives the size a shape needs).
+ *     exits.  Shapes whose scratch exceeds it return DMA_ERR_WORKSPACE (the
+ *     scratch is dma_plan_workspace_bytes less the backward's pool of
+ *     partials described there).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call outside any stream capture.
  *     Only a successful lookup is kept (a failed one returns DMA_ERR_CUDA and
