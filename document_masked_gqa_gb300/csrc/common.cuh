@@ -44,8 +44,8 @@ __host__ __device__ inline int kv_pool_slots(int batch, int seq_len, int n_kv_he
 
 // int32 words at kSchedOffset: the forward's work counters (next item, CTAs
 // exited), the dK/dV kernel's, the number of dK/dV list slices and of split
-// units (written by the planner), and the dK/dV kernel's counter of split
-// units taken for their final sum
+// units (written by the planner), and the dK/dV kernel's counter of the
+// (split unit, row chunk) sums taken
 constexpr int kSchedFwd = 0, kSchedDkdv = 2, kSchedSlices = 4, kSchedSplits = 5, kSchedTail = 6;
 // bytes at the start of the workspace: status words [0, 16), the words above [32, 64)
 constexpr int kStatusBytes = 64, kSchedOffset = 32;
