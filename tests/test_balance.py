@@ -228,3 +228,39 @@ def test_kv_work_list_on_the_workloads(name, cut):
                                 balance.kv_pool_slots(w.batch, w.seq_len, w.n_kv_heads, nqt))
     assert (work["L"] is not None) == cut
     _slices_cover(work, c["col_counts"].tolist())
+
+
+def _greedy_makespan(lengths, sms):
+    """Each item, in order, on the SM that frees first (the dK/dV kernel's
+    work counter); the busiest SM's total."""
+    import heapq
+    free = [0] * sms
+    for n in lengths:
+        t = heapq.heappop(free)
+        heapq.heappush(free, t + n)
+    return max(free)
+
+
+@pytest.mark.parametrize("name", ["70b", "sparse", "405b-logu"])
+def test_kv_work_list_shortens_the_greedy_makespan(name):
+    """On every rank whose lists the rule cuts, greedy scheduling of the cut
+    list over 152 SMs ends no later than that of the uncut list.  It also
+    stays within the list-scheduling bound of the mean plus the longest
+    slice (at most L).  On the 405B shape, where the lists are long against
+    the floor of 16 tiles, it ends within 1.1 x the mean, the rule's target."""
+    w = wl.WORKLOADS[name]
+    cu = wl.cu_doc_lens(w)
+    nqt = (w.seq_len // w.cp_size) // (128 // w.group)
+    cap = balance.kv_pool_slots(w.batch, w.seq_len, w.n_kv_heads, nqt)
+    for r in w.ranks:
+        counts = balance.tile_counts(cu, w.batch, w.seq_len, w.cp_size, r, w.group)["col_counts"]
+        cut = balance.kv_work_list(counts, w.n_kv_heads, 152, cap)
+        whole = balance.kv_work_list(counts, w.n_kv_heads, 152, 0)
+        assert cut["L"] is not None and whole["L"] is None
+        items = lambda work: [s[2] for s in work["slices"] for _ in range(w.n_kv_heads)]
+        m = sum(items(cut)) / 152
+        t_cut, t_whole = _greedy_makespan(items(cut), 152), _greedy_makespan(items(whole), 152)
+        assert t_cut <= t_whole, (name, r)
+        assert t_cut <= m + cut["L"], (name, r)
+        if name.startswith("405b"):
+            assert t_cut <= 1.1 * m, (name, r, t_cut / m)
